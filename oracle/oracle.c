@@ -1,0 +1,283 @@
+/*
+ * oracle.c -- TEST INFRASTRUCTURE ONLY.  A plain, slow CPU restatement of the
+ * frame-locked batched decode step, used to check the CUDA library.  Only the
+ * tests, __graft_entry__.smoke() and bench.py's CPU-baseline leg may load it.
+ * It shares no code, header, table or helper with the CUDA path.
+ *
+ * What it computes follows the pages' description of the frame step:
+ *   - "PersonaPlex 7B, 80 sessions, one H100" (narilabs blog), sections
+ *     "What Real-time Means for a Full-duplex Agent" (one 80 ms frame per
+ *     forward pass), "Compressing the Temporal KV cache" (bf16 weights and
+ *     activations, FP8 temporal K/V cache) and "A server built around the
+ *     conversation clock" (every session advances together, fixed shape);
+ *   - the dotwave.ai case study, "02 / The solution" and "04 / Under the
+ *     hood" (weights shared across sessions, state kept between beats).
+ * The pages give no layer-level definition; the decoder layer (RMSNorm, QKV,
+ * RoPE, FP8 K/V append, attention, output projection, SwiGLU MLP) and its
+ * shapes come from the workload definition, and every point the pages leave
+ * open is taken at its plainest reading (listed in the design notes):
+ *   rounding to bf16 only at the projection inputs (normed x, attention
+ *   output, SwiGLU output) and at y; rotate-half RoPE with pairs (i, i+D/2);
+ *   softmax scale 1/sqrt(D) over slots 0..pos inclusive; no biases, no GQA,
+ *   no final norm or LM head; FP8 scale amax/448 per (session, layer, K|V,
+ *   head, token), quantised by fp32 division.
+ * Arithmetic is fp64 everywhere except the FP8 quantiser, which is the fp32
+ * definition itself.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+  int n_layers, d_model, n_heads, head_dim, ffn;
+  float rms_eps, rope_base;
+} oracle_cfg;
+
+/* ------------------------------------------------------------------ bf16 */
+double oracle_bf16_to_double(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* Round a double to the nearest bfloat16 (8 significant bits, ties to even),
+ * straight from the double (no intermediate fp32 rounding). */
+uint16_t oracle_double_to_bf16(double x) {
+  if (isnan(x)) return 0x7FC0;
+  uint16_t sign = signbit(x) ? 0x8000 : 0;
+  double a = fabs(x);
+  if (a == 0.0) return sign;
+  int ex;
+  frexp(a, &ex); /* a = m * 2^ex, m in [0.5, 1) */
+  int e = ex - 1;  /* a in [2^e, 2^(e+1)) */
+  int ulp_e = (e < -126) ? -133 : e - 7;
+  double q = ldexp(a, -ulp_e);
+  double r = nearbyint(q); /* default rounding mode: to nearest, ties to even */
+  double v = ldexp(r, ulp_e);
+  if (v >= ldexp(1.0, 128)) return sign | 0x7F80;
+  float f = (float)v; /* exact: v has at most 8 significant bits */
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return (uint16_t)(sign | ((u >> 16) & 0x7FFF));
+}
+
+double oracle_bf16_round(double x) { return oracle_bf16_to_double(oracle_double_to_bf16(x)); }
+
+/* -------------------------------------------------------------- FP8 E4M3 */
+/* OCP 8-bit floating point, E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa
+ * bits; no infinities; S.1111.111 is NaN; largest finite magnitude 448. */
+double oracle_e4m3_decode(uint8_t c) {
+  int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  double v = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+/* Nearest of the 127 finite non-negative magnitudes (codes 0x00..0x7E, which
+ * increase with the code), ties to the code whose last bit is 0; magnitudes at
+ * or beyond 448 saturate to 448; the sign bit is kept (so -0 and negative
+ * underflow give 0x80). */
+uint8_t oracle_e4m3_encode(float v) {
+  if (isnan(v)) return 0x7F;
+  uint8_t sign = signbit(v) ? 0x80 : 0;
+  double a = fabs((double)v);
+  if (a >= 448.0) return sign | 0x7E;
+  int lo = 0, hi = 0x7E; /* largest code with decode(code) <= a */
+  while (lo < hi) {
+    int mid = (lo + hi + 1) / 2;
+    if (oracle_e4m3_decode((uint8_t)mid) <= a) lo = mid; else hi = mid - 1;
+  }
+  int c = lo;
+  if (c < 0x7E) {
+    double d0 = a - oracle_e4m3_decode((uint8_t)c);
+    double d1 = oracle_e4m3_decode((uint8_t)(c + 1)) - a;
+    if (d1 < d0 || (d1 == d0 && ((c + 1) & 1) == 0)) c = c + 1;
+  }
+  return sign | (uint8_t)c;
+}
+
+void oracle_e4m3_encode_many(const float* v, int64_t n, uint8_t* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(v[i]);
+}
+
+/* Per-row FP8 quantiser: amax over the row, scale = amax / 448 (fp32), code =
+ * E4M3(v / scale) with the division in fp32.  A zero scale gives all-zero
+ * codes and a stored scale of 0. */
+void oracle_quantize_row(const float* v, int D, uint8_t* codes, float* scale) {
+  float amax = 0.0f;
+  for (int i = 0; i < D; ++i) {
+    float a = fabsf(v[i]);
+    if (a > amax) amax = a;
+  }
+  float s = amax / 448.0f;
+  *scale = s;
+  for (int i = 0; i < D; ++i) codes[i] = (s == 0.0f) ? 0 : oracle_e4m3_encode(v[i] / s);
+}
+
+void oracle_quantize_rows(const float* v, int64_t rows, int D, uint8_t* codes, float* scales) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    oracle_quantize_row(v + r * D, D, codes + r * D, scales + r);
+}
+
+/* ------------------------------------------------------------ layer parts */
+/* out = r / sqrt(mean(r^2) + eps) * g */
+void oracle_rmsnorm(const double* r, const uint16_t* g, int d, double eps, double* out) {
+  double ss = 0.0;
+  for (int i = 0; i < d; ++i) ss += r[i] * r[i];
+  double inv = 1.0 / sqrt(ss / d + eps);
+  for (int i = 0; i < d; ++i) out[i] = r[i] * inv * oracle_bf16_to_double(g[i]);
+}
+
+/* y[n] = sum_k W[n][k] * x[k], W stored [N][K] in bf16. */
+void oracle_matvec(const uint16_t* W, int N, int K, const double* x, double* y) {
+#pragma omp parallel for schedule(static)
+  for (int n = 0; n < N; ++n) {
+    const uint16_t* w = W + (int64_t)n * K;
+    double acc = 0.0;
+    for (int k = 0; k < K; ++k) acc += oracle_bf16_to_double(w[k]) * x[k];
+    y[n] = acc;
+  }
+}
+
+/* Rotate-half RoPE on one head vector: pairs (i, i + D/2), angle pos * theta_i,
+ * theta_i = base^(-2i/D). */
+void oracle_rope(double* v, int D, int pos, double base) {
+  int half = D / 2;
+  for (int i = 0; i < half; ++i) {
+    double theta = pow(base, -2.0 * i / D);
+    double ang = (double)pos * theta;
+    double c = cos(ang), s = sin(ang);
+    double a = v[i], b = v[i + half];
+    v[i] = a * c - b * s;
+    v[i + half] = a * s + b * c;
+  }
+}
+
+/* Attention of one head over cache slots 0..pos inclusive:
+ * score_t = (q . dec(kc_t)) * ks_t / sqrt(D); p = softmax(score);
+ * o = sum_t p_t * vs_t * dec(vc_t).  kc/vc are [T][D] codes, ks/vs [T]. */
+void oracle_attention_head(const double* q, const uint8_t* kc, const float* ks,
+                           const uint8_t* vc, const float* vs, int pos, int D, double* o) {
+  int n = pos + 1;
+  double* sc = (double*)malloc(sizeof(double) * (size_t)n);
+  double m = -INFINITY;
+  for (int t = 0; t < n; ++t) {
+    double dot = 0.0;
+    for (int i = 0; i < D; ++i) dot += q[i] * oracle_e4m3_decode(kc[(int64_t)t * D + i]);
+    sc[t] = dot * (double)ks[t] / sqrt((double)D);
+    if (sc[t] > m) m = sc[t];
+  }
+  double l = 0.0;
+  for (int i = 0; i < D; ++i) o[i] = 0.0;
+  for (int t = 0; t < n; ++t) {
+    double p = exp(sc[t] - m);
+    l += p;
+    double w = p * (double)vs[t];
+    for (int i = 0; i < D; ++i) o[i] += w * oracle_e4m3_decode(vc[(int64_t)t * D + i]);
+  }
+  for (int i = 0; i < D; ++i) o[i] /= l;
+  free(sc);
+}
+
+double oracle_silu(double g) { return g / (1.0 + exp(-g)); }
+
+/* ------------------------------------------------------------- the step */
+static int64_t layer_elems(const oracle_cfg* c) {
+  int64_t d = c->d_model, HD = (int64_t)c->n_heads * c->head_dim, F = c->ffn;
+  return d + 3 * HD * d + d * HD + d + 2 * F * d + d * F;
+}
+
+/*
+ * One frame for n independent sessions.  kv is [L][2][n][H][T_max][D] codes,
+ * kv_scales [L][2][n][H][T_max]; both are read at slots 0..pos[s]-1 and slot
+ * pos[s] is written (then read back quantised).  x, y are [n][d] bf16.
+ * y_exact (nullable) receives the fp64 residual before the final rounding;
+ * kv_new (nullable) receives the fp32 K/V values that were quantised,
+ * [L][2][n][H][D].  round_acts = 0 skips the bf16 rounding of activations
+ * (an fp64 "pure" variant, for information).  Returns 0, or -(s+1) for the
+ * first session whose position is outside [0, T_max).
+ */
+int oracle_step(const oracle_cfg* c, int T_max, const uint16_t* weights, int n, uint8_t* kv,
+                float* kv_scales, const int32_t* pos, const uint16_t* x, uint16_t* y,
+                double* y_exact, int round_acts, float* kv_new) {
+  const int L = c->n_layers, d = c->d_model, H = c->n_heads, D = c->head_dim, F = c->ffn;
+  const int HD = H * D;
+  const int64_t le = layer_elems(c);
+  for (int s = 0; s < n; ++s)
+    if (pos[s] < 0 || pos[s] >= T_max) return -(s + 1);
+
+  double* r = (double*)malloc(sizeof(double) * d);
+  double* xn = (double*)malloc(sizeof(double) * d);
+  double* qkv = (double*)malloc(sizeof(double) * 3 * HD);
+  double* att = (double*)malloc(sizeof(double) * HD);
+  double* tmp = (double*)malloc(sizeof(double) * (d > 2 * F ? d : 2 * F));
+  double* u = (double*)malloc(sizeof(double) * F);
+  float* row = (float*)malloc(sizeof(float) * D);
+
+  for (int s = 0; s < n; ++s) {
+    const int P = pos[s];
+    for (int i = 0; i < d; ++i) r[i] = oracle_bf16_to_double(x[(int64_t)s * d + i]);
+    for (int l = 0; l < L; ++l) {
+      const uint16_t* Wl = weights + (int64_t)l * le;
+      const uint16_t* g_attn = Wl;
+      const uint16_t* wqkv = g_attn + d;
+      const uint16_t* wo = wqkv + (int64_t)3 * HD * d;
+      const uint16_t* g_mlp = wo + (int64_t)d * HD;
+      const uint16_t* wgu = g_mlp + d;
+      const uint16_t* wdown = wgu + (int64_t)2 * F * d;
+
+      /* attention block */
+      oracle_rmsnorm(r, g_attn, d, c->rms_eps, xn);
+      if (round_acts) for (int i = 0; i < d; ++i) xn[i] = oracle_bf16_round(xn[i]);
+      oracle_matvec(wqkv, 3 * HD, d, xn, qkv);
+      double* q = qkv;
+      double* k = qkv + HD;
+      double* v = qkv + 2 * HD;
+      for (int h = 0; h < H; ++h) {
+        oracle_rope(q + h * D, D, P, c->rope_base);
+        oracle_rope(k + h * D, D, P, c->rope_base);
+      }
+      for (int which = 0; which < 2; ++which) {
+        const double* src = which ? v : k;
+        for (int h = 0; h < H; ++h) {
+          int64_t sh = (((int64_t)l * 2 + which) * n + s) * H + h;
+          for (int i = 0; i < D; ++i) row[i] = (float)src[h * D + i];
+          if (kv_new)
+            memcpy(kv_new + ((((int64_t)l * 2 + which) * n + s) * H + h) * D, row, sizeof(float) * D);
+          oracle_quantize_row(row, D, kv + (sh * T_max + P) * D, kv_scales + sh * T_max + P);
+        }
+      }
+#pragma omp parallel for schedule(static)
+      for (int h = 0; h < H; ++h) {
+        int64_t shk = (((int64_t)l * 2 + 0) * n + s) * H + h;
+        int64_t shv = (((int64_t)l * 2 + 1) * n + s) * H + h;
+        oracle_attention_head(q + h * D, kv + shk * T_max * D, kv_scales + shk * T_max,
+                              kv + shv * T_max * D, kv_scales + shv * T_max, P, D, att + h * D);
+      }
+      if (round_acts) for (int i = 0; i < HD; ++i) att[i] = oracle_bf16_round(att[i]);
+      oracle_matvec(wo, d, HD, att, tmp);
+      for (int i = 0; i < d; ++i) r[i] += tmp[i];
+
+      /* MLP block */
+      oracle_rmsnorm(r, g_mlp, d, c->rms_eps, xn);
+      if (round_acts) for (int i = 0; i < d; ++i) xn[i] = oracle_bf16_round(xn[i]);
+      oracle_matvec(wgu, 2 * F, d, xn, tmp);
+      for (int i = 0; i < F; ++i) {
+        u[i] = oracle_silu(tmp[i]) * tmp[F + i];
+        if (round_acts) u[i] = oracle_bf16_round(u[i]);
+      }
+      oracle_matvec(wdown, d, F, u, tmp);
+      for (int i = 0; i < d; ++i) r[i] += tmp[i];
+    }
+    for (int i = 0; i < d; ++i) {
+      y[(int64_t)s * d + i] = oracle_double_to_bf16(r[i]);
+      if (y_exact) y_exact[(int64_t)s * d + i] = r[i];
+    }
+  }
+  free(r); free(xn); free(qkv); free(att); free(tmp); free(u); free(row);
+  return 0;
+}
