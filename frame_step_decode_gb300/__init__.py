@@ -1,0 +1,180 @@
+"""Python binding of libwave.so (include/wave.h): argument marshalling only.
+
+Every step of the frame runs in the library's CUDA kernels; PyTorch is used
+only to own device memory and streams.  There is no fallback: if the library
+is not built, importing the binding's entry points raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libwave.so")
+
+WAVE_OK, WAVE_EINVAL, WAVE_ECUDA, WAVE_ELAUNCH = 0, -1, -2, -3
+WAVE_ETIMEOUT, WAVE_EPOS, WAVE_EDEVICE, WAVE_ENOMEM = -4, -5, -6, -7
+
+
+class WaveConfig(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("d_model", ctypes.c_int), ("n_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("ffn", ctypes.c_int), ("rms_eps", ctypes.c_float),
+                ("rope_base", ctypes.c_float)]
+
+    @classmethod
+    def of(cls, w) -> "WaveConfig":
+        """From any object with the decoder-shape attributes."""
+        return cls(w.n_layers, w.d_model, w.n_heads, w.head_dim, w.ffn, w.rms_eps, w.rope_base)
+
+
+class WaveError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+        self.code = code
+
+
+_lib = None
+EXPORTS = ("wave_create", "wave_destroy", "wave_weights_bytes", "wave_weight_offset", "wave_step",
+           "wave_status", "wave_strerror", "wave_kv_quantize", "wave_fp8_encode",
+           "wave_set_timeout_ns", "wave_debug_skip_barrier", "wave_debug_dump_kv", "wave_grid_size",
+           "wave_barriers_per_step")
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built: run frame_step_decode_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        cfgp = ctypes.POINTER(WaveConfig)
+        L.wave_create.argtypes = [cfgp, i32, i32, ctypes.POINTER(vp)]
+        L.wave_create.restype = i32
+        L.wave_destroy.argtypes = [vp]
+        L.wave_destroy.restype = None
+        L.wave_weights_bytes.argtypes = [cfgp]
+        L.wave_weights_bytes.restype = sz
+        L.wave_weight_offset.argtypes = [cfgp, i32, i32]
+        L.wave_weight_offset.restype = sz
+        L.wave_step.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
+        L.wave_step.restype = i32
+        L.wave_status.argtypes = [vp]
+        L.wave_status.restype = i32
+        L.wave_strerror.argtypes = [i32]
+        L.wave_strerror.restype = ctypes.c_char_p
+        L.wave_kv_quantize.argtypes = [vp, i64, i32, vp, vp, vp]
+        L.wave_kv_quantize.restype = i32
+        L.wave_fp8_encode.argtypes = [vp, i64, vp, vp]
+        L.wave_fp8_encode.restype = i32
+        L.wave_set_timeout_ns.argtypes = [vp, ctypes.c_longlong]
+        L.wave_set_timeout_ns.restype = i32
+        L.wave_debug_skip_barrier.argtypes = [vp, i32, i32]
+        L.wave_debug_skip_barrier.restype = i32
+        L.wave_debug_dump_kv.argtypes = [vp, vp]
+        L.wave_debug_dump_kv.restype = i32
+        L.wave_grid_size.argtypes = [vp]
+        L.wave_grid_size.restype = i32
+        L.wave_barriers_per_step.argtypes = [vp]
+        L.wave_barriers_per_step.restype = i32
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().wave_strerror(code).decode()
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def weights_bytes(cfg: WaveConfig) -> int:
+    return lib().wave_weights_bytes(ctypes.byref(cfg))
+
+
+def weight_offset(cfg: WaveConfig, layer: int, which: int) -> int:
+    return lib().wave_weight_offset(ctypes.byref(cfg), layer, which)
+
+
+class Wave:
+    """A step context: wave_create / wave_step / wave_status / wave_destroy."""
+
+    def __init__(self, cfg: WaveConfig, S_max: int, T_max: int):
+        self.cfg = cfg
+        self.S_max, self.T_max = S_max, T_max
+        h = ctypes.c_void_p()
+        rc = lib().wave_create(ctypes.byref(cfg), S_max, T_max, ctypes.byref(h))
+        if rc != WAVE_OK:
+            raise WaveError(rc, "wave_create")
+        self.h = h
+
+    def step(self, S, weights, kv, kv_scales, positions, x, y, stream=None, check=True) -> int:
+        rc = lib().wave_step(self.h, S, _ptr(weights), _ptr(kv), _ptr(kv_scales), _ptr(positions),
+                             _ptr(x), _ptr(y), _stream(stream))
+        if check and rc != WAVE_OK:
+            raise WaveError(rc, "wave_step")
+        return rc
+
+    def status(self) -> int:
+        return lib().wave_status(self.h)
+
+    def set_timeout_ns(self, ns: int) -> None:
+        rc = lib().wave_set_timeout_ns(self.h, ns)
+        if rc != WAVE_OK:
+            raise WaveError(rc, "wave_set_timeout_ns")
+
+    def debug_skip_barrier(self, cta: int, barrier: int) -> None:
+        lib().wave_debug_skip_barrier(self.h, cta, barrier)
+
+    def debug_dump_kv(self, dst) -> None:
+        """Testing hook: later steps write their pre-quantisation K/V rows
+        into dst ([L][2][S_max][H][D] fp32 on the device); None disables."""
+        lib().wave_debug_dump_kv(self.h, _ptr(dst))
+
+    @property
+    def grid(self) -> int:
+        return lib().wave_grid_size(self.h)
+
+    @property
+    def barriers_per_step(self) -> int:
+        return lib().wave_barriers_per_step(self.h)
+
+    def close(self) -> None:
+        if getattr(self, "h", None):
+            lib().wave_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def kv_quantize(v, codes, scales, stream=None) -> None:
+    """FP8 quantiser of the K/V append on rows of v (last dim D)."""
+    D = v.shape[-1]
+    rows = v.numel() // D
+    rc = lib().wave_kv_quantize(_ptr(v), rows, D, _ptr(codes), _ptr(scales), _stream(stream))
+    if rc != WAVE_OK:
+        raise WaveError(rc, "wave_kv_quantize")
+
+
+def fp8_encode(inp, out, stream=None, n: int | None = None) -> None:
+    n = inp.numel() if n is None else n
+    rc = lib().wave_fp8_encode(_ptr(inp), n, _ptr(out), _stream(stream))
+    if rc != WAVE_OK:
+        raise WaveError(rc, "wave_fp8_encode")

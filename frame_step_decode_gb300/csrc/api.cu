@@ -1,0 +1,433 @@
+// api.cu -- host side of the C ABI in include/wave.h: argument checks,
+// workspace ownership, TMA tensor-map encoding and the single cooperative
+// launch per frame.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <vector>
+
+#include "../../include/wave.h"
+#include "internal.h"
+
+using namespace wave;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct wave_ctx {
+  wave_config cfg;
+  int S_max, S_pad_max, T_max, device, grid;
+  long long layer_elems, off[6];
+  int tiles[4], kblocks[4], max_tiles_per_cta;
+  // workspace
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  float* resid;
+  uint16_t *xn, *attn, *u;
+  float* qkv;
+  float* gemm_part;
+  int* tile_cnt;
+  float* att_part;
+  int* sh_cnt;
+  int4* pieces;
+  int* n_pieces;
+  float2* rope;
+  unsigned* bar;
+  int* err;
+  // cached tensor maps
+  CUtensorMap tm_w[4], tm_x[4], tm_kv;
+  const void* maps_weights = nullptr;
+  const void* maps_kv = nullptr;
+  int maps_S = -1;
+  cudaStream_t last_stream = nullptr;
+  long long timeout_ns = 2000000000LL;
+  int skip_cta = -1, skip_bar = -1;
+  float* kv_dump = nullptr;
+};
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)p;
+  }
+  return fn;
+}
+
+static bool shape_ok(const wave_config* c) {
+  if (!c) return false;
+  if (c->n_layers < 1 || c->n_layers > 1024) return false;
+  if (c->head_dim != 64 && c->head_dim != 128) return false;
+  if (c->n_heads < 1 || c->d_model < 64 || c->d_model % 64) return false;
+  if ((c->n_heads * c->head_dim) % 64) return false;
+  if (c->ffn < 8 || c->ffn % 8) return false;
+  if (!(c->rms_eps >= 0.f) || !(c->rope_base > 0.f)) return false;
+  return true;
+}
+
+static void layout_offsets(const wave_config* c, long long* off, long long* layer_elems) {
+  const long long d = c->d_model, HD = (long long)c->n_heads * c->head_dim, F = c->ffn;
+  const long long n[6] = {d, 3 * HD * d, d * HD, d, 2 * F * d, d * F};
+  long long o = 0;
+  for (int i = 0; i < 6; ++i) {
+    off[i] = o;
+    o += n[i];
+  }
+  *layer_elems = o;
+}
+
+extern "C" size_t wave_weights_bytes(const wave_config* cfg) {
+  if (!shape_ok(cfg)) return 0;
+  long long off[6], le;
+  layout_offsets(cfg, off, &le);
+  return (size_t)(le * cfg->n_layers * 2);
+}
+
+extern "C" size_t wave_weight_offset(const wave_config* cfg, int layer, int which) {
+  if (!shape_ok(cfg) || layer < 0 || layer >= cfg->n_layers || which < 0 || which > 5)
+    return (size_t)-1;
+  long long off[6], le;
+  layout_offsets(cfg, off, &le);
+  return (size_t)((le * layer + off[which]) * 2);
+}
+
+extern "C" const char* wave_strerror(int code) {
+  switch (code) {
+    case WAVE_OK: return "ok";
+    case WAVE_EINVAL: return "invalid argument";
+    case WAVE_ECUDA: return "CUDA call failed";
+    case WAVE_ELAUNCH: return "persistent grid could not be launched co-resident";
+    case WAVE_ETIMEOUT: return "a device-side wait timed out";
+    case WAVE_EPOS: return "a session position was outside [0, T_max)";
+    case WAVE_EDEVICE: return "device is not sm_103";
+    case WAVE_ENOMEM: return "device allocation failed";
+    default: return "unknown error";
+  }
+}
+
+// Stream-K split of tiles x kblocks over the grid: the most tiles one CTA touches.
+static int max_tiles_touched(long long tiles, long long kb, int grid) {
+  const long long U = tiles * kb;
+  const int G = (int)(U < grid ? U : grid);
+  int mt = 1;
+  for (int c = 0; c < G; ++c) {
+    const long long u0 = U * c / G, u1 = U * (c + 1) / G;
+    if (u1 <= u0) continue;
+    const int n = (int)((u1 - 1) / kb - u0 / kb + 1);
+    if (n > mt) mt = n;
+  }
+  return mt;
+}
+
+extern "C" int wave_create(const wave_config* cfg, int S_max, int T_max, wave_t** out) {
+  if (!out || !shape_ok(cfg) || S_max < 1 || S_max > 128 || T_max < 4 || T_max % 4) return WAVE_EINVAL;
+  const long long rows = (long long)cfg->n_layers * 2 * S_max * cfg->n_heads * T_max;
+  if (rows >= (1LL << 31) || T_max > 65535 * kChunk) return WAVE_EINVAL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return WAVE_ECUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return WAVE_ECUDA;
+  if (prop.major != 10 || prop.minor != 3) return WAVE_EDEVICE;
+  if (!encode_fn()) return WAVE_ECUDA;
+  if (configure_step_kernel() != cudaSuccess) return WAVE_ECUDA;
+
+  wave_ctx* h = new wave_ctx();
+  h->cfg = *cfg;
+  h->S_max = S_max;
+  h->S_pad_max = (S_max + 15) / 16 * 16;
+  h->T_max = T_max;
+  h->device = dev;
+  h->grid = prop.multiProcessorCount;
+  layout_offsets(cfg, h->off, &h->layer_elems);
+  const int d = cfg->d_model, HD = cfg->n_heads * cfg->head_dim, F = cfg->ffn, H = cfg->n_heads,
+            D = cfg->head_dim;
+  h->tiles[kQKV] = (3 * HD + kTileM - 1) / kTileM;
+  h->kblocks[kQKV] = (d + kKBlk - 1) / kKBlk;
+  h->tiles[kO] = (d + kTileM - 1) / kTileM;
+  h->kblocks[kO] = (HD + kKBlk - 1) / kKBlk;
+  h->tiles[kGU] = (F + 63) / 64;
+  h->kblocks[kGU] = (d + kKBlk - 1) / kKBlk;
+  h->tiles[kDown] = (d + kTileM - 1) / kTileM;
+  h->kblocks[kDown] = (F + kKBlk - 1) / kKBlk;
+  int mt = 1;
+  for (int k = 0; k < 4; ++k) {
+    if (h->tiles[k] > 1024) {
+      delete h;
+      return WAVE_EINVAL;
+    }
+    int m = max_tiles_touched(h->tiles[k], h->kblocks[k], h->grid);
+    if (m > mt) mt = m;
+  }
+  h->max_tiles_per_cta = mt;
+
+  // workspace carve-up (256-byte aligned pieces)
+  const long long SP = h->S_pad_max;
+  const long long max_pieces =
+      (long long)S_max * H * (((T_max + kChunk - 1) / kChunk + kPieceChunks - 1) / kPieceChunks);
+  struct Part { void** dst; size_t bytes; };
+  std::vector<Part> parts = {
+      {(void**)&h->resid, (size_t)(SP * d * 4)},
+      {(void**)&h->xn, (size_t)(SP * d * 2)},
+      {(void**)&h->qkv, (size_t)(SP * 3 * HD * 4)},
+      {(void**)&h->attn, (size_t)(SP * HD * 2)},
+      {(void**)&h->u, (size_t)(SP * F * 2)},
+      {(void**)&h->gemm_part, (size_t)h->grid * mt * SP * kTileM * 4},
+      {(void**)&h->tile_cnt, 1024 * 4},
+      {(void**)&h->att_part, (size_t)(max_pieces * (D + 4) * 4)},
+      {(void**)&h->sh_cnt, (size_t)(S_max * H * 4)},
+      {(void**)&h->pieces, (size_t)(max_pieces * 16)},
+      {(void**)&h->n_pieces, 16},
+      {(void**)&h->rope, (size_t)T_max * (D / 2) * 8},
+      {(void**)&h->bar, 16},
+      {(void**)&h->err, 16},
+  };
+  size_t total = 0;
+  for (auto& pt : parts) total += (pt.bytes + 255) & ~(size_t)255;
+  if (cudaMalloc(&h->ws, total) != cudaSuccess) {
+    delete h;
+    return WAVE_ENOMEM;
+  }
+  h->ws_bytes = total;
+  if (cudaMemset(h->ws, 0, total) != cudaSuccess) {
+    cudaFree(h->ws);
+    delete h;
+    return WAVE_ECUDA;
+  }
+  size_t o = 0;
+  for (auto& pt : parts) {
+    *pt.dst = (char*)h->ws + o;
+    o += (pt.bytes + 255) & ~(size_t)255;
+  }
+  // RoPE table: angle t * base^(-2i/D), evaluated in double, stored as fp32.
+  std::vector<float2> tab((size_t)T_max * (D / 2));
+  for (int t = 0; t < T_max; ++t)
+    for (int i = 0; i < D / 2; ++i) {
+      const double th = pow((double)cfg->rope_base, -2.0 * i / (double)D);
+      const double a = (double)t * th;
+      tab[(size_t)t * (D / 2) + i] = make_float2((float)cos(a), (float)sin(a));
+    }
+  if (cudaMemcpy(h->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) !=
+      cudaSuccess) {
+    cudaFree(h->ws);
+    delete h;
+    return WAVE_ECUDA;
+  }
+  // co-residency: one CTA per SM must fit
+  int per_sm = 0;
+  if (occupancy_per_sm(&per_sm) != cudaSuccess || per_sm < 1) {
+    cudaFree(h->ws);
+    delete h;
+    return WAVE_ELAUNCH;
+  }
+  *out = h;
+  return WAVE_OK;
+}
+
+extern "C" void wave_destroy(wave_t* h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  cudaFree(h->ws);
+  delete h;
+}
+
+static bool enc(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* base, const cuuint64_t* dims,
+                const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return encode_fn()(m, dt, (cuuint32_t)rank, base, dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int encode_weight_maps(wave_ctx* h, const void* weights) {
+  const wave_config& c = h->cfg;
+  const cuuint64_t d = c.d_model, HD = (cuuint64_t)c.n_heads * c.head_dim, F = c.ffn, L = c.n_layers;
+  const cuuint64_t ls = (cuuint64_t)h->layer_elems * 2;  // layer stride in bytes
+  char* base = (char*)weights;
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  {  // Wqkv [L][3HD][d]
+    cuuint64_t dims[3] = {d, 3 * HD, L}, str[2] = {d * 2, ls};
+    cuuint32_t box[3] = {kKBlk, kTileM, 1};
+    if (!enc(&h->tm_w[kQKV], BF, 3, base + h->off[1] * 2, dims, str, box, SW)) return WAVE_ECUDA;
+  }
+  {  // Wo [L][d][HD]
+    cuuint64_t dims[3] = {HD, d, L}, str[2] = {HD * 2, ls};
+    cuuint32_t box[3] = {kKBlk, kTileM, 1};
+    if (!enc(&h->tm_w[kO], BF, 3, base + h->off[2] * 2, dims, str, box, SW)) return WAVE_ECUDA;
+  }
+  {  // Wgu [L][2][F][d]
+    cuuint64_t dims[4] = {d, F, 2, L}, str[3] = {d * 2, F * d * 2, ls};
+    cuuint32_t box[4] = {kKBlk, 64, 1, 1};
+    if (!enc(&h->tm_w[kGU], BF, 4, base + h->off[4] * 2, dims, str, box, SW)) return WAVE_ECUDA;
+  }
+  {  // Wdown [L][d][F]
+    cuuint64_t dims[3] = {F, d, L}, str[2] = {F * 2, ls};
+    cuuint32_t box[3] = {kKBlk, kTileM, 1};
+    if (!enc(&h->tm_w[kDown], BF, 3, base + h->off[5] * 2, dims, str, box, SW)) return WAVE_ECUDA;
+  }
+  return WAVE_OK;
+}
+
+static int encode_act_maps(wave_ctx* h, int S_pad) {
+  const wave_config& c = h->cfg;
+  const cuuint64_t d = c.d_model, HD = (cuuint64_t)c.n_heads * c.head_dim, F = c.ffn;
+  const cuuint64_t R = h->S_pad_max;
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  cuuint32_t box[2] = {kKBlk, (cuuint32_t)S_pad};
+  {
+    cuuint64_t dims[2] = {d, R}, str[1] = {d * 2};
+    if (!enc(&h->tm_x[kQKV], BF, 2, h->xn, dims, str, box, SW)) return WAVE_ECUDA;
+    h->tm_x[kGU] = h->tm_x[kQKV];
+  }
+  {
+    cuuint64_t dims[2] = {HD, R}, str[1] = {HD * 2};
+    if (!enc(&h->tm_x[kO], BF, 2, h->attn, dims, str, box, SW)) return WAVE_ECUDA;
+  }
+  {
+    cuuint64_t dims[2] = {F, R}, str[1] = {F * 2};
+    if (!enc(&h->tm_x[kDown], BF, 2, h->u, dims, str, box, SW)) return WAVE_ECUDA;
+  }
+  return WAVE_OK;
+}
+
+static int encode_kv_map(wave_ctx* h, uint8_t* kv) {
+  const wave_config& c = h->cfg;
+  const cuuint64_t D = c.head_dim;
+  const cuuint64_t rows = (cuuint64_t)c.n_layers * 2 * h->S_max * c.n_heads * h->T_max;
+  cuuint64_t dims[2] = {D, rows}, str[1] = {D};
+  cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)kChunk};
+  const auto SW = (D == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  if (!enc(&h->tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv, dims, str, box, SW)) return WAVE_ECUDA;
+  return WAVE_OK;
+}
+
+extern "C" int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8, float* kv_scales,
+                         const int32_t* positions, const void* x, void* y, void* stream) {
+  if (!h || !weights || !kv_fp8 || !kv_scales || !positions || !x || !y) return WAVE_EINVAL;
+  if (S < 1 || S > h->S_max) return WAVE_EINVAL;
+  if (((uintptr_t)weights & 15) || ((uintptr_t)kv_fp8 & 15) || ((uintptr_t)kv_scales & 15) ||
+      ((uintptr_t)positions & 3) || ((uintptr_t)x & 3) || ((uintptr_t)y & 3))
+    return WAVE_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int S_pad = (S + 15) / 16 * 16;
+  if (weights != h->maps_weights) {
+    int rc = encode_weight_maps(h, weights);
+    if (rc) return rc;
+    h->maps_weights = weights;
+  }
+  if (kv_fp8 != h->maps_kv) {
+    int rc = encode_kv_map(h, kv_fp8);
+    if (rc) return rc;
+    h->maps_kv = kv_fp8;
+  }
+  if (S_pad != h->maps_S) {
+    int rc = encode_act_maps(h, S_pad);
+    if (rc) return rc;
+    h->maps_S = S_pad;
+  }
+  StepParams p;
+  memset(&p, 0, sizeof(p));
+  for (int k = 0; k < 4; ++k) {
+    p.tm_w[k] = h->tm_w[k];
+    p.tm_x[k] = h->tm_x[k];
+    p.tiles[k] = h->tiles[k];
+    p.kblocks[k] = h->kblocks[k];
+  }
+  p.tm_kv = h->tm_kv;
+  const wave_config& c = h->cfg;
+  p.L = c.n_layers;
+  p.d = c.d_model;
+  p.H = c.n_heads;
+  p.D = c.head_dim;
+  p.F = c.ffn;
+  p.HD = c.n_heads * c.head_dim;
+  p.S = S;
+  p.S_pad = S_pad;
+  p.S_max = h->S_max;
+  p.T_max = h->T_max;
+  p.eps = c.rms_eps;
+  const int stride = 16384 + ((S_pad * 128 + 1023) & ~1023);
+  int nst = smem_layout().ring_bytes / stride;
+  p.nstage = nst > kMaxStages ? kMaxStages : nst;
+  p.max_tiles_per_cta = h->max_tiles_per_cta;
+  p.layer_elems = h->layer_elems;
+  p.off_g_attn = h->off[0];
+  p.off_g_mlp = h->off[3];
+  p.weights = (const uint16_t*)weights;
+  p.kv = kv_fp8;
+  p.kv_scales = kv_scales;
+  p.pos = positions;
+  p.x = (const uint16_t*)x;
+  p.y = (uint16_t*)y;
+  p.resid = h->resid;
+  p.xn = h->xn;
+  p.qkv = h->qkv;
+  p.attn = h->attn;
+  p.u = h->u;
+  p.gemm_part = h->gemm_part;
+  p.tile_cnt = h->tile_cnt;
+  p.att_part = h->att_part;
+  p.sh_cnt = h->sh_cnt;
+  p.pieces = h->pieces;
+  p.n_pieces = h->n_pieces;
+  p.rope = h->rope;
+  p.bar = h->bar;
+  p.err = h->err;
+  p.timeout_ns = h->timeout_ns;
+  p.skip_cta = h->skip_cta;
+  p.skip_bar = h->skip_bar;
+  p.kv_dump = h->kv_dump;
+  if (cudaMemsetAsync(h->bar, 0, 4, st) != cudaSuccess) return WAVE_ECUDA;
+  cudaError_t e = launch_step(p, h->grid, st);
+  h->last_stream = st;
+  if (e == cudaErrorCooperativeLaunchTooLarge) return WAVE_ELAUNCH;
+  if (e != cudaSuccess) return WAVE_ECUDA;
+  return WAVE_OK;
+}
+
+extern "C" int wave_status(wave_t* h) {
+  if (!h) return WAVE_EINVAL;
+  if (cudaStreamSynchronize(h->last_stream) != cudaSuccess) return WAVE_ECUDA;
+  int e = 0;
+  if (cudaMemcpy(&e, h->err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return WAVE_ECUDA;
+  if (e == 0) return WAVE_OK;
+  if (cudaMemset(h->err, 0, 4) != cudaSuccess) return WAVE_ECUDA;
+  if (e & kErrTimeout) return WAVE_ETIMEOUT;
+  return WAVE_EPOS;
+}
+
+extern "C" int wave_set_timeout_ns(wave_t* h, long long ns) {
+  if (!h || ns <= 0) return WAVE_EINVAL;
+  h->timeout_ns = ns;
+  return WAVE_OK;
+}
+
+extern "C" int wave_debug_skip_barrier(wave_t* h, int cta, int barrier) {
+  if (!h) return WAVE_EINVAL;
+  h->skip_cta = cta;
+  h->skip_bar = barrier;
+  return WAVE_OK;
+}
+
+extern "C" int wave_debug_dump_kv(wave_t* h, float* dst) {
+  if (!h) return WAVE_EINVAL;
+  h->kv_dump = dst;
+  return WAVE_OK;
+}
+
+extern "C" int wave_grid_size(wave_t* h) { return h ? h->grid : WAVE_EINVAL; }
+
+extern "C" int wave_barriers_per_step(wave_t* h) {
+  return h ? barriers_per_step(h->cfg.n_layers) : WAVE_EINVAL;
+}

@@ -1,0 +1,96 @@
+// internal.h -- shared definitions of the step library (host and device).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace wave {
+
+constexpr int kThreads = 192;     // 6 warps: TMA producer, MMA issuer, 4 epilogue warps
+constexpr int kWarps = kThreads / 32;
+constexpr int kTileM = 128;       // weight rows per GEMM tile = tcgen05 M
+constexpr int kKBlk = 64;         // K elements per pipeline stage (128 B of bf16)
+constexpr int kChunk = 64;        // attention tokens per async-copy chunk
+constexpr int kAttStages = 2;     // chunks in flight per attention warp
+constexpr int kPieceChunks = 4;   // chunks per attention work piece (256 tokens)
+constexpr int kMaxStages = 8;     // GEMM ring depth cap
+constexpr int kTmemCols = 256;    // two fp32 accumulators of up to 128 columns
+constexpr int kSmemBytes = 212 * 1024;
+
+enum ErrBits : int { kErrTimeout = 1, kErrPos = 2 };
+
+// Device error word bits -> public codes live in api.cu.
+
+enum GemmKind : int { kQKV = 0, kO = 1, kGU = 2, kDown = 3 };
+
+struct StepParams {
+  CUtensorMap tm_w[4];   // weights of the four projections (see GemmKind)
+  CUtensorMap tm_x[4];   // their activation inputs: xn, attn, xn, u (box rows = S_pad)
+  CUtensorMap tm_kv;     // the FP8 history viewed as rows of D bytes
+  // shape
+  int L, d, H, D, F, HD, S, S_pad, S_max, T_max;
+  float eps;
+  int nstage;            // GEMM ring depth for this S
+  int tiles[4], kblocks[4];
+  int max_tiles_per_cta; // partial-sum slots per CTA
+  long long layer_elems, off_g_attn, off_g_mlp;
+  // caller buffers
+  const uint16_t* weights;
+  uint8_t* kv;
+  float* kv_scales;
+  const int32_t* pos;
+  const uint16_t* x;
+  uint16_t* y;
+  // workspace
+  float* resid;          // [S_pad_max][d] fp32 residual stream
+  uint16_t* xn;          // [S_pad_max][d] bf16 normed input of QKV / gate-up
+  float* qkv;            // [S_max][3*H*D] fp32
+  uint16_t* attn;        // [S_pad_max][H*D] bf16 attention output
+  uint16_t* u;           // [S_pad_max][F] bf16 SwiGLU output
+  float* gemm_part;      // [G][max_tiles_per_cta][S_pad][128] split-K partials
+  int* tile_cnt;         // [max tiles] arrivals per tile (reset by the last arriver)
+  float* att_part;       // [max pieces][D + 4] (acc, m, l) per attention piece
+  int* sh_cnt;           // [S_max*H] arrivals per (session, head)
+  int4* pieces;          // [max pieces] (sh, c_lo | c_hi << 16, n_pieces_of_sh, first_piece)
+  int* n_pieces;         // [1]
+  const float2* rope;    // [T_max][D/2] (cos, sin)
+  unsigned* bar;         // grid barrier counter (zeroed before each launch)
+  int* err;              // error bits (sticky until wave_status)
+  long long timeout_ns;
+  int skip_cta, skip_bar;
+  float* kv_dump;        // testing hook: [L][2][S_max][H][D] pre-quantisation K/V, or null
+};
+
+// Host-side launch (step.cu).
+cudaError_t launch_step(const StepParams& p, int grid, cudaStream_t stream);
+cudaError_t configure_step_kernel();
+cudaError_t occupancy_per_sm(int* blocks);
+int barriers_per_step(int L);
+// Dynamic shared memory layout shared by host checks and the kernel.
+struct SmemLayout {
+  int ring_off, ring_bytes;      // GEMM ring / attention buffers (union)
+  int xbuf_off;                  // gate/up exchange buffer (64 x 17 fp32)
+  int qscr_off;                  // per-warp query scratch (kWarps x 512 B)
+  int red_off;                   // reduction scratch (256 words)
+  int bar_off;                   // mbarriers
+  int misc_off;                  // tmem address, flags
+  int total;
+};
+__host__ __device__ inline SmemLayout smem_layout() {
+  SmemLayout s;
+  s.ring_off = 0;
+  s.ring_bytes = 204 * 1024;
+  s.xbuf_off = s.ring_off + s.ring_bytes;            // 64 x 17 fp32
+  s.qscr_off = s.xbuf_off + 64 * 17 * 4;             // 3 KB: q as f16 hi + lo per warp
+  s.red_off = s.qscr_off + kWarps * 512;             // 1 KB: one int per thread
+  s.bar_off = s.red_off + 1024;                      // 64 mbarriers
+  s.misc_off = s.bar_off + 64 * 8;
+  s.total = s.misc_off + 64 + 1024;                  // + alignment slack
+  return s;
+}
+__host__ __device__ inline int attn_stage_bytes(int D) {  // K tile, V tile, K scales, V scales; 1 KB aligned
+  int b = 2 * kChunk * D + 2 * kChunk * 4;
+  return (b + 1023) & ~1023;
+}
+
+}  // namespace wave

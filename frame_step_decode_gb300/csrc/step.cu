@@ -1,0 +1,901 @@
+// step.cu -- the persistent frame-step kernel: one cooperative launch runs
+// every decoder layer for all S sessions, phases separated by device-side
+// grid barriers (no CPU round trip between operations: dotwave.ai case study,
+// "02 / The solution" and "04 / Under the hood").
+//
+// Phases per layer l (7 grid barriers per layer):
+//   norm     RMSNorm rows of the fp32 residual -> bf16 xn           (CUDA cores)
+//   QKV      xn . Wqkv^T -> fp32 q,k,v                              (tcgen05, stream-K)
+//   attn     per (session, head) piece: RoPE(q); the piece holding the
+//            current slot also RoPEs k, quantises k and v to E4M3 and
+//            appends them at slot pos; then split-T flash-decode over the
+//            FP8 history (mma.sync f16 with in-register dequantisation),
+//            partials merged by the last piece to finish    (TMA + mma.sync)
+//   O        resid += attn . Wo^T                                  (tcgen05, stream-K)
+//   norm     RMSNorm -> xn
+//   GU       u = bf16(silu(xn . Wg^T) * (xn . Wu^T))               (tcgen05, stream-K)
+//   down     resid += u . Wdown^T (y = bf16(resid) after the last layer)
+//
+// Roles inside a 6-warp CTA during GEMM phases: warp 0 issues TMA loads of
+// weight/activation tiles into a shared-memory ring, warp 1 issues tcgen05
+// MMAs into a double-buffered TMEM accumulator, warps 2..5 drain TMEM and run
+// the fused epilogue.  Every wait is bounded (globaltimer) and reports
+// WAVE_ETIMEOUT through the device error word instead of hanging.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "fp8.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace wave {
+
+struct Ctx {
+  uint8_t* smem;
+  uint32_t sbase;       // shared-space address of smem
+  uint32_t tmem;        // TMEM base address of the two accumulators
+  unsigned bar_target;  // thread 0: next grid-barrier target
+  int bar_index;
+  uint32_t ring_it;     // GEMM ring stage counter (producer and MMA threads)
+  uint32_t acc_it;      // accumulator counter (MMA and epilogue threads)
+  uint32_t att_it;      // attention chunk counter (per warp)
+  SmemLayout lay;
+};
+
+// mbarrier slots (byte offsets from bar_off)
+__device__ __forceinline__ uint32_t bar_full(const Ctx& c, int i) { return c.sbase + c.lay.bar_off + 8 * i; }
+__device__ __forceinline__ uint32_t bar_empty(const Ctx& c, int i) { return c.sbase + c.lay.bar_off + 64 + 8 * i; }
+__device__ __forceinline__ uint32_t bar_accf(const Ctx& c, int i) { return c.sbase + c.lay.bar_off + 128 + 8 * i; }
+__device__ __forceinline__ uint32_t bar_acce(const Ctx& c, int i) { return c.sbase + c.lay.bar_off + 144 + 8 * i; }
+__device__ __forceinline__ uint32_t bar_att(const Ctx& c, int w, int st) {
+  return c.sbase + c.lay.bar_off + 160 + 8 * (w * kAttStages + st);
+}
+__device__ __forceinline__ uint32_t bar_drain(const Ctx& c) { return c.sbase + c.lay.bar_off + 320; }
+__device__ __forceinline__ volatile int* misc_word(const Ctx& c, int i) {
+  return (volatile int*)(c.smem + c.lay.misc_off + 4 * i);
+}
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void set_err(const StepParams& p, int bits) { atomicOr(p.err, bits); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// ------------------------------------------------------------- grid barrier
+// All CTAs arrive on one counter (zeroed before the launch) and wait until it
+// reaches (barrier index + 1) * grid.  The wait gives up after timeout_ns or
+// when another CTA has recorded an error.
+__device__ bool grid_sync(const StepParams& p, Ctx& c) {
+  fence_proxy_async_global();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    c.bar_target += gridDim.x;
+    __threadfence();
+    bool skip = ((int)blockIdx.x == p.skip_cta && c.bar_index == p.skip_bar);
+    if (!skip) atomicAdd(p.bar, 1u);
+    int ok = 1;
+    long long t0 = globaltimer();
+    for (uint32_t it = 0;; ++it) {
+      unsigned v = ld_acquire(p.bar);
+      if ((int)(v - c.bar_target) >= 0) break;
+      if (*(volatile int*)p.err & kErrTimeout) { ok = 0; break; }
+      if ((it & 15) == 15 && globaltimer() - t0 > p.timeout_ns) {
+        set_err(p, kErrTimeout);
+        ok = 0;
+        break;
+      }
+    }
+    __threadfence();
+    *misc_word(c, 2) = ok;
+  }
+  c.bar_index++;
+  __syncthreads();
+  bool ok = *misc_word(c, 2) != 0;
+  fence_proxy_async_global();
+  return ok;
+}
+
+// ------------------------------------------------------------------- norm
+// xn[s] = bf16(r * rstd * g), rstd = 1/sqrt(mean(r^2) + eps); rows strided
+// over CTAs.  At layer 0 the residual is first loaded from x (bf16).
+__device__ void norm_phase(const StepParams& p, Ctx& c, const uint16_t* g, bool from_x) {
+  float* red = (float*)(c.smem + c.lay.red_off);
+  const int d = p.d, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int s = blockIdx.x; s < p.S; s += gridDim.x) {
+    float* r = p.resid + (size_t)s * d;
+    float ss = 0.f;
+    for (int i = tid; i < d; i += kThreads) {
+      float v;
+      if (from_x) {
+        v = bf16_to_f32(p.x[(size_t)s * d + i]);
+        r[i] = v;
+      } else {
+        v = __ldcg(r + i);
+      }
+      ss = fmaf(v, v, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) tot += red[w];
+    const float rstd = 1.0f / sqrtf(tot / (float)d + p.eps);
+    for (int i = tid; i < d; i += kThreads) {
+      float v = from_x ? r[i] : __ldcg(r + i);
+      p.xn[(size_t)s * d + i] = f32_to_bf16((v * rstd) * bf16_to_f32(g[i]));
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------ GEMM (tcgen05)
+struct Span { long long u0, u1; };
+__device__ __forceinline__ Span cta_span(long long U, int G, int c) {
+  return Span{U * c / G, U * (c + 1) / G};
+}
+// Last CTA whose span starts at or before unit u (the owner of u).
+__device__ __forceinline__ int owner_of(long long U, int G, long long u) {
+  return (int)(((u + 1) * G + U - 1) / U - 1);
+}
+
+__device__ __forceinline__ void epilogue_apply(const StepParams& p, Ctx& c, int kind, int t, int r,
+                                               int col0, const float* v, bool last_layer) {
+  const int S = p.S;
+  if (kind == kQKV) {
+    const int N = 3 * p.HD, n = t * kTileM + r;
+    if (n < N) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (col0 + i < S) p.qkv[(size_t)(col0 + i) * N + n] = v[i];
+    }
+  } else if (kind == kO || kind == kDown) {
+    const int d = p.d, n = t * kTileM + r;
+    if (n < d) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int s = col0 + i;
+        if (s < S) {
+          float* rp = p.resid + (size_t)s * d + n;
+          float nr = __ldcg(rp) + v[i];
+          *rp = nr;
+          if (last_layer) p.y[(size_t)s * d + n] = f32_to_bf16(nr);
+        }
+      }
+    }
+  } else {  // kGU: rows 0..63 gate, 64..127 up of the same 64 features
+    float* xb = (float*)(c.smem + c.lay.xbuf_off);
+    if (r >= 64) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) xb[(r - 64) * 17 + i] = v[i];
+    }
+    named_bar(2, 128);
+    if (r < 64) {
+      const int F = p.F, n = t * 64 + r;
+      if (n < F) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int s = col0 + i;
+          if (s < S) {
+            float gt = v[i], up = xb[r * 17 + i];
+            float sl = gt / (1.0f + expf(-gt));
+            p.u[(size_t)s * F + n] = f32_to_bf16(sl * up);
+          }
+        }
+      }
+    }
+    named_bar(2, 128);
+  }
+}
+
+__device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, bool last_layer) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KB = p.kblocks[kind];
+  const long long U = (long long)p.tiles[kind] * KB;
+  // Split over min(grid, units) CTAs so that every participating span is
+  // non-empty and the owners of a tile's units are consecutive CTAs.
+  const int G = (int)min((long long)gridDim.x, U), cta = blockIdx.x;
+  const Span sp = (cta < G) ? cta_span(U, G, cta) : Span{0, 0};
+  const int S_pad = p.S_pad, nst = p.nstage;
+  const uint32_t b_bytes = (uint32_t)S_pad * 128u;
+  const uint32_t stride = 16384u + ((b_bytes + 1023u) & ~1023u);
+  const uint32_t ring = c.sbase + c.lay.ring_off;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      const CUtensorMap* wm = &p.tm_w[kind];
+      const CUtensorMap* xm = &p.tm_x[kind];
+      for (long long u = sp.u0; u < sp.u1;) {
+        const int t = (int)(u / KB);
+        const long long e = min(sp.u1, (long long)(t + 1) * KB);
+        for (int kb = (int)(u - (long long)t * KB); kb < (int)(e - (long long)t * KB); ++kb) {
+          const uint32_t slot = c.ring_it % nst, ph = (c.ring_it / nst) & 1u;
+          if (!mbar_wait(bar_empty(c, slot), ph ^ 1u, p.timeout_ns, p.err)) {
+            set_err(p, kErrTimeout);
+            return;
+          }
+          const uint32_t fb = bar_full(c, slot);
+          mbar_arrive_expect_tx(fb, 16384u + b_bytes);
+          const uint32_t a = ring + slot * stride;
+          if (kind == kGU) {
+            tma_load_4d(a, wm, kb * kKBlk, t * 64, 0, layer, fb, pol);
+            tma_load_4d(a + 8192, wm, kb * kKBlk, t * 64, 1, layer, fb, pol);
+          } else {
+            tma_load_3d(a, wm, kb * kKBlk, t * kTileM, layer, fb, pol);
+          }
+          tma_load_2d(a + 16384, xm, kb * kKBlk, 0, fb);
+          c.ring_it++;
+        }
+        u = e;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kTileM, S_pad);
+      for (long long u = sp.u0; u < sp.u1;) {
+        const int t = (int)(u / KB);
+        const long long e = min(sp.u1, (long long)(t + 1) * KB);
+        const uint32_t b = c.acc_it & 1u;
+        if (!mbar_wait(bar_acce(c, b), ((c.acc_it >> 1) & 1u) ^ 1u, p.timeout_ns, p.err)) {
+          set_err(p, kErrTimeout);
+          return;
+        }
+        tc_fence_after();
+        const uint32_t dt = c.tmem + b * 128u;
+        const int k0 = (int)(u - (long long)t * KB), k1 = (int)(e - (long long)t * KB);
+        for (int kb = k0; kb < k1; ++kb) {
+          const uint32_t slot = c.ring_it % nst, ph = (c.ring_it / nst) & 1u;
+          if (!mbar_wait(bar_full(c, slot), ph, p.timeout_ns, p.err)) {
+            set_err(p, kErrTimeout);
+            return;
+          }
+          tc_fence_after();
+          const uint32_t a = ring + slot * stride, bs = a + 16384u;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16(dt, sdesc_sw128(a + kk * 32), sdesc_sw128(bs + kk * 32), idesc,
+                        (kb > k0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar_empty(c, slot));
+          c.ring_it++;
+        }
+        tc_commit(bar_accf(c, b));
+        c.acc_it++;
+        u = e;
+      }
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3, r = q * 32 + lane;
+    const int MT = p.max_tiles_per_cta;
+    const int first_tile = (int)(sp.u0 / KB);
+    for (long long u = sp.u0; u < sp.u1;) {
+      const int t = (int)(u / KB);
+      const long long tb = (long long)t * KB, te = tb + KB;
+      const long long e = min(sp.u1, te);
+      const int c_first = owner_of(U, G, tb), c_last = owner_of(U, G, te - 1);
+      const int nseg = c_last - c_first + 1;
+      const uint32_t b = c.acc_it & 1u;
+      // one thread waits, the four warps take the same decision
+      volatile int* wflag = misc_word(c, 4 + (int)b);
+      if (threadIdx.x == 64)
+        *wflag = mbar_wait(bar_accf(c, b), (c.acc_it >> 1) & 1u, p.timeout_ns, p.err) ? 1 : 0;
+      named_bar(1, 128);
+      if (!*wflag) {
+        if (threadIdx.x == 64) set_err(p, kErrTimeout);
+        return;
+      }
+      tc_fence_after();
+      const uint32_t tb_addr = c.tmem + ((uint32_t)(q * 32) << 16) + b * 128u;
+      if (nseg == 1) {
+        for (int col = 0; col < S_pad; col += 16) {
+          float v[16];
+          tmem_ld16(tb_addr + col, v);
+          epilogue_apply(p, c, kind, t, r, col, v, last_layer);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_acce(c, b));
+      } else {
+        float* slot = p.gemm_part + ((size_t)cta * MT + (t - first_tile)) * (size_t)S_pad * kTileM;
+        for (int col = 0; col < S_pad; col += 16) {
+          float v[16];
+          tmem_ld16(tb_addr + col, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) slot[(size_t)(col + i) * kTileM + r] = v[i];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_acce(c, b));
+        __threadfence();
+        named_bar(1, 128);
+        if (threadIdx.x == 64) {
+          int old = atomicAdd(p.tile_cnt + t, 1);
+          *misc_word(c, 3) = (old == nseg - 1) ? 1 : 0;
+        }
+        named_bar(1, 128);
+        if (*misc_word(c, 3)) {
+          __threadfence();
+          for (int col = 0; col < S_pad; col += 16) {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            for (int j = 0; j < nseg; ++j) {
+              const int cj = c_first + j;
+              const int ftj = (int)(cta_span(U, G, cj).u0 / KB);
+              const float* sj =
+                  p.gemm_part + ((size_t)cj * MT + (t - ftj)) * (size_t)S_pad * kTileM;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] += __ldcg(sj + (size_t)(col + i) * kTileM + r);
+            }
+            epilogue_apply(p, c, kind, t, r, col, v, last_layer);
+          }
+          if (threadIdx.x == 64) p.tile_cnt[t] = 0;
+        }
+        named_bar(1, 128);
+      }
+      c.acc_it++;
+      u = e;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- attention
+// Byte offset inside a TMA tile written with the 128-byte (D = 128) or
+// 64-byte (D = 64) swizzle: the 16-byte chunk index (address bits 4..6) is
+// XORed with the 128-byte row index (bits 7..9), masked to the swizzle span.
+template <int D>
+__device__ __forceinline__ uint32_t swz(uint32_t off) {
+  constexpr uint32_t m = (D == 128) ? 7u : 3u;
+  return off ^ (((off >> 7) & m) << 4);
+}
+
+template <int D>
+__device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
+  constexpr int DPL = D / 32;    // dims per lane for row-wise work
+  constexpr int KQB = D / 4;     // K bytes per lane per token (score mma)
+  constexpr int KST = D / 16;    // k-steps of the score mma over the head dim
+  constexpr int VB = D / 8;      // V bytes per lane per token (P.V mma)
+  constexpr int MTV = D / 16;    // m-tiles of the P.V mma (16 head dims each)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t4 = lane & 3;       // thread-in-group of the mma fragments
+  const int g = lane >> 2;       // group of the mma fragments
+  const int NW = gridDim.x * kWarps;
+  const int gw = blockIdx.x * kWarps + warp;
+  const int n_pieces = __ldcg(p.n_pieces);
+  const int H = p.H, HD = p.HD;
+  const int stage_bytes = attn_stage_bytes(D);
+  uint8_t* wbuf = c.smem + c.lay.ring_off + warp * kAttStages * stage_bytes;
+  const uint32_t wbuf_s = c.sbase + c.lay.ring_off + warp * kAttStages * stage_bytes;
+  __half* qs_hi = (__half*)(c.smem + c.lay.qscr_off + warp * 512);
+  __half* qs_lo = qs_hi + 128;
+  const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
+
+  for (int pi = gw; pi < n_pieces; pi += NW) {
+    const int4 pc = __ldcg(p.pieces + pi);
+    const int sh = pc.x, c_lo = pc.y & 0xFFFF, c_hi = pc.y >> 16, np = pc.z, first = pc.w;
+    const int s = sh / H, h = sh - s * H;
+    const int P = __ldcg(p.pos + s);
+    const int nch = P / kChunk + 1;
+    const bool tail = (c_hi == nch);
+    const float* qrow = p.qkv + (size_t)s * 3 * HD + h * D;
+    const float2* cs = p.rope + (size_t)P * (D / 2);
+    const size_t rowK = ((((size_t)layer * 2 + 0) * p.S_max + s) * H + h) * (size_t)p.T_max;
+    const size_t rowV = ((((size_t)layer * 2 + 1) * p.S_max + s) * H + h) * (size_t)p.T_max;
+
+    // RoPE of q (and k) in fp32: lane i holds dims [i*DPL, (i+1)*DPL); its
+    // rotate-half partner dims are in lane i^16.
+    float rq[DPL], rk[DPL], vv[DPL];
+    {
+      float x[DPL], y[DPL];
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) x[e] = __ldcg(qrow + lane * DPL + e);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) y[e] = __shfl_xor_sync(0xffffffffu, x[e], 16);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) {
+        const float2 t = cs[(lane & 15) * DPL + e];
+        rq[e] = (lane < 16) ? (x[e] * t.x - y[e] * t.y) : (y[e] * t.y + x[e] * t.x);
+      }
+    }
+    uint32_t kcodes = 0, vcodes = 0;
+    float ks_new = 0.f, vs_new = 0.f;
+    if (tail) {
+      float x[DPL], y[DPL];
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) x[e] = __ldcg(qrow + HD + lane * DPL + e);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) y[e] = __shfl_xor_sync(0xffffffffu, x[e], 16);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) {
+        const float2 t = cs[(lane & 15) * DPL + e];
+        rk[e] = (lane < 16) ? (x[e] * t.x - y[e] * t.y) : (y[e] * t.y + x[e] * t.x);
+        vv[e] = __ldcg(qrow + 2 * HD + lane * DPL + e);
+      }
+      if (p.kv_dump) {
+        float* dk = p.kv_dump + ((((size_t)layer * 2 + 0) * p.S_max + s) * H + h) * D + lane * DPL;
+        float* dv = p.kv_dump + ((((size_t)layer * 2 + 1) * p.S_max + s) * H + h) * D + lane * DPL;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) {
+          dk[e] = rk[e];
+          dv[e] = vv[e];
+        }
+      }
+      kcodes = quantize_lane<DPL>(rk, ks_new);
+      vcodes = quantize_lane<DPL>(vv, vs_new);
+      uint8_t* kdst = p.kv + (rowK + P) * D + lane * DPL;
+      uint8_t* vdst = p.kv + (rowV + P) * D + lane * DPL;
+      if constexpr (DPL == 4) {
+        *(uint32_t*)kdst = kcodes;
+        *(uint32_t*)vdst = vcodes;
+      } else {
+        *(uint16_t*)kdst = (uint16_t)kcodes;
+        *(uint16_t*)vdst = (uint16_t)vcodes;
+      }
+      if (lane == 0) {
+        p.kv_scales[rowK + P] = ks_new;
+        p.kv_scales[rowV + P] = vs_new;
+      }
+    }
+    // q as an f16 pair hi + lo (|q - hi - lo| <~ 2^-22 |q|), so that the
+    // tensor-core dot products keep close to fp32 accuracy.
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) {
+      const __half hi = __float2half_rn(rq[e]);
+      qs_hi[lane * DPL + e] = hi;
+      qs_lo[lane * DPL + e] = __float2half_rn(rq[e] - __half2float(hi));
+    }
+    __syncwarp();
+    // B fragments of the score mma (q is column 0 of B): lanes 0..3 hold
+    // dims [t4*D/4, (t4+1)*D/4); k-step j takes dims +4j..+4j+3.
+    uint32_t qh0[KST], qh1[KST], ql0[KST], ql1[KST];
+    {
+      const uint32_t* wh = (const uint32_t*)(qs_hi + t4 * (D / 4));
+      const uint32_t* wl = (const uint32_t*)(qs_lo + t4 * (D / 4));
+#pragma unroll
+      for (int j = 0; j < KST; ++j) {
+        qh0[j] = (lane < 4) ? wh[2 * j] : 0u;
+        qh1[j] = (lane < 4) ? wh[2 * j + 1] : 0u;
+        ql0[j] = (lane < 4) ? wl[2 * j] : 0u;
+        ql1[j] = (lane < 4) ? wl[2 * j + 1] : 0u;
+      }
+    }
+
+    const int n = c_hi - c_lo;
+    auto issue = [&](int ci, int st) {
+      const uint32_t base = wbuf_s + st * stage_bytes;
+      const uint32_t fb = bar_att(c, warp, st);
+      const int t0 = ci * kChunk;
+      const uint32_t sbytes = 4u * (uint32_t)min(kChunk, p.T_max - t0);
+      mbar_arrive_expect_tx(fb, 2u * kChunk * D + 2u * sbytes);
+      tma_load_2d(base, &p.tm_kv, 0, (int)(rowK + t0), fb);
+      tma_load_2d(base + kChunk * D, &p.tm_kv, 0, (int)(rowV + t0), fb);
+      bulk_load(base + 2 * kChunk * D, p.kv_scales + rowK + t0, sbytes, fb);
+      bulk_load(base + 2 * kChunk * D + 256, p.kv_scales + rowV + t0, sbytes, fb);
+    };
+    if (lane == 0) {
+      for (int k = 0; k < min(n, kAttStages); ++k) issue(c_lo + k, (c.att_it + k) % kAttStages);
+    }
+    __syncwarp();
+
+    // acc[j]: c0 = o[dim of row g], c2 = o[dim of row g+8] of P.V m-tile j
+    // (real in lanes with t4 == 0; values in units of R).
+    float acc[MTV][4];
+#pragma unroll
+    for (int j = 0; j < MTV; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f, R = 0.f;
+    bool aborted = false;
+
+    for (int k = 0; k < n; ++k) {
+      const int ci = c_lo + k;
+      const uint32_t it = c.att_it + k;
+      const int st = it % kAttStages;
+      if (!mbar_wait(bar_att(c, warp, st), (it / kAttStages) & 1u, p.timeout_ns, p.err)) {
+        set_err(p, kErrTimeout);
+        aborted = true;
+        break;
+      }
+      uint8_t* kt = wbuf + st * stage_bytes;
+      uint8_t* vt = kt + kChunk * D;
+      float* ksm = (float*)(kt + 2 * kChunk * D);
+      float* vsm = ksm + 64;
+      const bool last = tail && (ci == nch - 1);
+      const int valid = last ? (P - ci * kChunk + 1) : kChunk;
+      if (last) {  // the current slot: use the codes just written
+        const int rr = P - ci * kChunk;
+        const uint32_t off = swz<D>((uint32_t)(rr * D + lane * DPL));
+        if constexpr (DPL == 4) {
+          *(uint32_t*)(kt + off) = kcodes;
+          *(uint32_t*)(vt + off) = vcodes;
+        } else {
+          *(uint16_t*)(kt + off) = (uint16_t)kcodes;
+          *(uint16_t*)(vt + off) = (uint16_t)vcodes;
+        }
+        if (lane == 0) {
+          ksm[rr] = ks_new;
+          vsm[rr] = vs_new;
+        }
+        __syncwarp();
+      }
+
+      // ---- scores S[token] = K . q: 4 m-tiles of 16 tokens; A = codes of
+      // tokens g and g+8 (lane's KQB bytes each), B = q (column 0).
+      float sc[4][2];  // [m-tile][token g, token g+8], real where t4 == 0
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        float cacc[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t k0[KQB / 4], k1[KQB / 4];
+#pragma unroll
+        for (int ch = 0; ch < KQB / 16; ++ch) {
+          const uint4 a = *(const uint4*)(kt + swz<D>((uint32_t)((mt * 16 + g) * D + t4 * KQB + ch * 16)));
+          const uint4 b = *(const uint4*)(kt + swz<D>((uint32_t)((mt * 16 + g + 8) * D + t4 * KQB + ch * 16)));
+          k0[4 * ch + 0] = a.x; k0[4 * ch + 1] = a.y; k0[4 * ch + 2] = a.z; k0[4 * ch + 3] = a.w;
+          k1[4 * ch + 0] = b.x; k1[4 * ch + 1] = b.y; k1[4 * ch + 2] = b.z; k1[4 * ch + 3] = b.w;
+        }
+#pragma unroll
+        for (int j = 0; j < KST; ++j) {
+          const uint32_t a0 = e4m3x2_to_f16x2(k0[j] & 0xFFFFu), a1 = e4m3x2_to_f16x2(k1[j] & 0xFFFFu);
+          const uint32_t a2 = e4m3x2_to_f16x2(k0[j] >> 16), a3 = e4m3x2_to_f16x2(k1[j] >> 16);
+          mma_f16_16816(cacc, a0, a1, a2, a3, qh0[j], qh1[j]);
+          mma_f16_16816(cacc, a0, a1, a2, a3, ql0[j], ql1[j]);
+        }
+        sc[mt][0] = cacc[0];
+        sc[mt][1] = cacc[2];
+      }
+      // ---- online softmax (base 2) over the lanes with t4 == 0
+      float mx = -INFINITY, vmax = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int tok = mt * 16 + g + 8 * e;
+          const bool ok = tok < valid;
+          const float v = ok ? sc[mt][e] * ksm[tok] * scale_log2 : -INFINITY;
+          sc[mt][e] = v;
+          mx = fmaxf(mx, v);
+          vmax = ok ? fmaxf(vmax, vsm[tok]) : vmax;
+        }
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+      }
+      const float m_new = fmaxf(m_run, mx);
+      const float alpha = ex2(m_run - m_new);
+      // acc holds values in units of R; move to units of the chunk's largest
+      // V scale so that the weights p * vs / R stay in [0, 1].
+      const float R_new = (vmax > 0.f) ? vmax : 1.f;
+      const float rescale = (R > 0.f) ? alpha * (R / R_new) : 0.f;
+      l_run *= alpha;
+#pragma unroll
+      for (int j = 0; j < MTV; ++j) {
+        acc[j][0] *= rescale;
+        acc[j][2] *= rescale;
+      }
+      R = R_new;
+      m_run = m_new;
+      const float inv_R = 1.0f / R_new;
+      // weights w = p * vs / R as f16 hi + lo, packed {token g, token g+8}
+      uint32_t whi[4], wlo[4];
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        float w2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int tok = mt * 16 + g + 8 * e;
+          const float pr = ex2(sc[mt][e] - m_new);
+          l_run += pr;
+          w2[e] = (tok < valid) ? pr * (vsm[tok] * inv_R) : 0.f;
+        }
+        const __half2 hi = __floats2half2_rn(w2[0], w2[1]);
+        const float2 hf = __half22float2(hi);
+        const __half2 lo = __floats2half2_rn(w2[0] - hf.x, w2[1] - hf.y);
+        whi[mt] = *(const uint32_t*)&hi;
+        wlo[mt] = *(const uint32_t*)&lo;
+      }
+      // ---- O += V^T . w: per 16-token group, A = V codes (rows = head dims,
+      // columns = tokens), B = w (column 0).  Lane t4 < 4 gathers the weights
+      // of tokens 2t4, 2t4+1, 2t4+8, 2t4+9 from lanes 8*t4 and 8*t4+4.
+      const int srcA = 8 * t4, srcB = 8 * t4 + 4;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const uint32_t hA = __shfl_sync(0xffffffffu, whi[mt], srcA);
+        const uint32_t hB = __shfl_sync(0xffffffffu, whi[mt], srcB);
+        const uint32_t lA = __shfl_sync(0xffffffffu, wlo[mt], srcA);
+        const uint32_t lB = __shfl_sync(0xffffffffu, wlo[mt], srcB);
+        const uint32_t bh0 = (lane < 4) ? prmt(hA, hB, 0x5410u) : 0u;
+        const uint32_t bh1 = (lane < 4) ? prmt(hA, hB, 0x7632u) : 0u;
+        const uint32_t bl0 = (lane < 4) ? prmt(lA, lB, 0x5410u) : 0u;
+        const uint32_t bl1 = (lane < 4) ? prmt(lA, lB, 0x7632u) : 0u;
+        const int r0 = mt * 16 + 2 * t4;
+        const int rows[4] = {r0, r0 + 1, r0 + 8, r0 + 9};
+        uint32_t vw[4][VB / 4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const uint32_t off = swz<D>((uint32_t)(rows[a] * D + g * VB));
+          if constexpr (VB == 16) {
+            const uint4 w4 = *(const uint4*)(vt + off);
+            vw[a][0] = w4.x;
+            vw[a][1] = w4.y;
+            vw[a][2 % (VB / 4)] = w4.z;
+            vw[a][3 % (VB / 4)] = w4.w;
+          } else {
+            const uint2 w2 = *(const uint2*)(vt + off);
+            vw[a][0] = w2.x;
+            vw[a][1] = w2.y;
+          }
+          if (rows[a] >= valid) {
+#pragma unroll
+            for (int w = 0; w < VB / 4; ++w) vw[a][w] = 0u;
+          }
+        }
+        // byte-pair tables: p01[b] = {tok r0 byte b, tok r0+1 byte b}, p23 likewise
+        uint32_t p01[VB / 2], p23[VB / 2];
+#pragma unroll
+        for (int w = 0; w < VB / 4; ++w) {
+          p01[2 * w] = prmt(vw[0][w], vw[1][w], 0x5140u);
+          p01[2 * w + 1] = prmt(vw[0][w], vw[1][w], 0x7362u);
+          p23[2 * w] = prmt(vw[2][w], vw[3][w], 0x5140u);
+          p23[2 * w + 1] = prmt(vw[2][w], vw[3][w], 0x7362u);
+        }
+        // byte b of a token vector sits in half (b & 1) of p..[b >> 1]
+        // m-tile j: row g <-> byte j, row g+8 <-> byte j + VB/2
+#pragma unroll
+        for (int j = 0; j < MTV; ++j) {
+          const int b0 = j, b1 = j + VB / 2;
+          const uint32_t a0 = e4m3x2_to_f16x2((p01[b0 >> 1] >> (16 * (b0 & 1))) & 0xFFFFu);
+          const uint32_t a1 = e4m3x2_to_f16x2((p01[b1 >> 1] >> (16 * (b1 & 1))) & 0xFFFFu);
+          const uint32_t a2 = e4m3x2_to_f16x2((p23[b0 >> 1] >> (16 * (b0 & 1))) & 0xFFFFu);
+          const uint32_t a3 = e4m3x2_to_f16x2((p23[b1 >> 1] >> (16 * (b1 & 1))) & 0xFFFFu);
+          mma_f16_16816(acc[j], a0, a1, a2, a3, bh0, bh1);
+          mma_f16_16816(acc[j], a0, a1, a2, a3, bl0, bl1);
+        }
+      }
+      if (last) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && k + kAttStages < n) issue(ci + kAttStages, st);
+      __syncwarp();
+    }
+    if (aborted) {
+      // let this warp's copies in flight land before returning
+      for (int k = 0; k < n; ++k) {
+        const uint32_t it = c.att_it + k;
+        mbar_wait(bar_att(c, warp, it % kAttStages), (it / kAttStages) & 1u, 100000000LL, p.err);
+      }
+      return;
+    }
+    c.att_it += n;
+
+    // ---- finish the piece: l over the lanes with t4 == 0
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, o);
+    // lane (g, 0): m-tile j row g -> dim g*VB + j, row g+8 -> dim g*VB + VB/2 + j
+    if (np == 1) {
+      if (t4 == 0) {
+        const float f = R / l_run;
+        uint16_t* o = p.attn + (size_t)s * HD + h * D + g * VB;
+#pragma unroll
+        for (int j = 0; j < MTV; ++j) {
+          o[j] = f32_to_bf16(acc[j][0] * f);
+          o[VB / 2 + j] = f32_to_bf16(acc[j][2] * f);
+        }
+      }
+    } else {
+      float* part = p.att_part + (size_t)pi * (D + 4);
+      if (t4 == 0) {
+#pragma unroll
+        for (int j = 0; j < MTV; ++j) {
+          part[g * VB + j] = acc[j][0] * R;
+          part[g * VB + VB / 2 + j] = acc[j][2] * R;
+        }
+        if (lane == 0) {
+          part[D] = m_run;
+          part[D + 1] = l_run;
+        }
+      }
+      __threadfence();
+      __syncwarp();
+      int last_arrival = 0;
+      if (lane == 0) last_arrival = (atomicAdd(p.sh_cnt + sh, 1) == np - 1);
+      last_arrival = __shfl_sync(0xffffffffu, last_arrival, 0);
+      if (last_arrival) {
+        __threadfence();
+        float M = -INFINITY;
+        for (int i = 0; i < np; ++i) M = fmaxf(M, __ldcg(p.att_part + (size_t)(first + i) * (D + 4) + D));
+        float Ls = 0.f, o[DPL];
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[e] = 0.f;
+        for (int i = 0; i < np; ++i) {
+          const float* pp = p.att_part + (size_t)(first + i) * (D + 4);
+          const float wgt = ex2(__ldcg(pp + D) - M);
+          Ls += __ldcg(pp + D + 1) * wgt;
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) o[e] += __ldcg(pp + lane * DPL + e) * wgt;
+        }
+        const float inv = 1.0f / Ls;
+        uint16_t* od = p.attn + (size_t)s * HD + h * D + lane * DPL;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) od[e] = f32_to_bf16(o[e] * inv);
+        if (lane == 0) p.sh_cnt[sh] = 0;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- prologue
+// One CTA turns positions into the attention work list: each (session, head)
+// history of pos+1 slots is cut into pieces of up to kPieceChunks chunks.
+static_assert(kThreads <= 256, "the reduction scratch holds one word per thread");
+__device__ void build_pieces(const StepParams& p, Ctx& c) {
+  int* red = (int*)(c.smem + c.lay.red_off);
+  const int N = p.S * p.H, tid = threadIdx.x;
+  const int b0 = (int)((long long)N * tid / kThreads), b1 = (int)((long long)N * (tid + 1) / kThreads);
+  auto count = [&](int sh) {
+    const int P = p.pos[sh / p.H];
+    if (P < 0 || P >= p.T_max) return 0;
+    const int nch = P / kChunk + 1;
+    return (nch + kPieceChunks - 1) / kPieceChunks;
+  };
+  int local = 0;
+  for (int sh = b0; sh < b1; ++sh) local += count(sh);
+  red[tid] = local;
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int i = 0; i < kThreads; ++i) {
+      const int v = red[i];
+      red[i] = run;
+      run += v;
+    }
+    *p.n_pieces = run;
+  }
+  __syncthreads();
+  int base = red[tid];
+  for (int sh = b0; sh < b1; ++sh) {
+    const int np = count(sh);
+    const int P = p.pos[sh / p.H];
+    const int nch = P / kChunk + 1;
+    for (int q = 0; q < np; ++q) {
+      const int lo = q * kPieceChunks, hi = min(nch, lo + kPieceChunks);
+      p.pieces[base + q] = make_int4(sh, lo | (hi << 16), np, base);
+    }
+    base += np;
+  }
+  // sessions with an invalid position: flag, and zero their attention rows
+  for (int s = tid; s < p.S; s += kThreads) {
+    const int P = p.pos[s];
+    if (P < 0 || P >= p.T_max) set_err(p, kErrPos);
+  }
+  for (int i = tid; i < p.S * p.HD; i += kThreads) {
+    const int P = p.pos[i / p.HD];
+    if (P < 0 || P >= p.T_max) p.attn[i] = 0;
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------ kernel
+__global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  Ctx c;
+  {  // align the shared-space address to 1024 B (swizzle atoms, TMA boxes)
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    c.smem = smem_raw + pad;
+    c.sbase = raw + pad;
+  }
+  c.lay = smem_layout();
+  c.bar_target = 0;
+  c.bar_index = 0;
+  c.ring_it = c.acc_it = c.att_it = 0;
+  const int warp = threadIdx.x >> 5;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kMaxStages; ++i) {
+      mbar_init(bar_full(c, i), 1);
+      mbar_init(bar_empty(c, i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_accf(c, i), 1);
+      mbar_init(bar_acce(c, i), 4);
+    }
+    for (int w = 0; w < kWarps; ++w)
+      for (int st = 0; st < kAttStages; ++st) mbar_init(bar_att(c, w, st), 1);
+    mbar_init(bar_drain(c), 1);
+    fence_mbar_init();
+    for (int i = 0; i < 4; ++i) {
+      prefetch_tmap(&p.tm_w[i]);
+      prefetch_tmap(&p.tm_x[i]);
+    }
+    prefetch_tmap(&p.tm_kv);
+  }
+  if (warp == 1) {
+    tmem_alloc(c.sbase + c.lay.misc_off, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  c.tmem = *(volatile uint32_t*)(c.smem + c.lay.misc_off);
+
+  // phase 0: work list, counter reset, residual and first norm
+  for (int i = blockIdx.x * kThreads + threadIdx.x; i < p.S_max * p.H; i += gridDim.x * kThreads)
+    p.sh_cnt[i] = 0;
+  for (int i = blockIdx.x * kThreads + threadIdx.x; i < 1024; i += gridDim.x * kThreads)
+    p.tile_cnt[i] = 0;
+  if (blockIdx.x == gridDim.x - 1) build_pieces(p, c);
+  norm_phase(p, c, p.weights + p.off_g_attn, true);
+  bool ok = grid_sync(p, c);
+
+  for (int l = 0; ok && l < p.L; ++l) {
+    const uint16_t* wl = p.weights + (size_t)l * p.layer_elems;
+    if (l > 0) {
+      norm_phase(p, c, wl + p.off_g_attn, false);
+      if (!(ok = grid_sync(p, c))) break;
+    }
+    gemm_phase(p, c, kQKV, l, false);
+    if (!(ok = grid_sync(p, c))) break;
+    if (p.D == 128) attention_phase<128>(p, c, l); else attention_phase<64>(p, c, l);
+    if (!(ok = grid_sync(p, c))) break;
+    gemm_phase(p, c, kO, l, false);
+    if (!(ok = grid_sync(p, c))) break;
+    norm_phase(p, c, wl + p.off_g_mlp, false);
+    if (!(ok = grid_sync(p, c))) break;
+    gemm_phase(p, c, kGU, l, false);
+    if (!(ok = grid_sync(p, c))) break;
+    gemm_phase(p, c, kDown, l, l == p.L - 1);
+    if (l < p.L - 1 && !(ok = grid_sync(p, c))) break;
+  }
+
+  if (!ok) {
+    // Abort path: let outstanding tensor-core work finish before TMEM is freed.
+    if (warp == 1 && (threadIdx.x & 31) == 0) {
+      tc_commit(bar_drain(c));
+      mbar_wait(bar_drain(c), 0, 100000000LL, p.err);
+    }
+    if (warp == 0 && (threadIdx.x & 31) == 0) {
+      // wait (bounded) for the most recent ring loads
+      const uint32_t nst = (uint32_t)p.nstage;
+      for (uint32_t k = 0; k < nst && k < c.ring_it; ++k) {
+        const uint32_t it = c.ring_it - 1 - k;
+        long long t0 = globaltimer();
+        while (!mbar_try_wait(bar_full(c, it % nst), (it / nst) & 1u) && globaltimer() - t0 < 100000000LL) {
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(c.tmem, kTmemCols);
+}
+
+cudaError_t configure_step_kernel() {
+  return cudaFuncSetAttribute(step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              smem_layout().total);
+}
+
+cudaError_t launch_step(const StepParams& p, int grid, cudaStream_t stream) {
+  void* args[] = {(void*)&p};
+  return cudaLaunchCooperativeKernel((const void*)step_kernel, dim3(grid), dim3(kThreads), args,
+                                     (size_t)smem_layout().total, stream);
+}
+
+int barriers_per_step(int L) { return 7 * L - 1; }
+
+cudaError_t occupancy_per_sm(int* blocks) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel, kThreads,
+                                                       (size_t)smem_layout().total);
+}
+
+}  // namespace wave

@@ -1,0 +1,164 @@
+/*
+ * wave.h -- C ABI of the frame-locked batched decode step for one GB300
+ * (sm_103a).  One call advances every live session by one 80 ms frame through
+ * all decoder layers in a single persistent GPU launch; each bf16 weight is
+ * read from HBM once per step and shared by all S sessions.
+ *
+ * The operation follows the pages' description of the frame step:
+ *   - "PersonaPlex 7B, 80 sessions, one H100" (narilabs blog): "What Real-time
+ *     Means for a Full-duplex Agent" (one 80 ms frame per forward pass),
+ *     "Compressing the Temporal KV cache" (bf16 weights and activations, FP8
+ *     temporal K/V cache), "A server built around the conversation clock"
+ *     (every session on one clock, fixed-shape batches, slots filled by new
+ *     sessions without changing execution);
+ *   - dotwave.ai case study, "02 / The solution" and "04 / Under the hood"
+ *     (weights shared across sessions, state resident between beats, no CPU
+ *     round trip between operations, profiles per session capacity and
+ *     context length).
+ * The decoder layer itself (RMSNorm, QKV, RoPE, FP8 K/V append, attention,
+ * output projection, SwiGLU MLP) is not spelled out on the pages; the
+ * readings taken are listed with wave_step below.
+ *
+ * Conventions.  Every pointer passed to wave_step / wave_kv_quantize /
+ * wave_fp8_encode is a DEVICE pointer owned by the caller.  Nothing returned
+ * by this library needs freeing except a handle (wave_destroy).  Functions
+ * return WAVE_OK (0) or a negative WAVE_E* code; no function aborts the
+ * process or traps the GPU.  A handle is used by one stream at a time.
+ */
+#ifndef WAVE_H_
+#define WAVE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define WAVE_OK 0
+#define WAVE_EINVAL (-1)   /* bad argument: null pointer, size out of range, misalignment */
+#define WAVE_ECUDA (-2)    /* a CUDA runtime/driver call failed */
+#define WAVE_ELAUNCH (-3)  /* the persistent grid could not be made co-resident */
+#define WAVE_ETIMEOUT (-4) /* a device-side wait (grid barrier, async copy) gave up */
+#define WAVE_EPOS (-5)     /* a session's position was outside [0, T_max) */
+#define WAVE_EDEVICE (-6)  /* the current device is not an sm_103 GPU */
+#define WAVE_ENOMEM (-7)   /* device allocation failed */
+
+/* Decoder shape.  Constraints checked by wave_create: head_dim is 64 or 128;
+ * d_model, n_heads*head_dim and ffn are multiples of 64, 64 and 8. */
+typedef struct {
+  int n_layers, d_model, n_heads, head_dim, ffn;
+  float rms_eps, rope_base;
+} wave_config;
+
+typedef struct wave_ctx wave_t; /* opaque; owns only its device workspace */
+
+/*
+ * Create a step context for at most S_max sessions (1..128) and a history of
+ * T_max slots per session (a multiple of 4).  This is the pages' "profile per
+ * model, session capacity and context length" (dotwave.ai "04 / Under the
+ * hood").  Allocates the device workspace on the current device (activations,
+ * partial sums, the RoPE cos/sin table, barrier words); about
+ * 0.5 MB + S_max * (2.1 * d_model + ...) bytes, e.g. ~60 MB for the 7B-class
+ * shape at S_max = 128.  Returns WAVE_EINVAL for a bad shape, WAVE_EDEVICE off
+ * sm_103, WAVE_ENOMEM/WAVE_ECUDA on failure; *out is set only on success.
+ */
+int wave_create(const wave_config* cfg, int S_max, int T_max, wave_t** out);
+
+/* Free the workspace.  Waits for the handle's work to finish.  NULL is a no-op. */
+void wave_destroy(wave_t* h);
+
+/* Bytes of the bf16 weight blob for cfg (see wave_weight_offset). */
+size_t wave_weights_bytes(const wave_config* cfg);
+
+/*
+ * Byte offset inside the weight blob of one tensor of one layer.  which:
+ *   0 g_attn  [d]            RMSNorm gain before attention
+ *   1 Wqkv    [3*H*D][d]     rows: q (H*D), then k (H*D), then v (H*D)
+ *   2 Wo      [d][H*D]
+ *   3 g_mlp   [d]            RMSNorm gain before the MLP
+ *   4 Wgu     [2*F][d]       rows: gate (F), then up (F)
+ *   5 Wdown   [d][F]
+ * All bf16, each matrix [out][in] with the in-dimension contiguous; layers are
+ * stored one after another in this order.  Returns (size_t)-1 on bad input.
+ */
+size_t wave_weight_offset(const wave_config* cfg, int layer, int which);
+
+/*
+ * One frame for sessions 0..S-1 (1 <= S <= S_max).  Asynchronous: enqueues
+ * two operations on `stream` (a 4-byte memset of the barrier word and one
+ * cooperative kernel launch) and returns; nothing is synchronised.
+ *
+ *   weights    bf16 blob, layout of wave_weight_offset, 16-byte aligned, read only.
+ *   kv_fp8     uint8 [L][2][S_max][H][T_max][D] E4M3 codes (index 0 = K, 1 = V),
+ *              16-byte aligned.  Slots 0..pos[s]-1 are read; slot pos[s] of every
+ *              (layer, K|V, s, head) is written; no other byte is touched.
+ *   kv_scales  float [L][2][S_max][H][T_max], 16-byte aligned: one scale per
+ *              (layer, K|V, session, head, token) with value = code * scale.
+ *   positions  int32 [S]: pos[s] is the RoPE position of this frame and the
+ *              cache slot it writes; attention spans slots 0..pos[s] inclusive.
+ *              Input only: the caller advances positions between frames.
+ *   x          bf16 [S][d] input activations; y bf16 [S][d] output (may alias x).
+ *
+ * Readings of what the pages leave open: bf16 rounding only at the projection
+ * inputs (normed x, attention output, SwiGLU output) and at y, fp32 elsewhere;
+ * RMSNorm r / sqrt(mean(r^2) + eps) * g; rotate-half RoPE, pairs (i, i+D/2),
+ * angle pos * base^(-2i/D); the current token's K/V are quantised first and
+ * read back quantised; scale = amax/448 in fp32, code = E4M3-RNE-satfinite of
+ * v/scale (fp32 division), all-zero codes and scale 0 for a zero row; softmax
+ * scale 1/sqrt(D); SwiGLU silu(gate) * up; no biases, no final norm.
+ *
+ * A session whose pos is outside [0, T_max) gets no cache write and a zero
+ * attention output; the step records WAVE_EPOS for wave_status.
+ * Returns WAVE_EINVAL for bad arguments (checked on the host before any
+ * launch), WAVE_ELAUNCH/WAVE_ECUDA if the launch fails.
+ */
+int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8, float* kv_scales,
+              const int32_t* positions, const void* x, void* y, void* stream);
+
+/*
+ * Synchronise the stream of the last wave_step on this handle, then return
+ * and clear the device error word: WAVE_OK, WAVE_ETIMEOUT (a device wait gave
+ * up; the step's outputs are undefined, the GPU context stays usable) or
+ * WAVE_EPOS.  Returns WAVE_ECUDA if the synchronisation itself failed.
+ */
+int wave_status(wave_t* h);
+
+/* Static description of a return code. */
+const char* wave_strerror(int code);
+
+/*
+ * FP8 quantiser of the K/V append, on its own: for each of `rows` rows of D
+ * fp32 values (row-major, device), scale = amax/448 and codes = E4M3(v/scale)
+ * exactly as wave_step writes them.  Used to prefill a history.  Writes
+ * codes [rows][D] and scales [rows].  Asynchronous on `stream`.
+ * D must be a multiple of 4 in [4, 1024].
+ */
+int wave_kv_quantize(const float* v, int64_t rows, int D, uint8_t* codes, float* scales,
+                     void* stream);
+
+/* Element-wise E4M3 encoder of the step (round to nearest even, saturate to
+ * +-448, sign kept): out[i] = E4M3(in[i]).  Asynchronous on `stream`. */
+int wave_fp8_encode(const float* in, int64_t n, uint8_t* out, void* stream);
+
+/* ---- testing hooks (fault tests without a GPU fault) ---------------------
+ * Limit for every device-side wait of later steps, in nanoseconds (default
+ * 2e9).  A wait that runs out sets WAVE_ETIMEOUT and the kernel returns. */
+int wave_set_timeout_ns(wave_t* h, long long ns);
+/* Make CTA `cta` skip its arrival at grid barrier number `barrier` (0-based)
+ * in later steps, so that the others' waits run out; cta < 0 disables. */
+int wave_debug_skip_barrier(wave_t* h, int cta, int barrier);
+/* Make later steps also write, for every session with a valid position, the
+ * fp32 K (after RoPE) and V rows they quantise into dst, a device buffer of
+ * [L][2][S_max][H][D] floats, so that tests can check the append bit for bit
+ * against a reference quantiser.  dst = NULL disables. */
+int wave_debug_dump_kv(wave_t* h, float* dst);
+/* Grid size (CTAs, one per SM) and barriers per step, for tests and tools. */
+int wave_grid_size(wave_t* h);
+int wave_barriers_per_step(wave_t* h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WAVE_H_ */

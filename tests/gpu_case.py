@@ -1,0 +1,88 @@
+"""Shared set-up for the GPU tests: seeded inputs on the device (through the
+library's own quantiser for the FP8 history) and the same inputs for the CPU
+oracle (through the oracle's quantiser).  Test infrastructure only."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import frame_step_decode_gb300 as fsd
+import oracle
+import synth
+
+POISON_CODE = 0x7F
+
+
+class DeviceCase:
+    """Device buffers of one workload at S sessions (S_max = S unless given)."""
+
+    def __init__(self, w, S=None, S_max=None, poison=True, device_gen=False, pos=None):
+        self.w = w
+        self.S = w.S if S is None else S
+        self.S_max = self.S if S_max is None else S_max
+        self.cfg = fsd.WaveConfig.of(w)
+        L, H, T, D = w.n_layers, w.n_heads, w.T_max, w.head_dim
+        dev = "cuda"
+        self.pos_h = synth.positions(w, self.S) if pos is None else np.asarray(pos, dtype=np.int32)
+        self.pos = torch.from_numpy(self.pos_h).to(dev)
+        self.x_h = synth.x_bf16(w, self.S)
+        self.x = torch.from_numpy(self.x_h.view(np.int16)).to(dev).view(torch.bfloat16)
+        self.y = torch.zeros_like(self.x)
+        n_w = synth.weight_elems(w)
+        if device_gen:
+            self.weights = torch.empty(n_w, dtype=torch.bfloat16, device=dev)
+            synth.weights_device(w, self.weights, torch.cuda.current_stream().cuda_stream)
+        else:
+            self.W_h = synth.weights_host(w)
+            self.weights = torch.from_numpy(self.W_h.view(np.int16)).to(dev).view(torch.bfloat16)
+        self.kv = torch.zeros((L, 2, self.S_max, H, T, D), dtype=torch.uint8, device=dev)
+        self.sc = torch.zeros((L, 2, self.S_max, H, T), dtype=torch.float32, device=dev)
+        stream = torch.cuda.current_stream().cuda_stream
+        raw = torch.empty((self.S, H, T, D), dtype=torch.float32, device=dev)
+        for l in range(L):
+            for which in range(2):
+                if device_gen:
+                    synth.kv_raw_device(w, l, which, 0, self.S, T, raw.data_ptr(), T, stream)
+                else:
+                    raw.copy_(torch.from_numpy(synth.kv_raw_host(w, l, which, 0, self.S, T)))
+                fsd.kv_quantize(raw, self.kv[l, which, :self.S], self.sc[l, which, :self.S])
+        del raw
+        if poison:
+            t = torch.arange(T, device=dev)
+            mask = t[None, :] >= self.pos.long()[:, None]  # [S][T]
+            m5 = mask[None, None, :, None, :].expand(L, 2, self.S, H, T)
+            self.kv[:, :, :self.S][m5] = POISON_CODE
+            self.sc[:, :, :self.S][m5] = float("nan")
+        torch.cuda.synchronize()
+
+    def y_bits(self) -> np.ndarray:
+        """y as bf16 bit patterns (uint16) on the host."""
+        return self.y.view(torch.int16).cpu().numpy().view(np.uint16)
+
+    def step(self, wave, S=None, stream=None):
+        return wave.step(self.S if S is None else S, self.weights, self.kv, self.sc, self.pos,
+                         self.x, self.y, stream=stream)
+
+
+def oracle_reference(w, sessions, pos, x_rows, W_h=None):
+    """Oracle y (bf16 bits), y_exact and the history it wrote, for the listed
+    sessions, from the oracle's own quantiser applied to the shared raw
+    values."""
+    W = synth.weights_host(w) if W_h is None else W_h
+    pos = np.asarray(pos, dtype=np.int32)
+    kv, sc = oracle.prefill_history(w, list(sessions), pos, poison=True)
+    y, y_exact, kv_new = oracle.step(w, W, kv, sc, pos, np.ascontiguousarray(x_rows),
+                                     want_kv_new=True)
+    return y, y_exact, kv, sc, kv_new
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    return synth.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def y_close(y_gpu_bits, y_ref_exact, atol=1e-3, rtol=2e-2):
+    """Element-wise |y - y_ref| <= atol + rtol * |y_ref| (the stated bound)."""
+    y = bf16_to_f64(y_gpu_bits)
+    err = np.abs(y - y_ref_exact)
+    bound = atol + rtol * np.abs(y_ref_exact)
+    return bool(np.all(err <= bound)), float(np.max(err / bound))

@@ -1,0 +1,41 @@
+"""CPU: the step library builds, loads, and exports every symbol that
+include/wave.h declares (no compute call: there may be no GPU here)."""
+import os
+import re
+
+import frame_step_decode_gb300 as fsd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    txt = open(os.path.join(ROOT, "include", "wave.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(wave_[a-z_0-9]+)\s*\(", txt)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = fsd.lib()
+    names = declared_symbols()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(fsd.EXPORTS)
+
+
+def test_weight_layout_matches_the_generator_layout():
+    import synth
+    for w in (synth.TINY, synth.SEVEN_B, synth.MID):
+        cfg = fsd.WaveConfig.of(w)
+        lay = synth.layer_layout(w)
+        assert fsd.weights_bytes(cfg) == 2 * synth.weight_elems(w)
+        for which, name in enumerate(("g_attn", "wqkv", "wo", "g_mlp", "wgu", "wdown")):
+            assert fsd.weight_offset(cfg, 1, which) == 2 * (lay["layer"] + lay[name])
+    assert fsd.weights_bytes(fsd.WaveConfig.of(synth.SEVEN_B)) == 12_952_535_040
+
+
+def test_strerror_and_bad_layout_queries():
+    assert fsd.strerror(fsd.WAVE_ETIMEOUT) == "a device-side wait timed out"
+    bad = fsd.WaveConfig(2, 256, 4, 96, 688, 1e-5, 1e4)
+    assert fsd.weights_bytes(bad) == 0
+    assert fsd.weight_offset(bad, 0, 0) == (1 << 64) - 1

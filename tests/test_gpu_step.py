@@ -1,0 +1,208 @@
+"""GPU parity of wave_step against the CPU oracle, plus its invariants and
+error paths.  Shapes: the tiny workload, and a 3-layer d=512 shape whose
+every dimension has a ragged tail (S = 19, F = 1376, positions up to 319)."""
+import numpy as np
+import pytest
+import torch
+
+import frame_step_decode_gb300 as fsd
+import synth
+from gpu_case import DeviceCase, oracle_reference, y_close
+
+pytestmark = pytest.mark.gpu
+
+KV_RTOL = 2e-2  # pre-quantisation K/V against the oracle's, per row (normwise)
+
+
+def _check_case(case: DeviceCase, wave, sessions=None):
+    """y within the stated bound; every appended code and scale equal, bit for
+    bit, to the oracle quantiser applied to the GPU's own pre-quantisation
+    K/V rows; those rows close to the oracle's; no other history byte moved."""
+    import oracle
+    w = case.w
+    sessions = list(range(case.S)) if sessions is None else sessions
+    L, H, D = w.n_layers, w.n_heads, w.head_dim
+    kv_before = case.kv.clone()
+    sc_before = case.sc.clone()
+    dump = torch.full((L, 2, case.S_max, H, D), float("nan"), device="cuda")
+    wave.debug_dump_kv(dump)
+    try:
+        case.step(wave)
+        assert wave.status() == fsd.WAVE_OK
+    finally:
+        wave.debug_dump_kv(None)
+    y = case.y_bits()
+    pos = case.pos_h[sessions]
+    _, y_exact, kv_ref, sc_ref, kv_new = oracle_reference(w, sessions, pos, case.x_h[sessions])
+    ok, worst = y_close(y[sessions], y_exact)
+    assert ok, f"y outside |dy| <= 1e-3 + 2e-2|y|: worst ratio {worst:.3f}"
+    kv_g = case.kv.cpu().numpy()
+    sc_g = case.sc.cpu().numpy()
+    dump_h = dump.cpu().numpy()
+    idx = np.arange(case.S)
+    P = case.pos_h.astype(np.int64)
+    got_codes = kv_g[:, :, idx, :, P]          # [S][L][2][H][D] (advanced index first)
+    got_sc = sc_g[:, :, idx, :, P]             # [S][L][2][H]
+    pre = np.ascontiguousarray(np.moveaxis(dump_h[:, :, :case.S], 2, 0))  # [S][L][2][H][D]
+    assert np.all(np.isfinite(pre))
+    ref_codes, ref_sc = oracle.quantize_rows(pre)
+    assert np.array_equal(got_codes, ref_codes), "appended codes differ from the oracle quantiser"
+    assert np.array_equal(got_sc.view(np.uint32), ref_sc.view(np.uint32))
+    # the GPU's pre-quantisation rows against the oracle's (fp64 path)
+    for j, s in enumerate(sessions):
+        a = pre[s].astype(np.float64)
+        b = kv_new[:, :, j].astype(np.float64)
+        err = np.max(np.abs(a - b), axis=-1)
+        ref = np.max(np.abs(b), axis=-1)
+        assert np.all(err <= KV_RTOL * ref + 1e-6), float(np.max(err / (ref + 1e-30)))
+    # every other byte of the history is untouched
+    mask = torch.ones(case.kv.shape[:5], dtype=torch.bool, device="cuda")
+    for s in range(case.S):
+        mask[:, :, s, :, int(case.pos_h[s])] = False
+    assert torch.equal(case.kv[mask], kv_before[mask])
+    assert torch.equal(torch.nan_to_num(case.sc[mask], nan=-7.0), torch.nan_to_num(sc_before[mask], nan=-7.0))
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    w = synth.TINY
+    case = DeviceCase(w)
+    wave = fsd.Wave(case.cfg, case.S_max, w.T_max)
+    yield case, wave
+    wave.close()
+
+
+@pytest.fixture(scope="module")
+def mid():
+    w = synth.MID
+    case = DeviceCase(w)
+    wave = fsd.Wave(case.cfg, case.S_max, w.T_max)
+    yield case, wave
+    wave.close()
+
+
+def test_tiny_step_matches_oracle(tiny):
+    case, wave = tiny
+    _check_case(case, wave)
+
+
+def test_mid_step_matches_oracle(mid):
+    case, wave = mid
+    _check_case(case, wave)
+
+
+@pytest.mark.parametrize("S", [1, 2, 7, 16, 17])
+def test_ragged_batch_sizes(S):
+    w = synth.MID
+    case = DeviceCase(w, S=S, S_max=19)
+    wave = fsd.Wave(case.cfg, 19, w.T_max)
+    try:
+        _check_case(case, wave)
+    finally:
+        wave.close()
+
+
+def test_edge_positions():
+    w = synth.MID
+    pos = np.array([0, 1, 63, 64, 65, 255, 256, 257, w.T_max - 1, 127, 128, 129], dtype=np.int32)
+    case = DeviceCase(w, S=pos.size, pos=pos)
+    wave = fsd.Wave(case.cfg, case.S_max, w.T_max)
+    try:
+        _check_case(case, wave)
+    finally:
+        wave.close()
+
+
+def test_batch_invariance_and_determinism():
+    w = synth.MID
+    big = DeviceCase(w, S=19)
+    wave = fsd.Wave(big.cfg, 19, w.T_max)
+    try:
+        kv0, sc0 = big.kv.clone(), big.sc.clone()
+        big.step(wave)
+        assert wave.status() == fsd.WAVE_OK
+        y_big = big.y.view(torch.int16).clone()
+        # same inputs again: identical bits
+        big.kv.copy_(kv0)
+        big.sc.copy_(sc0)
+        big.step(wave)
+        assert wave.status() == fsd.WAVE_OK
+        assert torch.equal(big.y.view(torch.int16), y_big)
+        # a smaller batch (a prefix of the same draws) gives the same bits
+        small = DeviceCase(w, S=5, S_max=19)
+        small.step(wave)
+        assert wave.status() == fsd.WAVE_OK
+        assert torch.equal(small.y.view(torch.int16), y_big[:5])
+        # changing the other sessions' inputs leaves session 0 unchanged
+        big.kv.copy_(kv0)
+        big.sc.copy_(sc0)
+        big.x[1:] = -big.x[1:]
+        big.step(wave)
+        assert torch.equal(big.y.view(torch.int16)[0], y_big[0])
+    finally:
+        wave.close()
+
+
+def test_invalid_arguments_are_rejected(tiny):
+    case, wave = tiny
+    for S in (0, -1, case.S_max + 1):
+        assert case.step.__self__ is case
+        rc = wave.step(S, case.weights, case.kv, case.sc, case.pos, case.x, case.y, check=False)
+        assert rc == fsd.WAVE_EINVAL
+    rc = wave.step(case.S, 0, case.kv, case.sc, case.pos, case.x, case.y, check=False)
+    assert rc == fsd.WAVE_EINVAL
+    rc = wave.step(case.S, case.weights.data_ptr() + 2, case.kv, case.sc, case.pos, case.x, case.y,
+                   check=False)
+    assert rc == fsd.WAVE_EINVAL
+    bad = fsd.WaveConfig(2, 256, 4, 96, 688, 1e-5, 1e4)
+    with pytest.raises(fsd.WaveError):
+        fsd.Wave(bad, 4, 64)
+    with pytest.raises(fsd.WaveError):
+        fsd.Wave(case.cfg, 129, 64)
+    with pytest.raises(fsd.WaveError):
+        fsd.Wave(case.cfg, 4, 62)
+
+
+def test_out_of_range_position_is_reported_and_skipped():
+    w = synth.TINY
+    case = DeviceCase(w)
+    wave = fsd.Wave(case.cfg, case.S_max, w.T_max)
+    try:
+        bad = case.pos.clone()
+        bad[2] = w.T_max
+        kv0 = case.kv.clone()
+        rc = wave.step(case.S, case.weights, case.kv, case.sc, bad, case.x, case.y)
+        assert rc == fsd.WAVE_OK
+        assert wave.status() == fsd.WAVE_EPOS
+        # no cache byte of session 2 changed
+        assert torch.equal(case.kv[:, :, 2], kv0[:, :, 2])
+        # the other sessions still match the oracle
+        y = case.y_bits()
+        sess = [0, 1, 3]
+        _, y_exact, _, _, _ = oracle_reference(w, sess, case.pos_h[sess], case.x_h[sess])
+        ok, worst = y_close(y[sess], y_exact)
+        assert ok, worst
+        assert wave.status() == fsd.WAVE_OK  # cleared by the previous read
+    finally:
+        wave.close()
+
+
+def test_barrier_timeout_is_reported_and_context_survives():
+    w = synth.TINY
+    case = DeviceCase(w)
+    wave = fsd.Wave(case.cfg, case.S_max, w.T_max)
+    try:
+        wave.set_timeout_ns(20_000_000)  # 20 ms
+        wave.debug_skip_barrier(3, 5)
+        case.step(wave)
+        assert wave.status() == fsd.WAVE_ETIMEOUT
+        wave.debug_skip_barrier(-1, -1)
+        wave.set_timeout_ns(2_000_000_000)
+        fresh = DeviceCase(w)
+        fresh.step(wave)
+        assert wave.status() == fsd.WAVE_OK
+        y = fresh.y_bits()
+        _, y_exact, _, _, _ = oracle_reference(w, range(fresh.S), fresh.pos_h, fresh.x_h)
+        assert y_close(y, y_exact)[0]
+    finally:
+        wave.close()
