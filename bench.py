@@ -1,0 +1,380 @@
+"""Benchmark of the frame-locked batched decode step (one JSON line).
+
+Default workload: the 7B-class temporal-transformer frame step (32 layers,
+d=4096, 32 heads x 128, SwiGLU 11008, bf16 weights, FP8 e4m3 K/V history
+with per-(session, head, token) scales), S = 80 sessions, positions uniform
+in [0, 3000).  Metric: session-frames/s = S / step time, with p50/p99 step
+latency and the HBM roofline fraction of the step kernel.
+
+  python bench.py [--gpus N --steps K --warmup W] [--S 80] [--impl reference]
+
+Inputs are seeded and synthetic and are drawn on the device (weights and the
+raw history by the generator's device twin, the history quantised by the
+library's own quantiser); every input is far larger than L2, so no flush is
+needed between steps.  With --gpus N > 1 (launched by torchrun) every rank
+runs an independent replica of S sessions on its own GPU: sessions shard
+with no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "session-frames/s"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "step_kernel_7b_traffic.txt")
+FALLBACK_HBM_GBS = 6800.0
+STEP_SRC = os.path.join(ROOT, "frame_step_decode_gb300", "csrc", "step.cu")
+
+
+def algorithmic_bytes(w, pos) -> int:
+    """Weights once + FP8 K/V codes and scales of slots 0..pos read + the
+    appended slot written, per step."""
+    L, H, D = w.n_layers, w.n_heads, w.head_dim
+    weights = 2 * synth.weight_elems(w)
+    kv_read = sum(L * 2 * H * (int(p) + 1) * (D + 4) for p in pos)
+    kv_write = L * 2 * len(pos) * H * (D + 4)
+    return weights + kv_read + kv_write
+
+
+def algorithmic_flops(w, pos) -> int:
+    L, H, D, d, F = w.n_layers, w.n_heads, w.head_dim, w.d_model, w.ffn
+    HD = H * D
+    gemm = 2 * len(pos) * L * (3 * HD * d + d * HD + 2 * F * d + d * F)
+    attn = sum(4 * D * L * H * (int(p) + 1) for p in pos)
+    return gemm + attn
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            for k in ("hbm_gbs", "hbm_GBps", "hbm"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_per_launch():
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    vals = {}
+    for line in open(PROFILE_TRAFFIC):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    src_sha = hashlib.sha256(open(STEP_SRC, "rb").read()).hexdigest()[:16]
+    if vals.get("step_cu_sha256_16") != src_sha:
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_full_launch"]))
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- oracle arm
+def oracle_session_time(w, sessions, pos):
+    """Time the CPU oracle for the listed sessions of workload w (its inputs
+    prepared outside the timed region).  Returns (seconds, threads)."""
+    import oracle
+    W = synth.weights_host(w)
+    x = synth.x_bf16(w)[sessions]
+    p = np.asarray(pos)[sessions].astype(np.int32)
+    kv, sc = oracle.prefill_history(w, sessions, p, poison=False)
+    t0 = time.perf_counter()
+    oracle.step(w, W, kv, sc, p, x)
+    dt = time.perf_counter() - t0
+    return dt, os.cpu_count()
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    pos = synth.positions(w, args.S)
+    W = synth.weights_host(w)
+    sess = [0]
+    x = synth.x_bf16(w)[sess]
+    p = pos[sess]
+    kv, sc = oracle.prefill_history(w, sess, p, poison=False)
+    kv0, sc0 = kv.copy(), sc.copy()
+    for _ in range(min(args.warmup, 1)):
+        oracle.step(w, W, kv, sc, p, x)
+    times = []
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        kv[...] = kv0
+        sc[...] = sc0
+        t0 = time.perf_counter()
+        oracle.step(w, W, kv, sc, p, x)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    ms = 1000 * total / args.steps
+    value = len(sess) / (total / args.steps)
+    sample = f"1 of {args.S} sessions (session 0, pos {int(p[0])}) of {w.name}, per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": METRIC, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": min(args.warmup, 1), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "S": args.S, "T_max": w.T_max,
+                   "positions": f"uniform [{w.pos_lo}, {w.pos_hi})"},
+        "cpu_baseline": {"value": value, "unit": METRIC, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": METRIC, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": time.perf_counter() - t_all,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def build_inputs(w, S, device):
+    import torch
+    import frame_step_decode_gb300 as fsd
+    stream = torch.cuda.current_stream().cuda_stream
+    L, H, T, D = w.n_layers, w.n_heads, w.T_max, w.head_dim
+    weights = torch.empty(synth.weight_elems(w), dtype=torch.bfloat16, device=device)
+    synth.weights_device(w, weights, stream)
+    kv = torch.empty((L, 2, S, H, T, D), dtype=torch.uint8, device=device)
+    sc = torch.empty((L, 2, S, H, T), dtype=torch.float32, device=device)
+    raw = torch.empty((S, H, T, D), dtype=torch.float32, device=device)
+    for l in range(L):
+        for which in range(2):
+            synth.kv_raw_device(w, l, which, 0, S, T, raw.data_ptr(), T, stream)
+            fsd.kv_quantize(raw, kv[l, which], sc[l, which])
+    del raw
+    pos_h = synth.positions(w, S)
+    pos = torch.from_numpy(pos_h).to(device)
+    x = torch.empty((S, w.d_model), dtype=torch.bfloat16, device=device)
+    synth.x_device(w, S, x.data_ptr(), stream)
+    y = torch.empty_like(x)
+    torch.cuda.synchronize()
+    return weights, kv, sc, pos, pos_h, x, y
+
+
+def run_gpu(args, w):
+    import torch
+    import frame_step_decode_gb300 as fsd
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    S = args.S
+    weights, kv, sc, pos, pos_h, x, y = build_inputs(w, S, device)
+    wave = fsd.Wave(fsd.WaveConfig.of(w), S, w.T_max)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        wave.step(S, weights, kv, sc, pos, x, y, stream=stream)
+    rc = wave.status()
+    if rc != fsd.WAVE_OK:
+        raise RuntimeError(f"warm-up step failed: {fsd.strerror(rc)}")
+
+    # ---- device-resident timed region
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev0[i].record(stream)
+        wave.step(S, weights, kv, sc, pos, x, y, stream=stream)
+        ev1[i].record(stream)
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    rc = wave.status()
+    if rc != fsd.WAVE_OK:
+        raise RuntimeError(f"timed step failed: {fsd.strerror(rc)}")
+    per = [ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)]
+    total_ms = t_start.elapsed_time(t_end)
+
+    # ---- end to end through the C ABI with host buffers
+    x_host = x.cpu().pin_memory()
+    pos_host = pos.cpu().pin_memory()
+    y_host = torch.empty_like(y, device="cpu").pin_memory()
+    for _ in range(2):
+        x.copy_(x_host, non_blocking=True)
+        pos.copy_(pos_host, non_blocking=True)
+        wave.step(S, weights, kv, sc, pos, x, y, stream=stream)
+        y_host.copy_(y, non_blocking=True)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x.copy_(x_host, non_blocking=True)
+        pos.copy_(pos_host, non_blocking=True)
+        wave.step(S, weights, kv, sc, pos, x, y, stream=stream)
+        y_host.copy_(y, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = x.numel() * 2 + pos.numel() * 4
+    d2h = y.numel() * 2
+
+    ms_per_step = total_ms / args.steps
+    if dist is not None:
+        t = torch.tensor([ms_per_step, e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step, e2e_ms = float(t[0]), float(t[1])
+    if rank == 0:
+        bytes_step = algorithmic_bytes(w, pos_h)
+        flops_step = algorithmic_flops(w, pos_h)
+        kern_ms = statistics.mean(per)
+        peak, peak_kind = measured_peaks()
+        achieved = bytes_step / (kern_ms * 1e-3) / 1e9
+        traffic = traffic_per_launch()
+        line = {
+            "metric": METRIC,
+            "value": world * S / (ms_per_step * 1e-3),
+            "unit": METRIC,
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms_per_step,
+            "p50_ms": statistics.median(per),
+            "p99_ms": float(np.percentile(per, 99)),
+            "late_frames_over_80ms": int(sum(1 for t in per if t > 80.0)),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded; weights N(0,0.02) bf16, x N(0,1), FP8 e4m3 history of N(0,1))",
+            "config": {"workload": w.name, "S": S, "T_max": w.T_max,
+                       "positions": f"uniform [{w.pos_lo}, {w.pos_hi})", "kv": "e4m3 + fp32 scales",
+                       "parallelism": f"replicas x{world} (sessions shard, no collective)",
+                       "l2": "inputs larger than L2 (no flush needed)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                         "frac_of_8000": achieved / 8000.0,
+                         "algorithmic_bytes_per_launch": bytes_step,
+                         "tflops": flops_step / (kern_ms * 1e-3) / 1e12},
+            "e2e": {"value": world * S / (e2e_ms * 1e-3), "unit": METRIC, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "clocks": clk,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            try:
+                dt, cores = oracle_session_time(w, [0], pos_h)
+                line["cpu_baseline"] = {"value": 1.0 / dt, "unit": METRIC, "cores": cores,
+                                        "kind": "oracle",
+                                        "sample": f"1 of {S} sessions (session 0, pos {int(pos_h[0])}) of "
+                                                  f"{w.name}, one frame"}
+            except Exception as e:  # the GPU number stands without it
+                line["cpu_baseline"] = {"value": None, "unit": METRIC, "cores": os.cpu_count(),
+                                        "kind": "oracle", "sample": f"failed: {e}"}
+        print(json.dumps(line), flush=True)
+    wave.close()
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--S", type=int, default=80)
+    ap.add_argument("--layers", type=int, default=None, help="fewer layers (profiling a small case)")
+    ap.add_argument("--tmax", type=int, default=None, help="shorter history (profiling a small case)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+    w = synth.SEVEN_B
+    if args.layers or args.tmax:
+        from dataclasses import replace
+        T = args.tmax or w.T_max
+        w = replace(w, n_layers=args.layers or w.n_layers, T_max=T, pos_hi=min(w.pos_hi, T),
+                    name=f"{w.name}-L{args.layers or w.n_layers}-T{T}")
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

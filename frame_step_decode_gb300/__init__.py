@@ -36,7 +36,8 @@ class WaveError(RuntimeError):
 _lib = None
 EXPORTS = ("wave_create", "wave_destroy", "wave_weights_bytes", "wave_weight_offset", "wave_step",
            "wave_status", "wave_strerror", "wave_kv_quantize", "wave_fp8_encode",
-           "wave_set_timeout_ns", "wave_debug_skip_barrier", "wave_debug_dump_kv", "wave_grid_size",
+           "wave_set_timeout_ns", "wave_debug_skip_barrier", "wave_debug_dump_kv", "wave_debug_phase_times",
+           "wave_grid_size",
            "wave_barriers_per_step")
 
 
@@ -72,6 +73,8 @@ def lib() -> ctypes.CDLL:
         L.wave_debug_skip_barrier.restype = i32
         L.wave_debug_dump_kv.argtypes = [vp, vp]
         L.wave_debug_dump_kv.restype = i32
+        L.wave_debug_phase_times.argtypes = [vp, vp]
+        L.wave_debug_phase_times.restype = i32
         L.wave_grid_size.argtypes = [vp]
         L.wave_grid_size.restype = i32
         L.wave_barriers_per_step.argtypes = [vp]
@@ -143,6 +146,11 @@ class Wave:
         """Testing hook: later steps write their pre-quantisation K/V rows
         into dst ([L][2][S_max][H][D] fp32 on the device); None disables."""
         lib().wave_debug_dump_kv(self.h, _ptr(dst))
+
+    def debug_phase_times(self, dst) -> None:
+        """Profiling hook: later steps write globaltimer stamps (int64) at
+        entry, after every grid barrier and at exit into dst; None disables."""
+        lib().wave_debug_phase_times(self.h, _ptr(dst))
 
     @property
     def grid(self) -> int:

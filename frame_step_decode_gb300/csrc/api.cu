@@ -49,6 +49,7 @@ struct wave_ctx {
   long long timeout_ns = 2000000000LL;
   int skip_cta = -1, skip_bar = -1;
   float* kv_dump = nullptr;
+  long long* phase_ts = nullptr;
 };
 
 static EncodeTiledFn encode_fn() {
@@ -68,7 +69,7 @@ static bool shape_ok(const wave_config* c) {
   if (!c) return false;
   if (c->n_layers < 1 || c->n_layers > 1024) return false;
   if (c->head_dim != 64 && c->head_dim != 128) return false;
-  if (c->n_heads < 1 || c->d_model < 64 || c->d_model % 64) return false;
+  if (c->n_heads < 1 || c->d_model < 64 || c->d_model % 64 || c->d_model > 8192) return false;
   if ((c->n_heads * c->head_dim) % 64) return false;
   if (c->ffn < 8 || c->ffn % 8) return false;
   if (!(c->rms_eps >= 0.f) || !(c->rope_base > 0.f)) return false;
@@ -118,7 +119,7 @@ extern "C" const char* wave_strerror(int code) {
 // Stream-K split of tiles x kblocks over the grid: the most tiles one CTA touches.
 static int max_tiles_touched(long long tiles, long long kb, int grid) {
   const long long U = tiles * kb;
-  const int G = (int)(U < grid ? U : grid);
+  const int G = stream_k_ctas(grid, U, (int)tiles);
   int mt = 1;
   for (int c = 0; c < G; ++c) {
     const long long u0 = U * c / G, u1 = U * (c + 1) / G;
@@ -127,6 +128,19 @@ static int max_tiles_touched(long long tiles, long long kb, int grid) {
     if (n > mt) mt = n;
   }
   return mt;
+}
+
+// Most segments (CTAs) any one tile is split into.
+static int max_segments(long long tiles, long long kb, int grid) {
+  const long long U = tiles * kb;
+  const int G = stream_k_ctas(grid, U, (int)tiles);
+  int ms = 1;
+  for (long long t = 0; t < tiles; ++t) {
+    const long long a = t * kb, b = (t + 1) * kb - 1;
+    const int ca = (int)(((a + 1) * G + U - 1) / U - 1), cb = (int)(((b + 1) * G + U - 1) / U - 1);
+    if (cb - ca + 1 > ms) ms = cb - ca + 1;
+  }
+  return ms;
 }
 
 extern "C" int wave_create(const wave_config* cfg, int S_max, int T_max, wave_t** out) {
@@ -167,6 +181,10 @@ extern "C" int wave_create(const wave_config* cfg, int S_max, int T_max, wave_t*
     }
     int m = max_tiles_touched(h->tiles[k], h->kblocks[k], h->grid);
     if (m > mt) mt = m;
+    if (max_segments(h->tiles[k], h->kblocks[k], h->grid) > 64) {  // kMaxSeg
+      delete h;
+      return WAVE_EINVAL;
+    }
   }
   h->max_tiles_per_cta = mt;
 
@@ -317,7 +335,7 @@ extern "C" int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8,
   if (!h || !weights || !kv_fp8 || !kv_scales || !positions || !x || !y) return WAVE_EINVAL;
   if (S < 1 || S > h->S_max) return WAVE_EINVAL;
   if (((uintptr_t)weights & 15) || ((uintptr_t)kv_fp8 & 15) || ((uintptr_t)kv_scales & 15) ||
-      ((uintptr_t)positions & 3) || ((uintptr_t)x & 3) || ((uintptr_t)y & 3))
+      ((uintptr_t)positions & 3) || ((uintptr_t)x & 15) || ((uintptr_t)y & 15))
     return WAVE_EINVAL;
   cudaStream_t st = (cudaStream_t)stream;
   const int S_pad = (S + 15) / 16 * 16;
@@ -388,6 +406,7 @@ extern "C" int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8,
   p.skip_cta = h->skip_cta;
   p.skip_bar = h->skip_bar;
   p.kv_dump = h->kv_dump;
+  p.phase_ts = h->phase_ts;
   if (cudaMemsetAsync(h->bar, 0, 4, st) != cudaSuccess) return WAVE_ECUDA;
   cudaError_t e = launch_step(p, h->grid, st);
   h->last_stream = st;
@@ -423,6 +442,12 @@ extern "C" int wave_debug_skip_barrier(wave_t* h, int cta, int barrier) {
 extern "C" int wave_debug_dump_kv(wave_t* h, float* dst) {
   if (!h) return WAVE_EINVAL;
   h->kv_dump = dst;
+  return WAVE_OK;
+}
+
+extern "C" int wave_debug_phase_times(wave_t* h, long long* dst) {
+  if (!h) return WAVE_EINVAL;
+  h->phase_ts = dst;
   return WAVE_OK;
 }
 

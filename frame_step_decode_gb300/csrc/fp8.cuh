@@ -21,6 +21,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
+// Four codes in a 32-bit word -> two f16x2: lo = bytes 0,1, hi = bytes 2,3
+// (byte k of each pair in half k).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
 // Per-row quantiser of the K/V append (one warp, D = 32 * kPer values, lane
 // i holding elements [i*kPer, (i+1)*kPer)): scale = amax/448 (fp32, RN),
 // codes = E4M3(v / scale) with an IEEE fp32 division; a zero row gives

@@ -59,7 +59,16 @@ struct StepParams {
   long long timeout_ns;
   int skip_cta, skip_bar;
   float* kv_dump;        // testing hook: [L][2][S_max][H][D] pre-quantisation K/V, or null
+  long long* phase_ts;   // profiling hook: globaltimer at start, after each barrier, at end
 };
+
+// CTAs taking part in a stream-K GEMM phase of `tiles` tiles and U units.
+__host__ __device__ inline int stream_k_ctas(int grid, long long U, int tiles) {
+  long long g = grid;
+  if (U < g) g = U;
+  if (62LL * tiles < g) g = 62LL * tiles;
+  return (int)g;
+}
 
 // Host-side launch (step.cu).
 cudaError_t launch_step(const StepParams& p, int grid, cudaStream_t stream);

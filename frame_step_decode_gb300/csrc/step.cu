@@ -96,6 +96,7 @@ __device__ bool grid_sync(const StepParams& p, Ctx& c) {
     }
     __threadfence();
     *misc_word(c, 2) = ok;
+    if (p.phase_ts && blockIdx.x == 0) p.phase_ts[1 + c.bar_index] = globaltimer();
   }
   c.bar_index++;
   __syncthreads();
@@ -105,23 +106,40 @@ __device__ bool grid_sync(const StepParams& p, Ctx& c) {
 }
 
 // ------------------------------------------------------------------- norm
-// xn[s] = bf16(r * rstd * g), rstd = 1/sqrt(mean(r^2) + eps); rows strided
-// over CTAs.  At layer 0 the residual is first loaded from x (bf16).
+// xn[s] = bf16(r * rstd * g), rstd = 1/sqrt(mean(r^2) + eps); one row per CTA
+// (rows strided over CTAs), the row held in registers as float4s so that its
+// loads are all in flight at once.  At layer 0 the residual is first loaded
+// from x (bf16).
+constexpr int kNormVec = 11;  // float4s per thread: d <= 4 * kThreads * kNormVec
 __device__ void norm_phase(const StepParams& p, Ctx& c, const uint16_t* g, bool from_x) {
   float* red = (float*)(c.smem + c.lay.red_off);
-  const int d = p.d, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int d = p.d, d4 = d / 4, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int s = blockIdx.x; s < p.S; s += gridDim.x) {
-    float* r = p.resid + (size_t)s * d;
+    float4* r4 = (float4*)(p.resid + (size_t)s * d);
+    float4 rv[kNormVec];
     float ss = 0.f;
-    for (int i = tid; i < d; i += kThreads) {
-      float v;
-      if (from_x) {
-        v = bf16_to_f32(p.x[(size_t)s * d + i]);
-        r[i] = v;
-      } else {
-        v = __ldcg(r + i);
+#pragma unroll
+    for (int k = 0; k < kNormVec; ++k) {
+      const int i4 = tid + k * kThreads;
+      if (i4 < d4) {
+        if (from_x) {
+          const uint2 xb = *(const uint2*)(p.x + (size_t)s * d + 4 * i4);
+          rv[k] = make_float4(bf16_to_f32((uint16_t)(xb.x & 0xFFFF)), bf16_to_f32((uint16_t)(xb.x >> 16)),
+                              bf16_to_f32((uint16_t)(xb.y & 0xFFFF)), bf16_to_f32((uint16_t)(xb.y >> 16)));
+          r4[i4] = rv[k];
+        } else {
+          rv[k] = __ldcg(r4 + i4);
+        }
       }
-      ss = fmaf(v, v, ss);
+    }
+#pragma unroll
+    for (int k = 0; k < kNormVec; ++k) {
+      if (tid + k * kThreads < d4) {
+        ss = fmaf(rv[k].x, rv[k].x, ss);
+        ss = fmaf(rv[k].y, rv[k].y, ss);
+        ss = fmaf(rv[k].z, rv[k].z, ss);
+        ss = fmaf(rv[k].w, rv[k].w, ss);
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -131,9 +149,18 @@ __device__ void norm_phase(const StepParams& p, Ctx& c, const uint16_t* g, bool 
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) tot += red[w];
     const float rstd = 1.0f / sqrtf(tot / (float)d + p.eps);
-    for (int i = tid; i < d; i += kThreads) {
-      float v = from_x ? r[i] : __ldcg(r + i);
-      p.xn[(size_t)s * d + i] = f32_to_bf16((v * rstd) * bf16_to_f32(g[i]));
+#pragma unroll
+    for (int k = 0; k < kNormVec; ++k) {
+      const int i4 = tid + k * kThreads;
+      if (i4 < d4) {
+        const uint2 gb = *(const uint2*)(g + 4 * i4);
+        const float g0 = bf16_to_f32((uint16_t)(gb.x & 0xFFFF)), g1 = bf16_to_f32((uint16_t)(gb.x >> 16));
+        const float g2 = bf16_to_f32((uint16_t)(gb.y & 0xFFFF)), g3 = bf16_to_f32((uint16_t)(gb.y >> 16));
+        uint2 o;
+        o.x = (uint32_t)f32_to_bf16((rv[k].x * rstd) * g0) | ((uint32_t)f32_to_bf16((rv[k].y * rstd) * g1) << 16);
+        o.y = (uint32_t)f32_to_bf16((rv[k].z * rstd) * g2) | ((uint32_t)f32_to_bf16((rv[k].w * rstd) * g3) << 16);
+        *(uint2*)(p.xn + (size_t)s * d + 4 * i4) = o;
+      }
     }
     __syncthreads();
   }
@@ -141,6 +168,7 @@ __device__ void norm_phase(const StepParams& p, Ctx& c, const uint16_t* g, bool 
 
 // ------------------------------------------------------------ GEMM (tcgen05)
 struct Span { long long u0, u1; };
+constexpr int kMaxSeg = 64;  // segments of one tile (checked on the host)
 __device__ __forceinline__ Span cta_span(long long U, int G, int c) {
   return Span{U * c / G, U * (c + 1) / G};
 }
@@ -162,13 +190,17 @@ __device__ __forceinline__ void epilogue_apply(const StepParams& p, Ctx& c, int 
   } else if (kind == kO || kind == kDown) {
     const int d = p.d, n = t * kTileM + r;
     if (n < d) {
+      // all loads first, then all stores: keeps the 16 L2 round trips in flight
+      float old[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        old[i] = (col0 + i < S) ? __ldcg(p.resid + (size_t)(col0 + i) * d + n) : 0.f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int s = col0 + i;
         if (s < S) {
-          float* rp = p.resid + (size_t)s * d + n;
-          float nr = __ldcg(rp) + v[i];
-          *rp = nr;
+          const float nr = old[i] + v[i];
+          p.resid[(size_t)s * d + n] = nr;
           if (last_layer) p.y[(size_t)s * d + n] = f32_to_bf16(nr);
         }
       }
@@ -202,9 +234,10 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KB = p.kblocks[kind];
   const long long U = (long long)p.tiles[kind] * KB;
-  // Split over min(grid, units) CTAs so that every participating span is
-  // non-empty and the owners of a tile's units are consecutive CTAs.
-  const int G = (int)min((long long)gridDim.x, U), cta = blockIdx.x;
+  // Split over min(grid, units, 62 * tiles) CTAs: every participating span is
+  // non-empty, the owners of a tile's units are consecutive CTAs, and a tile
+  // has at most kMaxSeg segments.
+  const int G = stream_k_ctas(gridDim.x, U, p.tiles[kind]), cta = blockIdx.x;
   const Span sp = (cta < G) ? cta_span(U, G, cta) : Span{0, 0};
   const int S_pad = p.S_pad, nst = p.nstage;
   const uint32_t b_bytes = (uint32_t)S_pad * 128u;
@@ -327,17 +360,34 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
         named_bar(1, 128);
         if (*misc_word(c, 3)) {
           __threadfence();
+          // offsets of the tile's partial slots, in segment order (shared scratch)
+          long long* seg = (long long*)(c.smem + c.lay.red_off);
+          for (int j = threadIdx.x - 64; j < nseg; j += 128) {
+            const int cj = c_first + j;
+            const int ftj = (int)(cta_span(U, G, cj).u0 / KB);
+            seg[j] = ((long long)cj * MT + (t - ftj)) * (long long)S_pad * kTileM;
+          }
+          named_bar(1, 128);
           for (int col = 0; col < S_pad; col += 16) {
             float v[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = 0.f;
-            for (int j = 0; j < nseg; ++j) {
-              const int cj = c_first + j;
-              const int ftj = (int)(cta_span(U, G, cj).u0 / KB);
-              const float* sj =
-                  p.gemm_part + ((size_t)cj * MT + (t - ftj)) * (size_t)S_pad * kTileM;
+            for (int j0 = 0; j0 < nseg; j0 += 4) {
+              // up to 4 segments x 16 columns of loads in flight, summed in order
+              float tmp[4][16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] += __ldcg(sj + (size_t)(col + i) * kTileM + r);
+              for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  tmp[jj][i] = (j0 + jj < nseg)
+                                   ? __ldcg(p.gemm_part + seg[j0 + jj] + (size_t)(col + i) * kTileM + r)
+                                   : 0.f;
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj)
+                if (j0 + jj < nseg) {
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) v[i] += tmp[jj][i];
+                }
             }
             epilogue_apply(p, c, kind, t, r, col, v, last_layer);
           }
@@ -529,29 +579,42 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
         __syncwarp();
       }
 
-      // ---- scores S[token] = K . q: 4 m-tiles of 16 tokens; A = codes of
-      // tokens g and g+8 (lane's KQB bytes each), B = q (column 0).
+      // ---- scores S[token] = K . q: 4 m-tiles of 16 tokens, interleaved so
+      // that 8 accumulators (m-tile x {q_hi, q_lo}) form independent chains;
+      // A = codes of tokens g and g+8 (the lane's KQB bytes), B = q (column 0).
+      float cac[4][2][4];
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int hl = 0; hl < 2; ++hl) cac[mt][hl][0] = cac[mt][hl][1] = cac[mt][hl][2] = cac[mt][hl][3] = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < KQB / 16; ++ch) {
+        uint32_t ka[4][4], kb[4][4];
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          const uint4 a = *(const uint4*)(kt + swz<D>((uint32_t)((mt * 16 + g) * D + t4 * KQB + ch * 16)));
+          const uint4 b = *(const uint4*)(kt + swz<D>((uint32_t)((mt * 16 + g + 8) * D + t4 * KQB + ch * 16)));
+          ka[mt][0] = a.x; ka[mt][1] = a.y; ka[mt][2] = a.z; ka[mt][3] = a.w;
+          kb[mt][0] = b.x; kb[mt][1] = b.y; kb[mt][2] = b.z; kb[mt][3] = b.w;
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = ch * 4 + jj;
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            e4m3x4_to_f16x2x2(ka[mt][jj], a0, a2);
+            e4m3x4_to_f16x2x2(kb[mt][jj], a1, a3);
+            mma_f16_16816(cac[mt][0], a0, a1, a2, a3, qh0[j], qh1[j]);
+            mma_f16_16816(cac[mt][1], a0, a1, a2, a3, ql0[j], ql1[j]);
+          }
+        }
+      }
       float sc[4][2];  // [m-tile][token g, token g+8], real where t4 == 0
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
-        float cacc[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t k0[KQB / 4], k1[KQB / 4];
-#pragma unroll
-        for (int ch = 0; ch < KQB / 16; ++ch) {
-          const uint4 a = *(const uint4*)(kt + swz<D>((uint32_t)((mt * 16 + g) * D + t4 * KQB + ch * 16)));
-          const uint4 b = *(const uint4*)(kt + swz<D>((uint32_t)((mt * 16 + g + 8) * D + t4 * KQB + ch * 16)));
-          k0[4 * ch + 0] = a.x; k0[4 * ch + 1] = a.y; k0[4 * ch + 2] = a.z; k0[4 * ch + 3] = a.w;
-          k1[4 * ch + 0] = b.x; k1[4 * ch + 1] = b.y; k1[4 * ch + 2] = b.z; k1[4 * ch + 3] = b.w;
-        }
-#pragma unroll
-        for (int j = 0; j < KST; ++j) {
-          const uint32_t a0 = e4m3x2_to_f16x2(k0[j] & 0xFFFFu), a1 = e4m3x2_to_f16x2(k1[j] & 0xFFFFu);
-          const uint32_t a2 = e4m3x2_to_f16x2(k0[j] >> 16), a3 = e4m3x2_to_f16x2(k1[j] >> 16);
-          mma_f16_16816(cacc, a0, a1, a2, a3, qh0[j], qh1[j]);
-          mma_f16_16816(cacc, a0, a1, a2, a3, ql0[j], ql1[j]);
-        }
-        sc[mt][0] = cacc[0];
-        sc[mt][1] = cacc[2];
+        sc[mt][0] = cac[mt][0][0] + cac[mt][1][0];
+        sc[mt][1] = cac[mt][0][2] + cac[mt][1][2];
       }
       // ---- online softmax (base 2) over the lanes with t4 == 0
       float mx = -INFINITY, vmax = 0.f;
@@ -641,24 +704,19 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
             for (int w = 0; w < VB / 4; ++w) vw[a][w] = 0u;
           }
         }
-        // byte-pair tables: p01[b] = {tok r0 byte b, tok r0+1 byte b}, p23 likewise
-        uint32_t p01[VB / 2], p23[VB / 2];
+        // f01[b] = f16 pair {tok r0 byte b, tok r0+1 byte b}; f23 likewise
+        uint32_t f01[VB], f23[VB];
 #pragma unroll
         for (int w = 0; w < VB / 4; ++w) {
-          p01[2 * w] = prmt(vw[0][w], vw[1][w], 0x5140u);
-          p01[2 * w + 1] = prmt(vw[0][w], vw[1][w], 0x7362u);
-          p23[2 * w] = prmt(vw[2][w], vw[3][w], 0x5140u);
-          p23[2 * w + 1] = prmt(vw[2][w], vw[3][w], 0x7362u);
+          e4m3x4_to_f16x2x2(prmt(vw[0][w], vw[1][w], 0x5140u), f01[4 * w + 0], f01[4 * w + 1]);
+          e4m3x4_to_f16x2x2(prmt(vw[0][w], vw[1][w], 0x7362u), f01[4 * w + 2], f01[4 * w + 3]);
+          e4m3x4_to_f16x2x2(prmt(vw[2][w], vw[3][w], 0x5140u), f23[4 * w + 0], f23[4 * w + 1]);
+          e4m3x4_to_f16x2x2(prmt(vw[2][w], vw[3][w], 0x7362u), f23[4 * w + 2], f23[4 * w + 3]);
         }
-        // byte b of a token vector sits in half (b & 1) of p..[b >> 1]
         // m-tile j: row g <-> byte j, row g+8 <-> byte j + VB/2
 #pragma unroll
         for (int j = 0; j < MTV; ++j) {
-          const int b0 = j, b1 = j + VB / 2;
-          const uint32_t a0 = e4m3x2_to_f16x2((p01[b0 >> 1] >> (16 * (b0 & 1))) & 0xFFFFu);
-          const uint32_t a1 = e4m3x2_to_f16x2((p01[b1 >> 1] >> (16 * (b1 & 1))) & 0xFFFFu);
-          const uint32_t a2 = e4m3x2_to_f16x2((p23[b0 >> 1] >> (16 * (b0 & 1))) & 0xFFFFu);
-          const uint32_t a3 = e4m3x2_to_f16x2((p23[b1 >> 1] >> (16 * (b1 & 1))) & 0xFFFFu);
+          const uint32_t a0 = f01[j], a1 = f01[j + VB / 2], a2 = f23[j], a3 = f23[j + VB / 2];
           mma_f16_16816(acc[j], a0, a1, a2, a3, bh0, bh1);
           mma_f16_16816(acc[j], a0, a1, a2, a3, bl0, bl1);
         }
@@ -740,11 +798,19 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
 static_assert(kThreads <= 256, "the reduction scratch holds one word per thread");
 __device__ void build_pieces(const StepParams& p, Ctx& c) {
   int* red = (int*)(c.smem + c.lay.red_off);
+  int* spos = (int*)(c.smem + c.lay.xbuf_off);  // positions, -1 where invalid
   const int N = p.S * p.H, tid = threadIdx.x;
+  for (int s = tid; s < p.S; s += kThreads) {
+    const int P = p.pos[s];
+    const bool ok = (P >= 0 && P < p.T_max);
+    spos[s] = ok ? P : -1;
+    if (!ok) set_err(p, kErrPos);
+  }
+  __syncthreads();
   const int b0 = (int)((long long)N * tid / kThreads), b1 = (int)((long long)N * (tid + 1) / kThreads);
   auto count = [&](int sh) {
-    const int P = p.pos[sh / p.H];
-    if (P < 0 || P >= p.T_max) return 0;
+    const int P = spos[sh / p.H];
+    if (P < 0) return 0;
     const int nch = P / kChunk + 1;
     return (nch + kPieceChunks - 1) / kPieceChunks;
   };
@@ -765,23 +831,18 @@ __device__ void build_pieces(const StepParams& p, Ctx& c) {
   int base = red[tid];
   for (int sh = b0; sh < b1; ++sh) {
     const int np = count(sh);
-    const int P = p.pos[sh / p.H];
-    const int nch = P / kChunk + 1;
+    if (np == 0) continue;
+    const int nch = spos[sh / p.H] / kChunk + 1;
     for (int q = 0; q < np; ++q) {
       const int lo = q * kPieceChunks, hi = min(nch, lo + kPieceChunks);
       p.pieces[base + q] = make_int4(sh, lo | (hi << 16), np, base);
     }
     base += np;
   }
-  // sessions with an invalid position: flag, and zero their attention rows
-  for (int s = tid; s < p.S; s += kThreads) {
-    const int P = p.pos[s];
-    if (P < 0 || P >= p.T_max) set_err(p, kErrPos);
-  }
-  for (int i = tid; i < p.S * p.HD; i += kThreads) {
-    const int P = p.pos[i / p.HD];
-    if (P < 0 || P >= p.T_max) p.attn[i] = 0;
-  }
+  // sessions with an invalid position get a zero attention output
+  for (int s = 0; s < p.S; ++s)
+    if (spos[s] < 0)
+      for (int i = tid; i < p.HD; i += kThreads) p.attn[(size_t)s * p.HD + i] = 0;
   __syncthreads();
 }
 
@@ -829,6 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   tc_fence_after();
   c.tmem = *(volatile uint32_t*)(c.smem + c.lay.misc_off);
 
+  if (p.phase_ts && blockIdx.x == 0 && threadIdx.x == 0) p.phase_ts[0] = globaltimer();
   // phase 0: work list, counter reset, residual and first norm
   for (int i = blockIdx.x * kThreads + threadIdx.x; i < p.S_max * p.H; i += gridDim.x * kThreads)
     p.sh_cnt[i] = 0;
@@ -877,6 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   }
   tc_fence_before();
   __syncthreads();
+  if (p.phase_ts && blockIdx.x == 0 && threadIdx.x == 0) p.phase_ts[1 + c.bar_index] = globaltimer();
   if (warp == 1) tmem_dealloc(c.tmem, kTmemCols);
 }
 

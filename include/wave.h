@@ -46,7 +46,8 @@ extern "C" {
 #define WAVE_ENOMEM (-7)   /* device allocation failed */
 
 /* Decoder shape.  Constraints checked by wave_create: head_dim is 64 or 128;
- * d_model, n_heads*head_dim and ffn are multiples of 64, 64 and 8. */
+ * d_model (at most 8192), n_heads*head_dim and ffn are multiples of 64, 64
+ * and 8. */
 typedef struct {
   int n_layers, d_model, n_heads, head_dim, ffn;
   float rms_eps, rope_base;
@@ -99,7 +100,8 @@ size_t wave_weight_offset(const wave_config* cfg, int layer, int which);
  *   positions  int32 [S]: pos[s] is the RoPE position of this frame and the
  *              cache slot it writes; attention spans slots 0..pos[s] inclusive.
  *              Input only: the caller advances positions between frames.
- *   x          bf16 [S][d] input activations; y bf16 [S][d] output (may alias x).
+ *   x          bf16 [S][d] input activations; y bf16 [S][d] output (may alias x);
+ *              both 16-byte aligned.
  *
  * Readings of what the pages leave open: bf16 rounding only at the projection
  * inputs (normed x, attention output, SwiGLU output) and at y, fp32 elsewhere;
@@ -154,6 +156,11 @@ int wave_debug_skip_barrier(wave_t* h, int cta, int barrier);
  * [L][2][S_max][H][D] floats, so that tests can check the append bit for bit
  * against a reference quantiser.  dst = NULL disables. */
 int wave_debug_dump_kv(wave_t* h, float* dst);
+/* Profiling hook: make later steps record %globaltimer (ns) into dst, a device
+ * buffer of wave_barriers_per_step(h) + 2 int64: [0] at kernel entry, [1+b]
+ * when grid barrier b released CTA 0, and the last entry at kernel exit.
+ * dst = NULL disables. */
+int wave_debug_phase_times(wave_t* h, long long* dst);
 /* Grid size (CTAs, one per SM) and barriers per step, for tests and tools. */
 int wave_grid_size(wave_t* h);
 int wave_barriers_per_step(wave_t* h);
