@@ -6,16 +6,16 @@
 
 namespace wave {
 
-constexpr int kThreads = 192;     // 6 warps: TMA producer, MMA issuer, 4 epilogue warps
+constexpr int kThreads = 256;     // 8 warps: TMA producer, MMA issuer, 4 epilogue warps, 2 more
+                                  // (all 8 run attention and the norms)
 constexpr int kWarps = kThreads / 32;
 constexpr int kTileM = 128;       // weight rows per GEMM tile = tcgen05 M
 constexpr int kKBlk = 64;         // K elements per pipeline stage (128 B of bf16)
-constexpr int kChunk = 64;        // attention tokens per async-copy chunk
+constexpr int kChunk = 48;        // attention tokens per async-copy chunk (3 x 16)
 constexpr int kAttStages = 2;     // chunks in flight per attention warp
-constexpr int kPieceChunks = 4;   // chunks per attention work piece (256 tokens)
+constexpr int kPieceChunks = 5;   // chunks per attention work piece (240 tokens)
 constexpr int kMaxStages = 8;     // GEMM ring depth cap
 constexpr int kTmemCols = 256;    // two fp32 accumulators of up to 128 columns
-constexpr int kSmemBytes = 212 * 1024;
 
 enum ErrBits : int { kErrTimeout = 1, kErrPos = 2 };
 
@@ -88,7 +88,7 @@ struct SmemLayout {
 __host__ __device__ inline SmemLayout smem_layout() {
   SmemLayout s;
   s.ring_off = 0;
-  s.ring_bytes = 204 * 1024;
+  s.ring_bytes = 208 * 1024;
   s.xbuf_off = s.ring_off + s.ring_bytes;            // 64 x 17 fp32
   s.qscr_off = s.xbuf_off + 64 * 17 * 4;             // 3 KB: q as f16 hi + lo per warp
   s.red_off = s.qscr_off + kWarps * 512;             // 1 KB: one int per thread
@@ -98,7 +98,7 @@ __host__ __device__ inline SmemLayout smem_layout() {
   return s;
 }
 __host__ __device__ inline int attn_stage_bytes(int D) {  // K tile, V tile, K scales, V scales; 1 KB aligned
-  int b = 2 * kChunk * D + 2 * kChunk * 4;
+  int b = 2 * kChunk * D + 2 * 256;  // scales in 256-byte slots
   return (b + 1023) & ~1023;
 }
 

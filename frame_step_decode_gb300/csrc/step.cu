@@ -309,7 +309,7 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     const int q = warp & 3, r = q * 32 + lane;
     const int MT = p.max_tiles_per_cta;
     const int first_tile = (int)(sp.u0 / KB);
@@ -418,6 +418,7 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
   constexpr int KST = D / 16;    // k-steps of the score mma over the head dim
   constexpr int VB = D / 8;      // V bytes per lane per token (P.V mma)
   constexpr int MTV = D / 16;    // m-tiles of the P.V mma (16 head dims each)
+  constexpr int kMT = kChunk / 16;  // 16-token tiles per chunk
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t4 = lane & 3;       // thread-in-group of the mma fragments
   const int g = lane >> 2;       // group of the mma fragments
@@ -582,16 +583,16 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
       // ---- scores S[token] = K . q: 4 m-tiles of 16 tokens, interleaved so
       // that 8 accumulators (m-tile x {q_hi, q_lo}) form independent chains;
       // A = codes of tokens g and g+8 (the lane's KQB bytes), B = q (column 0).
-      float cac[4][2][4];
+      float cac[kMT][2][4];
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt)
+      for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
         for (int hl = 0; hl < 2; ++hl) cac[mt][hl][0] = cac[mt][hl][1] = cac[mt][hl][2] = cac[mt][hl][3] = 0.f;
 #pragma unroll
       for (int ch = 0; ch < KQB / 16; ++ch) {
-        uint32_t ka[4][4], kb[4][4];
+        uint32_t ka[kMT][4], kb[kMT][4];
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
+        for (int mt = 0; mt < kMT; ++mt) {
           const uint4 a = *(const uint4*)(kt + swz<D>((uint32_t)((mt * 16 + g) * D + t4 * KQB + ch * 16)));
           const uint4 b = *(const uint4*)(kt + swz<D>((uint32_t)((mt * 16 + g + 8) * D + t4 * KQB + ch * 16)));
           ka[mt][0] = a.x; ka[mt][1] = a.y; ka[mt][2] = a.z; ka[mt][3] = a.w;
@@ -601,7 +602,7 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
         for (int jj = 0; jj < 4; ++jj) {
           const int j = ch * 4 + jj;
 #pragma unroll
-          for (int mt = 0; mt < 4; ++mt) {
+          for (int mt = 0; mt < kMT; ++mt) {
             uint32_t a0, a1, a2, a3;
             e4m3x4_to_f16x2x2(ka[mt][jj], a0, a2);
             e4m3x4_to_f16x2x2(kb[mt][jj], a1, a3);
@@ -610,16 +611,16 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
           }
         }
       }
-      float sc[4][2];  // [m-tile][token g, token g+8], real where t4 == 0
+      float sc[kMT][2];  // [m-tile][token g, token g+8], real where t4 == 0
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
+      for (int mt = 0; mt < kMT; ++mt) {
         sc[mt][0] = cac[mt][0][0] + cac[mt][1][0];
         sc[mt][1] = cac[mt][0][2] + cac[mt][1][2];
       }
       // ---- online softmax (base 2) over the lanes with t4 == 0
       float mx = -INFINITY, vmax = 0.f;
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
+      for (int mt = 0; mt < kMT; ++mt) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int tok = mt * 16 + g + 8 * e;
@@ -651,9 +652,9 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
       m_run = m_new;
       const float inv_R = 1.0f / R_new;
       // weights w = p * vs / R as f16 hi + lo, packed {token g, token g+8}
-      uint32_t whi[4], wlo[4];
+      uint32_t whi[kMT], wlo[kMT];
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
+      for (int mt = 0; mt < kMT; ++mt) {
         float w2[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -673,7 +674,7 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
       // of tokens 2t4, 2t4+1, 2t4+8, 2t4+9 from lanes 8*t4 and 8*t4+4.
       const int srcA = 8 * t4, srcB = 8 * t4 + 4;
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
+      for (int mt = 0; mt < kMT; ++mt) {
         const uint32_t hA = __shfl_sync(0xffffffffu, whi[mt], srcA);
         const uint32_t hB = __shfl_sync(0xffffffffu, whi[mt], srcB);
         const uint32_t lA = __shfl_sync(0xffffffffu, wlo[mt], srcA);
