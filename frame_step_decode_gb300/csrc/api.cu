@@ -200,7 +200,7 @@ extern "C" int wave_create(const wave_config* cfg, int S_max, int T_max, wave_t*
       {(void**)&h->attn, (size_t)(SP * HD * 2)},
       {(void**)&h->u, (size_t)(SP * F * 2)},
       {(void**)&h->gemm_part, (size_t)h->grid * mt * SP * kTileM * 4},
-      {(void**)&h->tile_cnt, 1024 * 4},
+      {(void**)&h->tile_cnt, 2048 * 4},
       {(void**)&h->att_part, (size_t)(max_pieces * (D + 4) * 4)},
       {(void**)&h->sh_cnt, (size_t)(S_max * H * 4)},
       {(void**)&h->pieces, (size_t)(max_pieces * 16)},
@@ -382,6 +382,8 @@ extern "C" int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8,
   p.layer_elems = h->layer_elems;
   p.off_g_attn = h->off[0];
   p.off_g_mlp = h->off[3];
+  p.off_wo = h->off[2];
+  p.off_wdown = h->off[5];
   p.weights = (const uint16_t*)weights;
   p.kv = kv_fp8;
   p.kv_scales = kv_scales;

@@ -33,7 +33,7 @@ struct StepParams {
   int nstage;            // GEMM ring depth for this S
   int tiles[4], kblocks[4];
   int max_tiles_per_cta; // partial-sum slots per CTA
-  long long layer_elems, off_g_attn, off_g_mlp;
+  long long layer_elems, off_g_attn, off_g_mlp, off_wo, off_wdown;
   // caller buffers
   const uint16_t* weights;
   uint8_t* kv;
@@ -48,7 +48,7 @@ struct StepParams {
   uint16_t* attn;        // [S_pad_max][H*D] bf16 attention output
   uint16_t* u;           // [S_pad_max][F] bf16 SwiGLU output
   float* gemm_part;      // [G][max_tiles_per_cta][S_pad][128] split-K partials
-  int* tile_cnt;         // [max tiles] arrivals per tile (reset by the last arriver)
+  int* tile_cnt;         // [2][1024] per tile: segments arrived, final reducers done
   float* att_part;       // [max pieces][D + 4] (acc, m, l) per attention piece
   int* sh_cnt;           // [S_max*H] arrivals per (session, head)
   int4* pieces;          // [max pieces] (sh, c_lo | c_hi << 16, n_pieces_of_sh, first_piece)
@@ -63,7 +63,10 @@ struct StepParams {
 };
 
 // CTAs taking part in a stream-K GEMM phase of `tiles` tiles and U units.
+// With at least half a grid of tiles (and no more than a grid), one whole
+// tile per CTA: no split-K partial sums at all.
 __host__ __device__ inline int stream_k_ctas(int grid, long long U, int tiles) {
+  if (2 * tiles >= grid && tiles <= grid) return tiles;
   long long g = grid;
   if (U < g) g = U;
   if (62LL * tiles < g) g = 62LL * tiles;

@@ -177,6 +177,30 @@ __device__ __forceinline__ int owner_of(long long U, int G, long long u) {
   return (int)(((u + 1) * G + U - 1) / U - 1);
 }
 
+
+// Prefetch into L2 the weight rows this CTA will stream in GEMM `kind` of
+// `layer` (its stream-K span), so that the phase reads them from L2.  Issued
+// by one thread while an earlier phase streams other data from HBM.
+__device__ void prefetch_gemm_weights(const StepParams& p, int kind, int layer) {
+  const int KB = p.kblocks[kind], T = p.tiles[kind];
+  const long long U = (long long)T * KB;
+  const int G = stream_k_ctas(gridDim.x, U, T), cta = blockIdx.x;
+  if (cta >= G) return;
+  const Span sp = cta_span(U, G, cta);
+  const int K = (kind == kO) ? p.HD : p.F;   // O and down only
+  const int N = p.d;
+  const uint16_t* W = p.weights + (size_t)layer * p.layer_elems +
+                      (kind == kO ? p.off_wo : p.off_wdown);
+  for (long long u = sp.u0; u < sp.u1;) {
+    const int t = (int)(u / KB);
+    const long long e = min(sp.u1, (long long)(t + 1) * KB);
+    const int k0 = (int)(u - (long long)t * KB) * kKBlk, k1 = min(K, (int)(e - (long long)t * KB) * kKBlk);
+    for (int r = t * kTileM; r < min(N, (t + 1) * kTileM); ++r)
+      bulk_prefetch_l2(W + (size_t)r * K + k0, (uint32_t)(k1 - k0) * 2u);
+    u = e;
+  }
+}
+
 __device__ __forceinline__ void epilogue_apply(const StepParams& p, Ctx& c, int kind, int t, int r,
                                                int col0, const float* v, bool last_layer) {
   const int S = p.S;
@@ -309,7 +333,9 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
       }
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp >= 6) {
+    // idle during GEMMs
+  } else {
     const int q = warp & 3, r = q * 32 + lane;
     const int MT = p.max_tiles_per_cta;
     const int first_tile = (int)(sp.u0 / KB);
@@ -341,6 +367,10 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_acce(c, b));
       } else {
+        // Split tile: store this segment's partial.  The CTAs whose spans end
+        // inside the tile then wait (bounded) until every segment has arrived
+        // and each sums, in segment order, its share of the tile's 16-column
+        // chunks; the other contributors move on.
         float* slot = p.gemm_part + ((size_t)cta * MT + (t - first_tile)) * (size_t)S_pad * kTileM;
         for (int col = 0; col < S_pad; col += 16) {
           float v[16];
@@ -353,13 +383,31 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
         if (lane == 0) mbar_arrive(bar_acce(c, b));
         __threadfence();
         named_bar(1, 128);
+        const bool final_seg = (sp.u1 <= te);
         if (threadIdx.x == 64) {
-          int old = atomicAdd(p.tile_cnt + t, 1);
-          *misc_word(c, 3) = (old == nseg - 1) ? 1 : 0;
+          atomicAdd(p.tile_cnt + t, 1);
+          int ok = 1;
+          if (final_seg) {
+            long long t0 = globaltimer();
+            for (uint32_t it = 0;; ++it) {
+              if ((int)ld_acquire((const unsigned*)(p.tile_cnt + t)) >= nseg) break;
+              if ((it & 15) == 15) {
+                if (*(volatile int*)p.err & kErrTimeout) { ok = 0; break; }
+                if (globaltimer() - t0 > p.timeout_ns) {
+                  set_err(p, kErrTimeout);
+                  ok = 0;
+                  break;
+                }
+              }
+            }
+          }
+          *misc_word(c, 3) = ok;
         }
         named_bar(1, 128);
-        if (*misc_word(c, 3)) {
-          __threadfence();
+        if (!*misc_word(c, 3)) return;
+        if (final_seg) {
+          const int m = (c_last - c_first) + (cta_span(U, G, c_last).u1 == te ? 1 : 0);
+          const int idx = cta - c_first;
           // offsets of the tile's partial slots, in segment order (shared scratch)
           long long* seg = (long long*)(c.smem + c.lay.red_off);
           for (int j = threadIdx.x - 64; j < nseg; j += 128) {
@@ -368,7 +416,8 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
             seg[j] = ((long long)cj * MT + (t - ftj)) * (long long)S_pad * kTileM;
           }
           named_bar(1, 128);
-          for (int col = 0; col < S_pad; col += 16) {
+          for (int cc = idx; cc < S_pad / 16; cc += m) {
+            const int col = cc * 16;
             float v[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = 0.f;
@@ -391,9 +440,13 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
             }
             epilogue_apply(p, c, kind, t, r, col, v, last_layer);
           }
-          if (threadIdx.x == 64) p.tile_cnt[t] = 0;
+          named_bar(1, 128);
+          // the last final contributor to finish re-arms the tile's counters
+          if (threadIdx.x == 64 && atomicAdd(p.tile_cnt + 1024 + t, 1) == m - 1) {
+            p.tile_cnt[t] = 0;
+            p.tile_cnt[1024 + t] = 0;
+          }
         }
-        named_bar(1, 128);
       }
       c.acc_it++;
       u = e;
@@ -432,6 +485,10 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
   __half* qs_hi = (__half*)(c.smem + c.lay.qscr_off + warp * 512);
   __half* qs_lo = qs_hi + 128;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
+  const uint64_t kv_policy = policy_evict_first();
+  // the output projection's weights are read next: bring them into L2 now
+  if (warp == kWarps - 1 && lane == 0) prefetch_gemm_weights(p, kO, layer);
+  __syncwarp();
 
   for (int pi = gw; pi < n_pieces; pi += NW) {
     const int4 pc = __ldcg(p.pieces + pi);
@@ -530,8 +587,8 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
       const int t0 = ci * kChunk;
       const uint32_t sbytes = 4u * (uint32_t)min(kChunk, p.T_max - t0);
       mbar_arrive_expect_tx(fb, 2u * kChunk * D + 2u * sbytes);
-      tma_load_2d(base, &p.tm_kv, 0, (int)(rowK + t0), fb);
-      tma_load_2d(base + kChunk * D, &p.tm_kv, 0, (int)(rowV + t0), fb);
+      tma_load_2d_hint(base, &p.tm_kv, 0, (int)(rowK + t0), fb, kv_policy);
+      tma_load_2d_hint(base + kChunk * D, &p.tm_kv, 0, (int)(rowV + t0), fb, kv_policy);
       bulk_load(base + 2 * kChunk * D, p.kv_scales + rowK + t0, sbytes, fb);
       bulk_load(base + 2 * kChunk * D + 256, p.kv_scales + rowV + t0, sbytes, fb);
     };
@@ -895,7 +952,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   // phase 0: work list, counter reset, residual and first norm
   for (int i = blockIdx.x * kThreads + threadIdx.x; i < p.S_max * p.H; i += gridDim.x * kThreads)
     p.sh_cnt[i] = 0;
-  for (int i = blockIdx.x * kThreads + threadIdx.x; i < 1024; i += gridDim.x * kThreads)
+  for (int i = blockIdx.x * kThreads + threadIdx.x; i < 2048; i += gridDim.x * kThreads)
     p.tile_cnt[i] = 0;
   if (blockIdx.x == gridDim.x - 1) build_pieces(p, c);
   norm_phase(p, c, p.weights + p.off_g_attn, true);
