@@ -351,6 +351,51 @@ def run_gpu(args, w):
         dist.destroy_process_group()
 
 
+def run_phases(args, w):
+    """Per-phase time of one step from the kernel's phase timestamps
+    (profiling hook): mean per layer of each phase, barrier included."""
+    import torch
+    import frame_step_decode_gb300 as fsd
+    device = torch.device("cuda", 0)
+    S = args.S
+    weights, kv, sc, pos, pos_h, x, y = build_inputs(w, S, device)
+    wave = fsd.Wave(fsd.WaveConfig.of(w), S, w.T_max)
+    for _ in range(max(3, args.warmup)):
+        wave.step(S, weights, kv, sc, pos, x, y)
+    ts = torch.zeros(wave.barriers_per_step + 2, dtype=torch.int64, device=device)
+    wave.debug_phase_times(ts)
+    runs = []
+    for _ in range(3):
+        wave.step(S, weights, kv, sc, pos, x, y)
+        if wave.status() != fsd.WAVE_OK:
+            raise RuntimeError("step failed")
+        runs.append(np.diff(ts.cpu().numpy().astype(np.float64)) / 1000.0)
+    wave.debug_phase_times(None)
+    t = np.mean(runs, axis=0)
+    names = ["prologue"]
+    for l in range(w.n_layers):
+        if l > 0:
+            names.append("norm1")
+        names += ["qkv", "attn", "o", "norm2", "gu", "down"]
+    d, HD, F = w.d_model, w.HD, w.ffn
+    wbytes = {"qkv": 3 * HD * d * 2, "o": d * HD * 2, "gu": 2 * F * d * 2, "down": d * F * 2}
+    kvb = sum(2 * w.n_heads * (int(q) + 1) * (w.head_dim + 4) for q in pos_h)
+    print(f"{w.name} S={S}: step {t.sum():.1f} us (phase = work + the grid barrier after it)")
+    agg = {}
+    for n, v in zip(names, t):
+        agg.setdefault(n, []).append(v)
+    for n, v in agg.items():
+        m = float(np.mean(v))
+        extra = ""
+        if n in wbytes:
+            extra = f"  {wbytes[n] / m / 1e3:6.0f} GB/s of weights"
+        if n == "attn":
+            extra = f"  {kvb / m / 1e3:6.0f} GB/s of FP8 K/V"
+        print(f"  {n:8s} x{len(v):3d}  mean {m:8.1f} us  total {np.sum(v):9.1f} us "
+              f"({100 * np.sum(v) / t.sum():5.1f}%){extra}")
+    wave.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -361,6 +406,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (profiling a small case)")
     ap.add_argument("--tmax", type=int, default=None, help="shorter history (profiling a small case)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--phases", action="store_true",
+                    help="print the per-phase time table of one step instead of the JSON line")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
@@ -370,7 +417,9 @@ def main():
         T = args.tmax or w.T_max
         w = replace(w, n_layers=args.layers or w.n_layers, T_max=T, pos_hi=min(w.pos_hi, T),
                     name=f"{w.name}-L{args.layers or w.n_layers}-T{T}")
-    if args.impl == "reference":
+    if args.phases:
+        run_phases(args, w)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_gpu(args, w)

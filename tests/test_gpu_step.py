@@ -104,7 +104,9 @@ def test_ragged_batch_sizes(S):
 
 def test_edge_positions():
     w = synth.MID
-    pos = np.array([0, 1, 63, 64, 65, 255, 256, 257, w.T_max - 1, 127, 128, 129], dtype=np.int32)
+    # chunk (48 tokens) and piece (240 tokens) boundaries, and the extremes
+    pos = np.array([0, 1, 47, 48, 49, 95, 96, 239, 240, 241, 255, 256, w.T_max - 1, 63, 64, 287, 288],
+                   dtype=np.int32)
     case = DeviceCase(w, S=pos.size, pos=pos)
     wave = fsd.Wave(case.cfg, case.S_max, w.T_max)
     try:
