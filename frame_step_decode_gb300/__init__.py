@@ -35,7 +35,7 @@ class WaveError(RuntimeError):
 
 _lib = None
 EXPORTS = ("wave_create", "wave_destroy", "wave_weights_bytes", "wave_weight_offset", "wave_step",
-           "wave_status", "wave_strerror", "wave_kv_quantize", "wave_fp8_encode",
+           "wave_status", "wave_strerror", "wave_kv_quantize", "wave_fp8_encode", "wave_step_static",
            "wave_set_timeout_ns", "wave_debug_skip_barrier", "wave_debug_dump_kv", "wave_debug_phase_times",
            "wave_grid_size",
            "wave_barriers_per_step")
@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.wave_kv_quantize.restype = i32
         L.wave_fp8_encode.argtypes = [vp, i64, vp, vp]
         L.wave_fp8_encode.restype = i32
+        L.wave_step_static.argtypes = [cfgp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+        L.wave_step_static.restype = i32
         L.wave_set_timeout_ns.argtypes = [vp, ctypes.c_longlong]
         L.wave_set_timeout_ns.restype = i32
         L.wave_debug_skip_barrier.argtypes = [vp, i32, i32]
@@ -170,6 +172,16 @@ class Wave:
             self.close()
         except Exception:
             pass
+
+
+def step_static(cfg: WaveConfig, S_max: int, T_max: int, S: int, weights, kv, kv_scales, positions,
+                x, y, stream=None) -> int:
+    """wave_step_static: one frame with the library's fixed scratch instead
+    of an allocated workspace, for callers that cannot allocate device memory.
+    Waits for the step and returns its status code."""
+    return lib().wave_step_static(ctypes.byref(cfg), S_max, T_max, S, _ptr(weights), _ptr(kv),
+                                  _ptr(kv_scales), _ptr(positions), _ptr(x), _ptr(y),
+                                  _stream(stream))
 
 
 def kv_quantize(v, codes, scales, stream=None) -> None:

@@ -168,7 +168,6 @@ __device__ void norm_phase(const StepParams& p, Ctx& c, const uint16_t* g, bool 
 
 // ------------------------------------------------------------ GEMM (tcgen05)
 struct Span { long long u0, u1; };
-constexpr int kMaxSeg = 64;  // segments of one tile (checked on the host)
 __device__ __forceinline__ Span cta_span(long long U, int G, int c) {
   return Span{U * c / G, U * (c + 1) / G};
 }
@@ -260,7 +259,7 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
   const long long U = (long long)p.tiles[kind] * KB;
   // Split over min(grid, units, 62 * tiles) CTAs: every participating span is
   // non-empty, the owners of a tile's units are consecutive CTAs, and a tile
-  // has at most kMaxSeg segments.
+  // has at most 64 segments.
   const int G = stream_k_ctas(gridDim.x, U, p.tiles[kind]), cta = blockIdx.x;
   const Span sp = (cta < G) ? cta_span(U, G, cta) : Span{0, 0};
   const int S_pad = p.S_pad, nst = p.nstage;

@@ -144,6 +144,30 @@ int wave_kv_quantize(const float* v, int64_t rows, int D, uint8_t* codes, float*
  * +-448, sign kept): out[i] = E4M3(in[i]).  Asynchronous on `stream`. */
 int wave_fp8_encode(const float* in, int64_t n, uint8_t* out, void* stream);
 
+/*
+ * wave_step for callers that cannot allocate device memory (inside another
+ * runtime's memory pool or a fixed device-memory budget, a plug-in that must
+ * not create untracked allocations, or a real-time loop where cudaMalloc's
+ * implicit synchronisation is not allowed).  The paper has no counterpart:
+ * this is an interface addition of this library.
+ *
+ * Same arguments and layouts as wave_create(cfg, S_max, T_max) followed by
+ * wave_step(S, ...), but no handle and no allocation: the workspace lives in
+ * one fixed 32 MiB device array of the library, present on every GPU that
+ * loads it until the process exits.  Shapes whose workspace does not fit
+ * (roughly: S_max * (2.1 d + 3 H*D + 0.5 F) * 4 bytes of activations plus
+ * split-K and attention partials plus a T_max * D * 4-byte RoPE table)
+ * return WAVE_EINVAL.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  Unlike wave_step the call waits for its step to finish on
+ * `stream` and returns the step's status (WAVE_OK, WAVE_EPOS, WAVE_ETIMEOUT)
+ * directly.  All calls share the array: calls that overlap on the GPU (from
+ * several streams or threads at once) race and must not be made.
+ */
+int wave_step_static(const wave_config* cfg, int S_max, int T_max, int S, const void* weights,
+                     uint8_t* kv_fp8, float* kv_scales, const int32_t* positions, const void* x,
+                     void* y, void* stream);
+
 /* ---- testing hooks (fault tests without a GPU fault) ---------------------
  * Limit for every device-side wait of later steps, in nanoseconds (default
  * 2e9).  A wait that runs out sets WAVE_ETIMEOUT and the kernel returns. */
