@@ -564,18 +564,17 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
       qs_lo[lane * DPL + e] = __float2half_rn(rq[e] - __half2float(hi));
     }
     __syncwarp();
-    // B fragments of the score mma (q is column 0 of B): lanes 0..3 hold
-    // dims [t4*D/4, (t4+1)*D/4); k-step j takes dims +4j..+4j+3.
-    uint32_t qh0[KST], qh1[KST], ql0[KST], ql1[KST];
+    // B fragments of the score mma: column 0 = q_hi (lanes 0..3), column 1 =
+    // q_lo (lanes 4..7), zero elsewhere, so that one mma yields both partial
+    // products; lane t4 holds dims [t4*D/4, (t4+1)*D/4), k-step j takes
+    // dims +4j..+4j+3.
+    uint32_t qb0[KST], qb1[KST];
     {
-      const uint32_t* wh = (const uint32_t*)(qs_hi + t4 * (D / 4));
-      const uint32_t* wl = (const uint32_t*)(qs_lo + t4 * (D / 4));
+      const uint32_t* wq = (const uint32_t*)(((lane < 4) ? qs_hi : qs_lo) + t4 * (D / 4));
 #pragma unroll
       for (int j = 0; j < KST; ++j) {
-        qh0[j] = (lane < 4) ? wh[2 * j] : 0u;
-        qh1[j] = (lane < 4) ? wh[2 * j + 1] : 0u;
-        ql0[j] = (lane < 4) ? wl[2 * j] : 0u;
-        ql1[j] = (lane < 4) ? wl[2 * j + 1] : 0u;
+        qb0[j] = (lane < 8) ? wq[2 * j] : 0u;
+        qb1[j] = (lane < 8) ? wq[2 * j + 1] : 0u;
       }
     }
 
@@ -596,8 +595,8 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
     }
     __syncwarp();
 
-    // acc[j]: c0 = o[dim of row g], c2 = o[dim of row g+8] of P.V m-tile j
-    // (real in lanes with t4 == 0; values in units of R).
+    // acc[j]: c0 + c1 = o[dim of row g], c2 + c3 = o[dim of row g+8] of P.V
+    // m-tile j (w_hi and w_lo parts; real in lanes with t4 == 0; units of R).
     float acc[MTV][4];
 #pragma unroll
     for (int j = 0; j < MTV; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
@@ -639,11 +638,9 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
       // ---- scores S[token] = K . q: 4 m-tiles of 16 tokens, interleaved so
       // that 8 accumulators (m-tile x {q_hi, q_lo}) form independent chains;
       // A = codes of tokens g and g+8 (the lane's KQB bytes), B = q (column 0).
-      float cac[kMT][2][4];
+      float cac[kMT][4];
 #pragma unroll
-      for (int mt = 0; mt < kMT; ++mt)
-#pragma unroll
-        for (int hl = 0; hl < 2; ++hl) cac[mt][hl][0] = cac[mt][hl][1] = cac[mt][hl][2] = cac[mt][hl][3] = 0.f;
+      for (int mt = 0; mt < kMT; ++mt) cac[mt][0] = cac[mt][1] = cac[mt][2] = cac[mt][3] = 0.f;
 #pragma unroll
       for (int ch = 0; ch < KQB / 16; ++ch) {
         uint32_t ka[kMT][4], kb[kMT][4];
@@ -662,16 +659,15 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
             uint32_t a0, a1, a2, a3;
             e4m3x4_to_f16x2x2(ka[mt][jj], a0, a2);
             e4m3x4_to_f16x2x2(kb[mt][jj], a1, a3);
-            mma_f16_16816(cac[mt][0], a0, a1, a2, a3, qh0[j], qh1[j]);
-            mma_f16_16816(cac[mt][1], a0, a1, a2, a3, ql0[j], ql1[j]);
+            mma_f16_16816(cac[mt], a0, a1, a2, a3, qb0[j], qb1[j]);
           }
         }
       }
       float sc[kMT][2];  // [m-tile][token g, token g+8], real where t4 == 0
 #pragma unroll
       for (int mt = 0; mt < kMT; ++mt) {
-        sc[mt][0] = cac[mt][0][0] + cac[mt][1][0];
-        sc[mt][1] = cac[mt][0][2] + cac[mt][1][2];
+        sc[mt][0] = cac[mt][0] + cac[mt][1];  // token g: q_hi part + q_lo part
+        sc[mt][1] = cac[mt][2] + cac[mt][3];  // token g + 8
       }
       // ---- online softmax (base 2) over the lanes with t4 == 0
       float mx = -INFINITY, vmax = 0.f;
@@ -702,7 +698,9 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
 #pragma unroll
       for (int j = 0; j < MTV; ++j) {
         acc[j][0] *= rescale;
+        acc[j][1] *= rescale;
         acc[j][2] *= rescale;
+        acc[j][3] *= rescale;
       }
       R = R_new;
       m_run = m_new;
@@ -735,10 +733,10 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
         const uint32_t hB = __shfl_sync(0xffffffffu, whi[mt], srcB);
         const uint32_t lA = __shfl_sync(0xffffffffu, wlo[mt], srcA);
         const uint32_t lB = __shfl_sync(0xffffffffu, wlo[mt], srcB);
-        const uint32_t bh0 = (lane < 4) ? prmt(hA, hB, 0x5410u) : 0u;
-        const uint32_t bh1 = (lane < 4) ? prmt(hA, hB, 0x7632u) : 0u;
-        const uint32_t bl0 = (lane < 4) ? prmt(lA, lB, 0x5410u) : 0u;
-        const uint32_t bl1 = (lane < 4) ? prmt(lA, lB, 0x7632u) : 0u;
+        // column 0 of B = w_hi (lanes 0..3), column 1 = w_lo (lanes 4..7)
+        const uint32_t xA = (lane < 4) ? hA : lA, xB = (lane < 4) ? hB : lB;
+        const uint32_t bw0 = (lane < 8) ? prmt(xA, xB, 0x5410u) : 0u;
+        const uint32_t bw1 = (lane < 8) ? prmt(xA, xB, 0x7632u) : 0u;
         const int r0 = mt * 16 + 2 * t4;
         const int rows[4] = {r0, r0 + 1, r0 + 8, r0 + 9};
         uint32_t vw[4][VB / 4];
@@ -774,8 +772,7 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
 #pragma unroll
         for (int j = 0; j < MTV; ++j) {
           const uint32_t a0 = f01[j], a1 = f01[j + VB / 2], a2 = f23[j], a3 = f23[j + VB / 2];
-          mma_f16_16816(acc[j], a0, a1, a2, a3, bh0, bh1);
-          mma_f16_16816(acc[j], a0, a1, a2, a3, bl0, bl1);
+          mma_f16_16816(acc[j], a0, a1, a2, a3, bw0, bw1);
         }
       }
       if (last) fence_proxy_async_smem();
@@ -803,8 +800,8 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
         uint16_t* o = p.attn + (size_t)s * HD + h * D + g * VB;
 #pragma unroll
         for (int j = 0; j < MTV; ++j) {
-          o[j] = f32_to_bf16(acc[j][0] * f);
-          o[VB / 2 + j] = f32_to_bf16(acc[j][2] * f);
+          o[j] = f32_to_bf16((acc[j][0] + acc[j][1]) * f);
+          o[VB / 2 + j] = f32_to_bf16((acc[j][2] + acc[j][3]) * f);
         }
       }
     } else {
@@ -812,8 +809,8 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
       if (t4 == 0) {
 #pragma unroll
         for (int j = 0; j < MTV; ++j) {
-          part[g * VB + j] = acc[j][0] * R;
-          part[g * VB + VB / 2 + j] = acc[j][2] * R;
+          part[g * VB + j] = (acc[j][0] + acc[j][1]) * R;
+          part[g * VB + VB / 2 + j] = (acc[j][2] + acc[j][3]) * R;
         }
         if (lane == 0) {
           part[D] = m_run;
