@@ -41,9 +41,10 @@ struct wave_ctx {
   unsigned* bar;
   int* err;
   // cached tensor maps
-  CUtensorMap tm_w[4], tm_x[4], tm_kv;
+  CUtensorMap tm_w[4], tm_x[4], tm_kv, tm_sc;
   const void* maps_weights = nullptr;
   const void* maps_kv = nullptr;
+  const void* maps_sc = nullptr;
   int maps_S = -1;
   cudaStream_t last_stream = nullptr;
   long long timeout_ns = 2000000000LL;
@@ -319,14 +320,23 @@ static int encode_act_maps(wave_ctx* h, int S_pad) {
   return WAVE_OK;
 }
 
-static int encode_kv_map(wave_ctx* h, uint8_t* kv) {
+static int encode_kv_map(wave_ctx* h, uint8_t* kv, float* scales) {
   const wave_config& c = h->cfg;
-  const cuuint64_t D = c.head_dim;
-  const cuuint64_t rows = (cuuint64_t)c.n_layers * 2 * h->S_max * c.n_heads * h->T_max;
-  cuuint64_t dims[2] = {D, rows}, str[1] = {D};
-  cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)kChunk};
-  const auto SW = (D == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  if (!enc(&h->tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv, dims, str, box, SW)) return WAVE_ECUDA;
+  const cuuint64_t D = c.head_dim, L = c.n_layers;
+  const cuuint64_t n1 = (cuuint64_t)h->S_max * c.n_heads * h->T_max;  // slots of one (layer, K|V)
+  {
+    cuuint64_t dims[4] = {D, n1, 2, L}, str[3] = {D, n1 * D, 2 * n1 * D};
+    cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)kChunk, 2, 1};
+    const auto SW = (D == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!enc(&h->tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, kv, dims, str, box, SW)) return WAVE_ECUDA;
+  }
+  {
+    cuuint64_t dims[3] = {n1, 2, L}, str[2] = {n1 * 4, 2 * n1 * 4};
+    cuuint32_t box[3] = {(cuuint32_t)kChunk, 2, 1};
+    if (!enc(&h->tm_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, scales, dims, str, box,
+             CU_TENSOR_MAP_SWIZZLE_NONE))
+      return WAVE_ECUDA;
+  }
   return WAVE_OK;
 }
 
@@ -344,10 +354,11 @@ extern "C" int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8,
     if (rc) return rc;
     h->maps_weights = weights;
   }
-  if (kv_fp8 != h->maps_kv) {
-    int rc = encode_kv_map(h, kv_fp8);
+  if (kv_fp8 != h->maps_kv || kv_scales != h->maps_sc) {
+    int rc = encode_kv_map(h, kv_fp8, kv_scales);
     if (rc) return rc;
     h->maps_kv = kv_fp8;
+    h->maps_sc = kv_scales;
   }
   if (S_pad != h->maps_S) {
     int rc = encode_act_maps(h, S_pad);
@@ -363,6 +374,7 @@ extern "C" int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8,
     p.kblocks[k] = h->kblocks[k];
   }
   p.tm_kv = h->tm_kv;
+  p.tm_sc = h->tm_sc;
   const wave_config& c = h->cfg;
   p.L = c.n_layers;
   p.d = c.d_model;

@@ -11,9 +11,9 @@ constexpr int kThreads = 256;     // 8 warps: TMA producer, MMA issuer, 4 epilog
 constexpr int kWarps = kThreads / 32;
 constexpr int kTileM = 128;       // weight rows per GEMM tile = tcgen05 M
 constexpr int kKBlk = 64;         // K elements per pipeline stage (128 B of bf16)
-constexpr int kChunk = 48;        // attention tokens per async-copy chunk (3 x 16)
-constexpr int kAttStages = 2;     // chunks in flight per attention warp
-constexpr int kPieceChunks = 5;   // chunks per attention work piece (240 tokens)
+constexpr int kChunk = 32;        // attention tokens per async-copy chunk (2 x 16)
+constexpr int kAttStages = 3;     // stages per attention warp (two in flight while one is read)
+constexpr int kPieceChunks = 8;   // chunks per attention work piece (256 tokens)
 constexpr int kMaxStages = 8;     // GEMM ring depth cap
 constexpr int kTmemCols = 256;    // two fp32 accumulators of up to 128 columns
 
@@ -26,7 +26,8 @@ enum GemmKind : int { kQKV = 0, kO = 1, kGU = 2, kDown = 3 };
 struct StepParams {
   CUtensorMap tm_w[4];   // weights of the four projections (see GemmKind)
   CUtensorMap tm_x[4];   // their activation inputs: xn, attn, xn, u (box rows = S_pad)
-  CUtensorMap tm_kv;     // the FP8 history viewed as rows of D bytes
+  CUtensorMap tm_kv;     // the FP8 history as [D][S_max*H*T_max][K|V][L]: one box = a chunk's K and V
+  CUtensorMap tm_sc;     // the scales as [S_max*H*T_max][K|V][L]: one box = a chunk's K and V scales
   // shape
   int L, d, H, D, F, HD, S, S_pad, S_max, T_max;
   float eps;
@@ -80,7 +81,8 @@ cudaError_t occupancy_per_sm(int* blocks);
 int barriers_per_step(int L);
 // Dynamic shared memory layout shared by host checks and the kernel.
 struct SmemLayout {
-  int ring_off, ring_bytes;      // GEMM ring / attention buffers (union)
+  int ring_off, ring_bytes;      // GEMM ring / attention K and V tiles (union)
+  int ascale_off;                // attention K/V scales: kWarps x kAttStages x 256 B
   int xbuf_off;                  // gate/up exchange buffer (64 x 17 fp32)
   int qscr_off;                  // per-warp query scratch (kWarps x 512 B)
   int red_off;                   // reduction scratch (256 words)
@@ -91,8 +93,9 @@ struct SmemLayout {
 __host__ __device__ inline SmemLayout smem_layout() {
   SmemLayout s;
   s.ring_off = 0;
-  s.ring_bytes = 208 * 1024;
-  s.xbuf_off = s.ring_off + s.ring_bytes;            // 64 x 17 fp32
+  s.ring_bytes = 200 * 1024;
+  s.ascale_off = s.ring_off + s.ring_bytes;
+  s.xbuf_off = s.ascale_off + kWarps * kAttStages * 256;  // 64 x 17 fp32
   s.qscr_off = s.xbuf_off + 64 * 17 * 4;             // 3 KB: q as f16 hi + lo per warp
   s.red_off = s.qscr_off + kWarps * 512;             // 1 KB: one int per thread
   s.bar_off = s.red_off + 1024;                      // 64 mbarriers
@@ -100,9 +103,8 @@ __host__ __device__ inline SmemLayout smem_layout() {
   s.total = s.misc_off + 64 + 1024;                  // + alignment slack
   return s;
 }
-__host__ __device__ inline int attn_stage_bytes(int D) {  // K tile, V tile, K scales, V scales; 1 KB aligned
-  int b = 2 * kChunk * D + 2 * 256;  // scales in 256-byte slots
-  return (b + 1023) & ~1023;
+__host__ __device__ inline int attn_stage_bytes(int D) {  // K tile + V tile (scales live apart)
+  return 2 * kChunk * D;
 }
 
 }  // namespace wave

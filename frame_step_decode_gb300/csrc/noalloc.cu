@@ -240,10 +240,15 @@ extern "C" int wave_step_static(const wave_config* cfg, int S_max, int T_max, in
     ok = ok && encode(&p.tm_x[kDown], BF, 2, p.u, d3, s3, box, SW);
   }
   {
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows}, str[1] = {(cuuint64_t)D};
-    cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)kChunk};
-    ok = ok && encode(&p.tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv_fp8, dims, str, box,
+    const cuuint64_t uD = D, n1 = (cuuint64_t)S_max * H * T_max;
+    cuuint64_t dims[4] = {uD, n1, 2, uL}, str[3] = {uD, n1 * uD, 2 * n1 * uD};
+    cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)kChunk, 2, 1};
+    ok = ok && encode(&p.tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, kv_fp8, dims, str, box,
                       D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    cuuint64_t sdims[3] = {n1, 2, uL}, sstr[2] = {n1 * 4, 2 * n1 * 4};
+    cuuint32_t sbox[3] = {(cuuint32_t)kChunk, 2, 1};
+    ok = ok && encode(&p.tm_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, kv_scales, sdims, sstr, sbox,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   if (!ok) return WAVE_ECUDA;
 

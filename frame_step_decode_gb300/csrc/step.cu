@@ -582,13 +582,12 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
     auto issue = [&](int ci, int st) {
       const uint32_t base = wbuf_s + st * stage_bytes;
       const uint32_t fb = bar_att(c, warp, st);
-      const int t0 = ci * kChunk;
-      const uint32_t sbytes = 4u * (uint32_t)min(kChunk, p.T_max - t0);
-      mbar_arrive_expect_tx(fb, 2u * kChunk * D + 2u * sbytes);
-      tma_load_2d_hint(base, &p.tm_kv, 0, (int)(rowK + t0), fb, kv_policy);
-      tma_load_2d_hint(base + kChunk * D, &p.tm_kv, 0, (int)(rowV + t0), fb, kv_policy);
-      bulk_load(base + 2 * kChunk * D, p.kv_scales + rowK + t0, sbytes, fb);
-      bulk_load(base + 2 * kChunk * D + 256, p.kv_scales + rowV + t0, sbytes, fb);
+      // one box holds the chunk's K tile then its V tile; one more its scales
+      const int xrow = sh * p.T_max + ci * kChunk;
+      mbar_arrive_expect_tx(fb, 2u * kChunk * D + 2u * kChunk * 4u);
+      tma_load_4d(base, &p.tm_kv, 0, xrow, 0, layer, fb, kv_policy);
+      const uint32_t sc_s = c.sbase + c.lay.ascale_off + (warp * kAttStages + st) * 256;
+      tma_load_3d(sc_s, &p.tm_sc, xrow, 0, layer, fb, kv_policy);
     };
     if (lane == 0) {
       for (int k = 0; k < min(n, kAttStages); ++k) issue(c_lo + k, (c.att_it + k) % kAttStages);
@@ -614,8 +613,8 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
       }
       uint8_t* kt = wbuf + st * stage_bytes;
       uint8_t* vt = kt + kChunk * D;
-      float* ksm = (float*)(kt + 2 * kChunk * D);
-      float* vsm = ksm + 64;
+      float* ksm = (float*)(c.smem + c.lay.ascale_off + (warp * kAttStages + st) * 256);
+      float* vsm = ksm + 32;
       const bool last = tail && (ci == nch - 1);
       const int valid = last ? (P - ci * kChunk + 1) : kChunk;
       if (last) {  // the current slot: use the codes just written
@@ -934,6 +933,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       prefetch_tmap(&p.tm_x[i]);
     }
     prefetch_tmap(&p.tm_kv);
+    prefetch_tmap(&p.tm_sc);
   }
   if (warp == 1) {
     tmem_alloc(c.sbase + c.lay.misc_off, kTmemCols);
