@@ -489,7 +489,11 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
   if (warp == kWarps - 1 && lane == 0) prefetch_gemm_weights(p, kO, layer);
   __syncwarp();
 
-  for (int pi = gw; pi < n_pieces; pi += NW) {
+  // snake order over the longest-first list: warp gw takes list entries
+  // r*NW + gw for even r and r*NW + NW-1-gw for odd r
+  for (int r = 0;; ++r) {
+    const int pi = r * NW + ((r & 1) ? NW - 1 - gw : gw);
+    if (pi >= n_pieces) break;
     const int4 pc = __ldcg(p.pieces + pi);
     const int sh = pc.x, c_lo = pc.y & 0xFFFF, c_hi = pc.y >> 16, np = pc.z, first = pc.w;
     const int s = sh / H, h = sh - s * H;
@@ -804,7 +808,7 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
         }
       }
     } else {
-      float* part = p.att_part + (size_t)pi * (D + 4);
+      float* part = p.att_part + (size_t)(first + c_lo / kPieceChunks) * (D + 4);
       if (t4 == 0) {
 #pragma unroll
         for (int j = 0; j < MTV; ++j) {
@@ -848,11 +852,20 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
 // ---------------------------------------------------------------- prologue
 // One CTA turns positions into the attention work list: each (session, head)
 // history of pos+1 slots is cut into pieces of up to kPieceChunks chunks.
+// The list is ordered by piece length, longest first (a counting sort over
+// the kPieceChunks possible lengths), and the attention phase deals it out
+// to warps in snake order, which balances the warps' loads.  A piece's slot
+// for its partial result is first + c_lo / kPieceChunks, first being the
+// first slot of its (session, head).
 static_assert(kThreads <= 256, "the reduction scratch holds one word per thread");
+static_assert(kWarps == kPieceChunks, "one warp scans each piece-length class");
+static_assert(kThreads % 32 == 0 && kThreads / 32 <= 8, "lanes scan kThreads/32 entries");
 __device__ void build_pieces(const StepParams& p, Ctx& c) {
-  int* red = (int*)(c.smem + c.lay.red_off);
-  int* spos = (int*)(c.smem + c.lay.xbuf_off);  // positions, -1 where invalid
-  const int N = p.S * p.H, tid = threadIdx.x;
+  int* red = (int*)(c.smem + c.lay.red_off);     // per-thread slot counts -> first slots
+  int* tab = (int*)(c.smem + c.lay.ring_off);    // [length class][thread] counts -> offsets
+  int* cbase = tab + kPieceChunks * kThreads;    // [length class] totals -> list offsets
+  int* spos = (int*)(c.smem + c.lay.xbuf_off);   // positions, -1 where invalid
+  const int N = p.S * p.H, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int s = tid; s < p.S; s += kThreads) {
     const int P = p.pos[s];
     const bool ok = (P >= 0 && P < p.T_max);
@@ -861,36 +874,82 @@ __device__ void build_pieces(const StepParams& p, Ctx& c) {
   }
   __syncthreads();
   const int b0 = (int)((long long)N * tid / kThreads), b1 = (int)((long long)N * (tid + 1) / kThreads);
-  auto count = [&](int sh) {
+  int cc[kPieceChunks];
+#pragma unroll
+  for (int k = 0; k < kPieceChunks; ++k) cc[k] = 0;
+  int slots = 0;
+  for (int sh = b0; sh < b1; ++sh) {
     const int P = spos[sh / p.H];
-    if (P < 0) return 0;
-    const int nch = P / kChunk + 1;
-    return (nch + kPieceChunks - 1) / kPieceChunks;
-  };
-  int local = 0;
-  for (int sh = b0; sh < b1; ++sh) local += count(sh);
-  red[tid] = local;
+    if (P < 0) continue;
+    const int nch = P / kChunk + 1, nf = nch / kPieceChunks, ts = nch % kPieceChunks;
+    cc[kPieceChunks - 1] += nf;
+#pragma unroll
+    for (int k = 0; k < kPieceChunks - 1; ++k) cc[k] += (ts == k + 1) ? 1 : 0;
+    slots += nf + (ts ? 1 : 0);
+  }
+#pragma unroll
+  for (int k = 0; k < kPieceChunks; ++k) tab[k * kThreads + tid] = cc[k];
+  red[tid] = slots;
+  __syncthreads();
+  {  // warp w: exclusive scan over threads of length class kPieceChunks-1-w
+    constexpr int per = kThreads / 32;
+    const int k = kPieceChunks - 1 - warp;
+    int* row = tab + k * kThreads;
+    int v[per], sum = 0;
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+      v[i] = row[lane * per + i];
+      sum += v[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+      row[lane * per + i] = run;
+      run += v[i];
+    }
+    if (lane == 31) cbase[k] = incl;
+  }
   __syncthreads();
   if (tid == 0) {
+    int off = 0;
+    for (int k = kPieceChunks - 1; k >= 0; --k) {  // longest pieces first
+      const int t = cbase[k];
+      cbase[k] = off;
+      off += t;
+    }
+    *p.n_pieces = off;
     int run = 0;
     for (int i = 0; i < kThreads; ++i) {
       const int v = red[i];
       red[i] = run;
       run += v;
     }
-    *p.n_pieces = run;
   }
   __syncthreads();
-  int base = red[tid];
+  int at[kPieceChunks];
+#pragma unroll
+  for (int k = 0; k < kPieceChunks; ++k) at[k] = cbase[k] + tab[k * kThreads + tid];
+  int first = red[tid];
   for (int sh = b0; sh < b1; ++sh) {
-    const int np = count(sh);
-    if (np == 0) continue;
-    const int nch = spos[sh / p.H] / kChunk + 1;
+    const int P = spos[sh / p.H];
+    if (P < 0) continue;
+    const int nch = P / kChunk + 1;
+    const int np = (nch + kPieceChunks - 1) / kPieceChunks;
     for (int q = 0; q < np; ++q) {
       const int lo = q * kPieceChunks, hi = min(nch, lo + kPieceChunks);
-      p.pieces[base + q] = make_int4(sh, lo | (hi << 16), np, base);
+      int idx = 0;
+#pragma unroll
+      for (int k = 0; k < kPieceChunks; ++k)
+        if (hi - lo == k + 1) idx = at[k]++;
+      p.pieces[idx] = make_int4(sh, lo | (hi << 16), np, first);
     }
-    base += np;
+    first += np;
   }
   // sessions with an invalid position get a zero attention output
   for (int s = 0; s < p.S; ++s)
