@@ -34,7 +34,7 @@ struct wave_ctx {
   float* gemm_part;
   int* tile_cnt;
   float* att_part;
-  int* sh_cnt;
+  int2* sh_info;
   int4* pieces;
   int* n_pieces;
   float2* rope;
@@ -203,8 +203,8 @@ extern "C" int wave_create(const wave_config* cfg, int S_max, int T_max, wave_t*
       {(void**)&h->gemm_part, (size_t)h->grid * mt * SP * kTileM * 4},
       {(void**)&h->tile_cnt, 2048 * 4},
       {(void**)&h->att_part, (size_t)(max_pieces * (D + 4) * 4)},
-      {(void**)&h->sh_cnt, (size_t)(S_max * H * 4)},
-      {(void**)&h->pieces, (size_t)(max_pieces * 16)},
+      {(void**)&h->sh_info, (size_t)(S_max * H * 8)},
+      {(void**)&h->pieces, (size_t)(max_pieces * 32)},
       {(void**)&h->n_pieces, 16},
       {(void**)&h->rope, (size_t)T_max * (D / 2) * 8},
       {(void**)&h->bar, 16},
@@ -410,7 +410,7 @@ extern "C" int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8,
   p.gemm_part = h->gemm_part;
   p.tile_cnt = h->tile_cnt;
   p.att_part = h->att_part;
-  p.sh_cnt = h->sh_cnt;
+  p.sh_info = h->sh_info;
   p.pieces = h->pieces;
   p.n_pieces = h->n_pieces;
   p.rope = h->rope;

@@ -13,7 +13,7 @@ constexpr int kTileM = 128;       // weight rows per GEMM tile = tcgen05 M
 constexpr int kKBlk = 64;         // K elements per pipeline stage (128 B of bf16)
 constexpr int kChunk = 32;        // attention tokens per async-copy chunk (2 x 16)
 constexpr int kAttStages = 3;     // stages per attention warp (two in flight while one is read)
-constexpr int kPieceChunks = 8;   // chunks per attention work piece (256 tokens)
+constexpr int kPieceChunks = 16;  // chunks per attention work piece (512 tokens)
 constexpr int kMaxStages = 8;     // GEMM ring depth cap
 constexpr int kTmemCols = 256;    // two fp32 accumulators of up to 128 columns
 
@@ -51,8 +51,8 @@ struct StepParams {
   float* gemm_part;      // [G][max_tiles_per_cta][S_pad][128] split-K partials
   int* tile_cnt;         // [2][1024] per tile: segments arrived, final reducers done
   float* att_part;       // [max pieces][D + 4] (acc, m, l) per attention piece
-  int* sh_cnt;           // [S_max*H] arrivals per (session, head)
-  int4* pieces;          // [max pieces] (sh, c_lo | c_hi << 16, n_pieces_of_sh, first_piece)
+  int2* sh_info;         // [S_max*H] (first partial slot, pieces) per (session, head)
+  int4* pieces;          // [2 * max pieces] (sh, c_lo | c_hi << 16, pieces of sh, first slot), (pos, 0, 0, 0)
   int* n_pieces;         // [1]
   const float2* rope;    // [T_max][D/2] (cos, sin)
   unsigned* bar;         // grid barrier counter (zeroed before each launch)

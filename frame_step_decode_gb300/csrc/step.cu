@@ -3,14 +3,15 @@
 // grid barriers (no CPU round trip between operations: dotwave.ai case study,
 // "02 / The solution" and "04 / Under the hood").
 //
-// Phases per layer l (7 grid barriers per layer):
+// Phases per layer l (8 grid barriers per layer):
 //   norm     RMSNorm rows of the fp32 residual -> bf16 xn           (CUDA cores)
 //   QKV      xn . Wqkv^T -> fp32 q,k,v                              (tcgen05, stream-K)
 //   attn     per (session, head) piece: RoPE(q); the piece holding the
 //            current slot also RoPEs k, quantises k and v to E4M3 and
 //            appends them at slot pos; then split-T flash-decode over the
 //            FP8 history (mma.sync f16 with in-register dequantisation),
-//            partials merged by the last piece to finish    (TMA + mma.sync)
+//            partials of split (session, head) pairs kept     (TMA + mma.sync)
+//   merge    combine the split-T partials -> bf16 attention output
 //   O        resid += attn . Wo^T                                  (tcgen05, stream-K)
 //   norm     RMSNorm -> xn
 //   GU       u = bf16(silu(xn . Wg^T) * (xn . Wu^T))               (tcgen05, stream-K)
@@ -494,16 +495,32 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
   for (int r = 0;; ++r) {
     const int pi = r * NW + ((r & 1) ? NW - 1 - gw : gw);
     if (pi >= n_pieces) break;
-    const int4 pc = __ldcg(p.pieces + pi);
+    const int4 pc = __ldcg(p.pieces + 2 * pi);
+    const int P = __ldcg(p.pieces + 2 * pi + 1).x;
     const int sh = pc.x, c_lo = pc.y & 0xFFFF, c_hi = pc.y >> 16, np = pc.z, first = pc.w;
     const int s = sh / H, h = sh - s * H;
-    const int P = __ldcg(p.pos + s);
     const int nch = P / kChunk + 1;
     const bool tail = (c_hi == nch);
     const float* qrow = p.qkv + (size_t)s * 3 * HD + h * D;
     const float2* cs = p.rope + (size_t)P * (D / 2);
     const size_t rowK = ((((size_t)layer * 2 + 0) * p.S_max + s) * H + h) * (size_t)p.T_max;
     const size_t rowV = ((((size_t)layer * 2 + 1) * p.S_max + s) * H + h) * (size_t)p.T_max;
+    // start the copies first: the q / k / v work below overlaps their latency
+    const int n = c_hi - c_lo;
+    auto issue = [&](int ci, int st) {
+      const uint32_t base = wbuf_s + st * stage_bytes;
+      const uint32_t fb = bar_att(c, warp, st);
+      // one box holds the chunk's K tile then its V tile; one more its scales
+      const int xrow = sh * p.T_max + ci * kChunk;
+      mbar_arrive_expect_tx(fb, 2u * kChunk * D + 2u * kChunk * 4u);
+      tma_load_4d(base, &p.tm_kv, 0, xrow, 0, layer, fb, kv_policy);
+      const uint32_t sc_s = c.sbase + c.lay.ascale_off + (warp * kAttStages + st) * 256;
+      tma_load_3d(sc_s, &p.tm_sc, xrow, 0, layer, fb, kv_policy);
+    };
+    if (lane == 0) {
+      for (int k = 0; k < min(n, kAttStages); ++k) issue(c_lo + k, (c.att_it + k) % kAttStages);
+    }
+    __syncwarp();
 
     // RoPE of q (and k) in fp32: lane i holds dims [i*DPL, (i+1)*DPL); its
     // rotate-half partner dims are in lane i^16.
@@ -582,21 +599,6 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
       }
     }
 
-    const int n = c_hi - c_lo;
-    auto issue = [&](int ci, int st) {
-      const uint32_t base = wbuf_s + st * stage_bytes;
-      const uint32_t fb = bar_att(c, warp, st);
-      // one box holds the chunk's K tile then its V tile; one more its scales
-      const int xrow = sh * p.T_max + ci * kChunk;
-      mbar_arrive_expect_tx(fb, 2u * kChunk * D + 2u * kChunk * 4u);
-      tma_load_4d(base, &p.tm_kv, 0, xrow, 0, layer, fb, kv_policy);
-      const uint32_t sc_s = c.sbase + c.lay.ascale_off + (warp * kAttStages + st) * 256;
-      tma_load_3d(sc_s, &p.tm_sc, xrow, 0, layer, fb, kv_policy);
-    };
-    if (lane == 0) {
-      for (int k = 0; k < min(n, kAttStages); ++k) issue(c_lo + k, (c.att_it + k) % kAttStages);
-    }
-    __syncwarp();
 
     // acc[j]: c0 + c1 = o[dim of row g], c2 + c3 = o[dim of row g+8] of P.V
     // m-tile j (w_hi and w_lo parts; real in lanes with t4 == 0; units of R).
@@ -808,6 +810,8 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
         }
       }
     } else {
+      // split (session, head): store this piece's (acc, m, l); the merge phase
+      // combines them after the next grid barrier
       float* part = p.att_part + (size_t)(first + c_lo / kPieceChunks) * (D + 4);
       if (t4 == 0) {
 #pragma unroll
@@ -820,32 +824,65 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
           part[D + 1] = l_run;
         }
       }
-      __threadfence();
-      __syncwarp();
-      int last_arrival = 0;
-      if (lane == 0) last_arrival = (atomicAdd(p.sh_cnt + sh, 1) == np - 1);
-      last_arrival = __shfl_sync(0xffffffffu, last_arrival, 0);
-      if (last_arrival) {
-        __threadfence();
-        float M = -INFINITY;
-        for (int i = 0; i < np; ++i) M = fmaxf(M, __ldcg(p.att_part + (size_t)(first + i) * (D + 4) + D));
-        float Ls = 0.f, o[DPL];
+    }
+  }
+}
+
+// --------------------------------------------------------------- merge
+// Combine the split-T partials of every (session, head) cut into several
+// pieces, in piece order: M = max m_i, L = sum l_i 2^(m_i - M),
+// o = sum acc_i 2^(m_i - M) / L, written as bf16; one warp per (session,
+// head), lane i owning dims [i*D/32, (i+1)*D/32).
+constexpr int kMergeMax = 4;
+template <int D>
+__device__ void merge_phase(const StepParams& p, Ctx& c) {
+  constexpr int DPL = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int NW = gridDim.x * kWarps;
+  const int N = p.S * p.H;
+  for (int sh = blockIdx.x * kWarps + (threadIdx.x >> 5); sh < N; sh += NW) {
+    const int2 info = __ldcg(p.sh_info + sh);
+    const int first = info.x, np = info.y;
+    if (np <= 1) continue;
+    float M = -INFINITY;
+    for (int i0 = 0; i0 < np; i0 += kMergeMax) {
+      float mv[kMergeMax];
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) o[e] = 0.f;
-        for (int i = 0; i < np; ++i) {
-          const float* pp = p.att_part + (size_t)(first + i) * (D + 4);
-          const float wgt = ex2(__ldcg(pp + D) - M);
-          Ls += __ldcg(pp + D + 1) * wgt;
+      for (int i = 0; i < kMergeMax; ++i)
+        mv[i] = (i0 + i < np) ? __ldcg(p.att_part + (size_t)(first + i0 + i) * (D + 4) + D) : -INFINITY;
 #pragma unroll
-          for (int e = 0; e < DPL; ++e) o[e] += __ldcg(pp + lane * DPL + e) * wgt;
+      for (int i = 0; i < kMergeMax; ++i) M = fmaxf(M, mv[i]);
+    }
+    float Ls = 0.f, o[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[e] = 0.f;
+    for (int i0 = 0; i0 < np; i0 += kMergeMax) {
+      float mv[kMergeMax], lv[kMergeMax], ov[kMergeMax][DPL];
+#pragma unroll
+      for (int i = 0; i < kMergeMax; ++i) {
+        if (i0 + i < np) {
+          const float* pp = p.att_part + (size_t)(first + i0 + i) * (D + 4);
+          mv[i] = __ldcg(pp + D);
+          lv[i] = __ldcg(pp + D + 1);
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) ov[i][e] = __ldcg(pp + lane * DPL + e);
         }
-        const float inv = 1.0f / Ls;
-        uint16_t* od = p.attn + (size_t)s * HD + h * D + lane * DPL;
+      }
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) od[e] = f32_to_bf16(o[e] * inv);
-        if (lane == 0) p.sh_cnt[sh] = 0;
+      for (int i = 0; i < kMergeMax; ++i) {
+        if (i0 + i < np) {
+          const float wgt = ex2(mv[i] - M);
+          Ls += lv[i] * wgt;
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) o[e] += ov[i][e] * wgt;
+        }
       }
     }
+    const float inv = 1.0f / Ls;
+    const int s = sh / p.H, h = sh - s * p.H;
+    uint16_t* od = p.attn + (size_t)s * p.HD + h * D + lane * DPL;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) od[e] = f32_to_bf16(o[e] * inv);
   }
 }
 
@@ -858,7 +895,7 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
 // for its partial result is first + c_lo / kPieceChunks, first being the
 // first slot of its (session, head).
 static_assert(kThreads <= 256, "the reduction scratch holds one word per thread");
-static_assert(kWarps == kPieceChunks, "one warp scans each piece-length class");
+static_assert(kPieceChunks % kWarps == 0, "each warp scans kPieceChunks / kWarps length classes");
 static_assert(kThreads % 32 == 0 && kThreads / 32 <= 8, "lanes scan kThreads/32 entries");
 __device__ void build_pieces(const StepParams& p, Ctx& c) {
   int* red = (int*)(c.smem + c.lay.red_off);     // per-thread slot counts -> first slots
@@ -891,9 +928,8 @@ __device__ void build_pieces(const StepParams& p, Ctx& c) {
   for (int k = 0; k < kPieceChunks; ++k) tab[k * kThreads + tid] = cc[k];
   red[tid] = slots;
   __syncthreads();
-  {  // warp w: exclusive scan over threads of length class kPieceChunks-1-w
+  for (int k = kPieceChunks - 1 - warp; k >= 0; k -= kWarps) {  // exclusive scan over threads
     constexpr int per = kThreads / 32;
-    const int k = kPieceChunks - 1 - warp;
     int* row = tab + k * kThreads;
     int v[per], sum = 0;
 #pragma unroll
@@ -938,16 +974,21 @@ __device__ void build_pieces(const StepParams& p, Ctx& c) {
   int first = red[tid];
   for (int sh = b0; sh < b1; ++sh) {
     const int P = spos[sh / p.H];
-    if (P < 0) continue;
+    if (P < 0) {
+      p.sh_info[sh] = make_int2(0, 0);
+      continue;
+    }
     const int nch = P / kChunk + 1;
     const int np = (nch + kPieceChunks - 1) / kPieceChunks;
+    p.sh_info[sh] = make_int2(first, np);
     for (int q = 0; q < np; ++q) {
       const int lo = q * kPieceChunks, hi = min(nch, lo + kPieceChunks);
       int idx = 0;
 #pragma unroll
       for (int k = 0; k < kPieceChunks; ++k)
         if (hi - lo == k + 1) idx = at[k]++;
-      p.pieces[idx] = make_int4(sh, lo | (hi << 16), np, first);
+      p.pieces[2 * idx] = make_int4(sh, lo | (hi << 16), np, first);
+      p.pieces[2 * idx + 1] = make_int4(P, 0, 0, 0);
     }
     first += np;
   }
@@ -1005,8 +1046,6 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 
   if (p.phase_ts && blockIdx.x == 0 && threadIdx.x == 0) p.phase_ts[0] = globaltimer();
   // phase 0: work list, counter reset, residual and first norm
-  for (int i = blockIdx.x * kThreads + threadIdx.x; i < p.S_max * p.H; i += gridDim.x * kThreads)
-    p.sh_cnt[i] = 0;
   for (int i = blockIdx.x * kThreads + threadIdx.x; i < 2048; i += gridDim.x * kThreads)
     p.tile_cnt[i] = 0;
   if (blockIdx.x == gridDim.x - 1) build_pieces(p, c);
@@ -1022,6 +1061,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     gemm_phase(p, c, kQKV, l, false);
     if (!(ok = grid_sync(p, c))) break;
     if (p.D == 128) attention_phase<128>(p, c, l); else attention_phase<64>(p, c, l);
+    if (!(ok = grid_sync(p, c))) break;
+    if (p.D == 128) merge_phase<128>(p, c); else merge_phase<64>(p, c);
     if (!(ok = grid_sync(p, c))) break;
     gemm_phase(p, c, kO, l, false);
     if (!(ok = grid_sync(p, c))) break;
@@ -1067,7 +1108,7 @@ cudaError_t launch_step(const StepParams& p, int grid, cudaStream_t stream) {
                                      (size_t)smem_layout().total, stream);
 }
 
-int barriers_per_step(int L) { return 7 * L - 1; }
+int barriers_per_step(int L) { return 8 * L - 1; }
 
 cudaError_t occupancy_per_sm(int* blocks) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel, kThreads,
