@@ -36,7 +36,7 @@ class WaveError(RuntimeError):
 _lib = None
 EXPORTS = ("wave_create", "wave_destroy", "wave_weights_bytes", "wave_weight_offset", "wave_step",
            "wave_status", "wave_strerror", "wave_kv_quantize", "wave_fp8_encode", "wave_step_static",
-           "wave_set_timeout_ns", "wave_debug_skip_barrier", "wave_debug_dump_kv", "wave_debug_phase_times",
+           "wave_set_timeout_ns", "wave_debug_skip_barrier", "wave_debug_dump_kv", "wave_debug_phase_times", "wave_debug_arrival_times",
            "wave_grid_size",
            "wave_barriers_per_step")
 
@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
         L.wave_debug_dump_kv.restype = i32
         L.wave_debug_phase_times.argtypes = [vp, vp]
         L.wave_debug_phase_times.restype = i32
+        L.wave_debug_arrival_times.argtypes = [vp, vp]
+        L.wave_debug_arrival_times.restype = i32
         L.wave_grid_size.argtypes = [vp]
         L.wave_grid_size.restype = i32
         L.wave_barriers_per_step.argtypes = [vp]
@@ -153,6 +155,12 @@ class Wave:
         """Profiling hook: later steps write globaltimer stamps (int64) at
         entry, after every grid barrier and at exit into dst; None disables."""
         lib().wave_debug_phase_times(self.h, _ptr(dst))
+
+    def debug_arrival_times(self, dst) -> None:
+        """Profiling hook: later steps write each CTA's globaltimer stamp at
+        each grid barrier arrival into dst ([barriers][grid] int64); None
+        disables."""
+        lib().wave_debug_arrival_times(self.h, _ptr(dst))
 
     @property
     def grid(self) -> int:

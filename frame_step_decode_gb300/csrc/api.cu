@@ -51,6 +51,7 @@ struct wave_ctx {
   int skip_cta = -1, skip_bar = -1;
   float* kv_dump = nullptr;
   long long* phase_ts = nullptr;
+  long long* arrive_ts = nullptr;
 };
 
 static EncodeTiledFn encode_fn() {
@@ -421,6 +422,7 @@ extern "C" int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8,
   p.skip_bar = h->skip_bar;
   p.kv_dump = h->kv_dump;
   p.phase_ts = h->phase_ts;
+  p.arrive_ts = h->arrive_ts;
   if (cudaMemsetAsync(h->bar, 0, 4, st) != cudaSuccess) return WAVE_ECUDA;
   cudaError_t e = launch_step(p, h->grid, st);
   h->last_stream = st;
@@ -462,6 +464,12 @@ extern "C" int wave_debug_dump_kv(wave_t* h, float* dst) {
 extern "C" int wave_debug_phase_times(wave_t* h, long long* dst) {
   if (!h) return WAVE_EINVAL;
   h->phase_ts = dst;
+  return WAVE_OK;
+}
+
+extern "C" int wave_debug_arrival_times(wave_t* h, long long* dst) {
+  if (!h) return WAVE_EINVAL;
+  h->arrive_ts = dst;
   return WAVE_OK;
 }
 

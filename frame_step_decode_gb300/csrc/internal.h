@@ -61,6 +61,7 @@ struct StepParams {
   int skip_cta, skip_bar;
   float* kv_dump;        // testing hook: [L][2][S_max][H][D] pre-quantisation K/V, or null
   long long* phase_ts;   // profiling hook: globaltimer at start, after each barrier, at end
+  long long* arrive_ts;  // profiling hook: [barrier][cta] globaltimer at barrier arrival
 };
 
 // CTAs taking part in a stream-K GEMM phase of `tiles` tiles and U units.

@@ -82,6 +82,7 @@ __device__ bool grid_sync(const StepParams& p, Ctx& c) {
     c.bar_target += gridDim.x;
     __threadfence();
     bool skip = ((int)blockIdx.x == p.skip_cta && c.bar_index == p.skip_bar);
+    if (p.arrive_ts) p.arrive_ts[(size_t)c.bar_index * gridDim.x + blockIdx.x] = globaltimer();
     if (!skip) atomicAdd(p.bar, 1u);
     int ok = 1;
     long long t0 = globaltimer();
@@ -202,7 +203,8 @@ __device__ void prefetch_gemm_weights(const StepParams& p, int kind, int layer) 
 }
 
 __device__ __forceinline__ void epilogue_apply(const StepParams& p, Ctx& c, int kind, int t, int r,
-                                               int col0, const float* v, bool last_layer) {
+                                               int col0, const float* v, bool last_layer,
+                                               const float* old_in = nullptr) {
   const int S = p.S;
   if (kind == kQKV) {
     const int N = 3 * p.HD, n = t * kTileM + r;
@@ -218,7 +220,7 @@ __device__ __forceinline__ void epilogue_apply(const StepParams& p, Ctx& c, int 
       float old[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        old[i] = (col0 + i < S) ? __ldcg(p.resid + (size_t)(col0 + i) * d + n) : 0.f;
+        old[i] = old_in ? old_in[i] : ((col0 + i < S) ? __ldcg(p.resid + (size_t)(col0 + i) * d + n) : 0.f);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int s = col0 + i;
@@ -416,29 +418,75 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
             seg[j] = ((long long)cj * MT + (t - ftj)) * (long long)S_pad * kTileM;
           }
           named_bar(1, 128);
-          for (int cc = idx; cc < S_pad / 16; cc += m) {
-            const int col = cc * 16;
-            float v[16];
+          const int NC = S_pad / 16;
+          const bool resid_kind = (kind == kO || kind == kDown);
+          const int n_out = t * kTileM + r;
+          if (nseg <= 2) {
+            // two column chunks per batch: 2 x 2 x 16 partial loads in flight
+            for (int cc = idx; cc < NC; cc += 2 * m) {
+              const int cc2 = cc + m;
+              const bool two = cc2 < NC;
+              float a[2][2][16], olda[2][16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = 0.f;
-            for (int j0 = 0; j0 < nseg; j0 += 4) {
-              // up to 4 segments x 16 columns of loads in flight, summed in order
-              float tmp[4][16];
+              for (int h2 = 0; h2 < 2; ++h2) {
+                const int col = (h2 == 0 ? cc : cc2) * 16;
+                const bool live = (h2 == 0) || two;
 #pragma unroll
-              for (int jj = 0; jj < 4; ++jj)
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                  for (int i = 0; i < 16; ++i)
+                    a[h2][j][i] = (live && j < nseg)
+                                      ? __ldcg(p.gemm_part + seg[j] + (size_t)(col + i) * kTileM + r)
+                                      : 0.f;
+                if (resid_kind) {
+#pragma unroll
+                  for (int i = 0; i < 16; ++i)
+                    olda[h2][i] = (live && n_out < p.d && col + i < p.S)
+                                      ? __ldcg(p.resid + (size_t)(col + i) * p.d + n_out)
+                                      : 0.f;
+                }
+              }
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {
+                if (h2 == 1 && !two) break;
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = a[h2][0][i] + (nseg > 1 ? a[h2][1][i] : 0.f);
+                epilogue_apply(p, c, kind, t, r, (h2 == 0 ? cc : cc2) * 16, v, last_layer,
+                               resid_kind ? olda[h2] : nullptr);
+              }
+            }
+          } else {
+            // one column chunk per batch: up to 4 segments x 16 partial loads (the
+            // first batch together with the residual) in flight; summed in segment order
+            for (int cc = idx; cc < NC; cc += m) {
+              const int col = cc * 16;
+              float v[16], olda[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = 0.f;
+              if (resid_kind) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                  tmp[jj][i] = (j0 + jj < nseg)
-                                   ? __ldcg(p.gemm_part + seg[j0 + jj] + (size_t)(col + i) * kTileM + r)
-                                   : 0.f;
+                  olda[i] = (n_out < p.d && col + i < p.S) ? __ldcg(p.resid + (size_t)(col + i) * p.d + n_out) : 0.f;
+              }
+              for (int j0 = 0; j0 < nseg; j0 += 4) {
+                float tmp[4][16];
 #pragma unroll
-              for (int jj = 0; jj < 4; ++jj)
-                if (j0 + jj < nseg) {
+                for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
-                  for (int i = 0; i < 16; ++i) v[i] += tmp[jj][i];
-                }
+                  for (int i = 0; i < 16; ++i)
+                    tmp[jj][i] = (j0 + jj < nseg)
+                                     ? __ldcg(p.gemm_part + seg[j0 + jj] + (size_t)(col + i) * kTileM + r)
+                                     : 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                  if (j0 + jj < nseg) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] += tmp[jj][i];
+                  }
+              }
+              epilogue_apply(p, c, kind, t, r, col, v, last_layer, resid_kind ? olda : nullptr);
             }
-            epilogue_apply(p, c, kind, t, r, col, v, last_layer);
           }
           named_bar(1, 128);
           // the last final contributor to finish re-arms the tile's counters

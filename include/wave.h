@@ -185,6 +185,11 @@ int wave_debug_dump_kv(wave_t* h, float* dst);
  * when grid barrier b released CTA 0, and the last entry at kernel exit.
  * dst = NULL disables. */
 int wave_debug_phase_times(wave_t* h, long long* dst);
+/* Profiling hook: later steps write, into the device buffer dst of
+ * wave_barriers_per_step(h) x wave_grid_size(h) int64, the globaltimer value
+ * at which each CTA arrived at each grid barrier ([barrier][cta]), so that
+ * the spread of a phase's finishing times can be read.  dst = NULL disables. */
+int wave_debug_arrival_times(wave_t* h, long long* dst);
 /* Grid size (CTAs, one per SM) and barriers per step, for tests and tools. */
 int wave_grid_size(wave_t* h);
 int wave_barriers_per_step(wave_t* h);
