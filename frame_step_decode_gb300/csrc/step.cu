@@ -41,6 +41,7 @@ struct Ctx {
   uint32_t ring_it;     // GEMM ring stage counter (producer and MMA threads)
   uint32_t acc_it;      // accumulator counter (MMA and epilogue threads)
   uint32_t att_it;      // attention chunk counter (per warp)
+  uint32_t norm_it;     // norm-row copy counter (all threads)
   SmemLayout lay;
 };
 
@@ -52,7 +53,13 @@ __device__ __forceinline__ uint32_t bar_acce(const Ctx& c, int i) { return c.sba
 __device__ __forceinline__ uint32_t bar_att(const Ctx& c, int w, int st) {
   return c.sbase + c.lay.bar_off + 160 + 8 * (w * kAttStages + st);
 }
-__device__ __forceinline__ uint32_t bar_drain(const Ctx& c) { return c.sbase + c.lay.bar_off + 320; }
+__device__ __forceinline__ uint32_t bar_drain(const Ctx& c) {
+  return c.sbase + c.lay.bar_off + 160 + 8 * kWarps * kAttStages;
+}
+__device__ __forceinline__ uint32_t bar_norm(const Ctx& c) {
+  return c.sbase + c.lay.bar_off + 168 + 8 * kWarps * kAttStages;
+}
+static_assert(176 + 8 * kWarps * kAttStages <= 64 * 8, "mbarrier slots exceed their region");
 __device__ __forceinline__ volatile int* misc_word(const Ctx& c, int i) {
   return (volatile int*)(c.smem + c.lay.misc_off + 4 * i);
 }
@@ -109,39 +116,54 @@ __device__ bool grid_sync(const StepParams& p, Ctx& c) {
 
 // ------------------------------------------------------------------- norm
 // xn[s] = bf16(r * rstd * g), rstd = 1/sqrt(mean(r^2) + eps); one row per CTA
-// (rows strided over CTAs), the row held in registers as float4s so that its
-// loads are all in flight at once.  At layer 0 the residual is first loaded
-// from x (bf16).
-constexpr int kNormVec = 11;  // float4s per thread: d <= 4 * kThreads * kNormVec
-__device__ void norm_phase(const StepParams& p, Ctx& c, const uint16_t* g, bool from_x) {
+// (rows strided over CTAs).  One thread bulk-copies the residual row (at
+// layer 0 the bf16 input row x) and g into the idle GEMM ring, so that the
+// whole row arrives in one round trip with no register staging, then the
+// block reduces the sum of squares and writes xn.  Returns false if the copy
+// wait gave up.
+__device__ bool norm_phase(const StepParams& p, Ctx& c, const uint16_t* g, bool from_x) {
   float* red = (float*)(c.smem + c.lay.red_off);
   const int d = p.d, d4 = d / 4, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float* rrow = (float*)(c.smem + c.lay.ring_off);                       // d fp32
+  const uint16_t* grow = (const uint16_t*)(c.smem + c.lay.ring_off + 4 * d);  // d bf16
+  const uint16_t* xrow = (const uint16_t*)(c.smem + c.lay.ring_off + 6 * d);  // d bf16 (layer 0)
+  const uint32_t nbar = bar_norm(c);
   for (int s = blockIdx.x; s < p.S; s += gridDim.x) {
-    float4* r4 = (float4*)(p.resid + (size_t)s * d);
-    float4 rv[kNormVec];
-    float ss = 0.f;
-#pragma unroll
-    for (int k = 0; k < kNormVec; ++k) {
-      const int i4 = tid + k * kThreads;
-      if (i4 < d4) {
-        if (from_x) {
-          const uint2 xb = *(const uint2*)(p.x + (size_t)s * d + 4 * i4);
-          rv[k] = make_float4(bf16_to_f32((uint16_t)(xb.x & 0xFFFF)), bf16_to_f32((uint16_t)(xb.x >> 16)),
-                              bf16_to_f32((uint16_t)(xb.y & 0xFFFF)), bf16_to_f32((uint16_t)(xb.y >> 16)));
-          r4[i4] = rv[k];
-        } else {
-          rv[k] = __ldcg(r4 + i4);
-        }
-      }
+    if (tid == 0) {
+      fence_proxy_async_smem();  // earlier generic accesses to this area come first
+      mbar_arrive_expect_tx(nbar, (from_x ? 4u : 6u) * (uint32_t)d);  // row + g
+      if (from_x)
+        bulk_load(c.sbase + c.lay.ring_off + 6 * d, p.x + (size_t)s * d, 2u * d, nbar);
+      else
+        bulk_load(c.sbase + c.lay.ring_off, p.resid + (size_t)s * d, 4u * d, nbar);
+      bulk_load(c.sbase + c.lay.ring_off + 4 * d, g, 2u * d, nbar);
     }
-#pragma unroll
-    for (int k = 0; k < kNormVec; ++k) {
-      if (tid + k * kThreads < d4) {
-        ss = fmaf(rv[k].x, rv[k].x, ss);
-        ss = fmaf(rv[k].y, rv[k].y, ss);
-        ss = fmaf(rv[k].z, rv[k].z, ss);
-        ss = fmaf(rv[k].w, rv[k].w, ss);
+    // one thread waits (bounded) and the block takes its decision
+    if (tid == 0) {
+      const bool ok0 = mbar_wait(nbar, c.norm_it & 1u, p.timeout_ns, p.err);
+      if (!ok0) set_err(p, kErrTimeout);
+      *misc_word(c, 6) = ok0 ? 1 : 0;
+    }
+    c.norm_it++;
+    __syncthreads();
+    if (!*misc_word(c, 6)) return false;
+    float ss = 0.f;
+#pragma unroll 1
+    for (int i4 = tid; i4 < d4; i4 += kThreads) {
+      float4 v;
+      if (from_x) {
+        const uint2 xb = *(const uint2*)(xrow + 4 * i4);
+        v = make_float4(bf16_to_f32((uint16_t)(xb.x & 0xFFFF)), bf16_to_f32((uint16_t)(xb.x >> 16)),
+                        bf16_to_f32((uint16_t)(xb.y & 0xFFFF)), bf16_to_f32((uint16_t)(xb.y >> 16)));
+        ((float4*)rrow)[i4] = v;
+        ((float4*)(p.resid + (size_t)s * d))[i4] = v;
+      } else {
+        v = ((const float4*)rrow)[i4];
       }
+      ss = fmaf(v.x, v.x, ss);
+      ss = fmaf(v.y, v.y, ss);
+      ss = fmaf(v.z, v.z, ss);
+      ss = fmaf(v.w, v.w, ss);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -151,21 +173,21 @@ __device__ void norm_phase(const StepParams& p, Ctx& c, const uint16_t* g, bool 
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) tot += red[w];
     const float rstd = 1.0f / sqrtf(tot / (float)d + p.eps);
-#pragma unroll
-    for (int k = 0; k < kNormVec; ++k) {
-      const int i4 = tid + k * kThreads;
-      if (i4 < d4) {
-        const uint2 gb = *(const uint2*)(g + 4 * i4);
-        const float g0 = bf16_to_f32((uint16_t)(gb.x & 0xFFFF)), g1 = bf16_to_f32((uint16_t)(gb.x >> 16));
-        const float g2 = bf16_to_f32((uint16_t)(gb.y & 0xFFFF)), g3 = bf16_to_f32((uint16_t)(gb.y >> 16));
-        uint2 o;
-        o.x = (uint32_t)f32_to_bf16((rv[k].x * rstd) * g0) | ((uint32_t)f32_to_bf16((rv[k].y * rstd) * g1) << 16);
-        o.y = (uint32_t)f32_to_bf16((rv[k].z * rstd) * g2) | ((uint32_t)f32_to_bf16((rv[k].w * rstd) * g3) << 16);
-        *(uint2*)(p.xn + (size_t)s * d + 4 * i4) = o;
-      }
+#pragma unroll 1
+    for (int i4 = tid; i4 < d4; i4 += kThreads) {
+      const float4 v = ((const float4*)rrow)[i4];
+      const uint2 gb = *(const uint2*)(grow + 4 * i4);
+      const float g0 = bf16_to_f32((uint16_t)(gb.x & 0xFFFF)), g1 = bf16_to_f32((uint16_t)(gb.x >> 16));
+      const float g2 = bf16_to_f32((uint16_t)(gb.y & 0xFFFF)), g3 = bf16_to_f32((uint16_t)(gb.y >> 16));
+      uint2 o;
+      o.x = (uint32_t)f32_to_bf16((v.x * rstd) * g0) | ((uint32_t)f32_to_bf16((v.y * rstd) * g1) << 16);
+      o.y = (uint32_t)f32_to_bf16((v.z * rstd) * g2) | ((uint32_t)f32_to_bf16((v.w * rstd) * g3) << 16);
+      *(uint2*)(p.xn + (size_t)s * d + 4 * i4) = o;
     }
     __syncthreads();
   }
+  fence_proxy_async_smem();  // the next phase's copies overwrite this area
+  return true;
 }
 
 // ------------------------------------------------------------ GEMM (tcgen05)
@@ -203,8 +225,7 @@ __device__ void prefetch_gemm_weights(const StepParams& p, int kind, int layer) 
 }
 
 __device__ __forceinline__ void epilogue_apply(const StepParams& p, Ctx& c, int kind, int t, int r,
-                                               int col0, const float* v, bool last_layer,
-                                               const float* old_in = nullptr) {
+                                               int col0, const float* v, bool last_layer) {
   const int S = p.S;
   if (kind == kQKV) {
     const int N = 3 * p.HD, n = t * kTileM + r;
@@ -220,7 +241,7 @@ __device__ __forceinline__ void epilogue_apply(const StepParams& p, Ctx& c, int 
       float old[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        old[i] = old_in ? old_in[i] : ((col0 + i < S) ? __ldcg(p.resid + (size_t)(col0 + i) * d + n) : 0.f);
+        old[i] = (col0 + i < S) ? __ldcg(p.resid + (size_t)(col0 + i) * d + n) : 0.f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int s = col0 + i;
@@ -253,6 +274,68 @@ __device__ __forceinline__ void epilogue_apply(const StepParams& p, Ctx& c, int 
       }
     }
     named_bar(2, 128);
+  }
+}
+
+__device__ __forceinline__ float4 ld4cg(const float* q) { return __ldcg((const float4*)q); }
+__device__ __forceinline__ void add4(float4& a, const float4& b) {
+  a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+}
+// Sum, in segment order, of the float4 at element offsets o0 / o1 of each of
+// a split tile's partial slots (offsets seg[0..nseg)); the first three
+// segments' loads in flight together, two more per later pass.
+__device__ __forceinline__ void seg_sum2(const float* part, const long long* seg, int nseg,
+                                         size_t o0, size_t o1, float4& a0, float4& a1) {
+  a0 = ld4cg(part + seg[0] + o0);
+  a1 = ld4cg(part + seg[0] + o1);
+  for (int j = 1; j < nseg; j += 2) {
+    float4 t0[2], t1[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      if (j + k < nseg) {
+        t0[k] = ld4cg(part + seg[j + k] + o0);
+        t1[k] = ld4cg(part + seg[j + k] + o1);
+      }
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      if (j + k < nseg) {
+        add4(a0, t0[k]);
+        add4(a1, t1[k]);
+      }
+  }
+}
+// The same for four offsets (gate and up rows of two items), one segment per
+// later pass.
+__device__ __forceinline__ void seg_sum4(const float* part, const long long* seg, int nseg,
+                                         size_t o0, size_t o1, size_t o2, size_t o3,
+                                         float4& a0, float4& a1, float4& a2, float4& a3) {
+  const float* b = part + seg[0];
+  a0 = ld4cg(b + o0); a1 = ld4cg(b + o1); a2 = ld4cg(b + o2); a3 = ld4cg(b + o3);
+  for (int j = 1; j < nseg; ++j) {
+    const float* bk = part + seg[j];
+    const float4 t0 = ld4cg(bk + o0), t1 = ld4cg(bk + o1), t2 = ld4cg(bk + o2), t3 = ld4cg(bk + o3);
+    add4(a0, t0); add4(a1, t1); add4(a2, t2); add4(a3, t3);
+  }
+}
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+// u[n..n+3] = bf16(silu(gate) * up) for one session row (F % 4 == 0).
+__device__ __forceinline__ void swiglu_store(uint16_t* urow, int n, int F, const float4& g, const float4& u) {
+  if (n >= F) return;
+  uint2 o;
+  o.x = (uint32_t)f32_to_bf16(silu_mul(g.x, u.x)) | ((uint32_t)f32_to_bf16(silu_mul(g.y, u.y)) << 16);
+  o.y = (uint32_t)f32_to_bf16(silu_mul(g.z, u.z)) | ((uint32_t)f32_to_bf16(silu_mul(g.w, u.w)) << 16);
+  *(uint2*)(urow + n) = o;
+}
+// resid[s][n..n+3] = old + v (and y = bf16 of it after the last layer).
+__device__ __forceinline__ void resid_store(const StepParams& p, int s, int n, float4 old, const float4& v,
+                                            bool last_layer) {
+  add4(old, v);
+  *(float4*)(p.resid + (size_t)s * p.d + n) = old;
+  if (last_layer) {
+    uint2 o;
+    o.x = (uint32_t)f32_to_bf16(old.x) | ((uint32_t)f32_to_bf16(old.y) << 16);
+    o.y = (uint32_t)f32_to_bf16(old.z) | ((uint32_t)f32_to_bf16(old.w) << 16);
+    *(uint2*)(p.y + (size_t)s * p.d + n) = o;
   }
 }
 
@@ -418,74 +501,55 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
             seg[j] = ((long long)cj * MT + (t - ftj)) * (long long)S_pad * kTileM;
           }
           named_bar(1, 128);
-          const int NC = S_pad / 16;
-          const bool resid_kind = (kind == kO || kind == kDown);
-          const int n_out = t * kTileM + r;
-          if (nseg <= 2) {
-            // two column chunks per batch: 2 x 2 x 16 partial loads in flight
-            for (int cc = idx; cc < NC; cc += 2 * m) {
-              const int cc2 = cc + m;
-              const bool two = cc2 < NC;
-              float a[2][2][16], olda[2][16];
-#pragma unroll
-              for (int h2 = 0; h2 < 2; ++h2) {
-                const int col = (h2 == 0 ? cc : cc2) * 16;
-                const bool live = (h2 == 0) || two;
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-#pragma unroll
-                  for (int i = 0; i < 16; ++i)
-                    a[h2][j][i] = (live && j < nseg)
-                                      ? __ldcg(p.gemm_part + seg[j] + (size_t)(col + i) * kTileM + r)
-                                      : 0.f;
-                if (resid_kind) {
-#pragma unroll
-                  for (int i = 0; i < 16; ++i)
-                    olda[h2][i] = (live && n_out < p.d && col + i < p.S)
-                                      ? __ldcg(p.resid + (size_t)(col + i) * p.d + n_out)
-                                      : 0.f;
-                }
-              }
-#pragma unroll
-              for (int h2 = 0; h2 < 2; ++h2) {
-                if (h2 == 1 && !two) break;
-                float v[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = a[h2][0][i] + (nseg > 1 ? a[h2][1][i] : 0.f);
-                epilogue_apply(p, c, kind, t, r, (h2 == 0 ? cc : cc2) * 16, v, last_layer,
-                               resid_kind ? olda[h2] : nullptr);
-              }
+          // Flat float4 items over the tile's valid columns, dealt to the m
+          // final contributors' 128 epilogue threads; two items per pass, and
+          // all segments of a pass in flight together, summed in segment order.
+          const int et = threadIdx.x - 64, step = m * 128;
+          if (kind == kGU) {
+            // item (s, r4): gate rows 4r4..4r4+3 and the up rows 64 below them
+            const int F = p.F, items = p.S * 16;
+#pragma unroll 1
+            for (int i0 = idx * 128 + et; i0 < items; i0 += 2 * step) {
+              const int i1 = i0 + step;
+              const bool two = i1 < items;
+              const size_t o0 = (size_t)(i0 >> 4) * kTileM + 4 * (i0 & 15);
+              const size_t o1 = two ? (size_t)(i1 >> 4) * kTileM + 4 * (i1 & 15) : o0;
+              float4 g0, g1, u0, u1;
+              seg_sum4(p.gemm_part, seg, nseg, o0, o1, o0 + 64, o1 + 64, g0, g1, u0, u1);
+              swiglu_store(p.u + (size_t)(i0 >> 4) * F, t * 64 + 4 * (i0 & 15), F, g0, u0);
+              if (two) swiglu_store(p.u + (size_t)(i1 >> 4) * F, t * 64 + 4 * (i1 & 15), F, g1, u1);
+            }
+          } else if (kind == kQKV) {
+            // item (s, r4): output rows 4r4..4r4+3 of the tile
+            const int N = 3 * p.HD, items = p.S * 32;
+#pragma unroll 1
+            for (int i0 = idx * 128 + et; i0 < items; i0 += 2 * step) {
+              const int i1 = i0 + step;
+              const bool two = i1 < items;
+              const int s0 = i0 >> 5, s1 = two ? (i1 >> 5) : s0;
+              const int r0 = 4 * (i0 & 31), r1 = two ? 4 * (i1 & 31) : r0;
+              float4 a0, a1;
+              seg_sum2(p.gemm_part, seg, nseg, (size_t)s0 * kTileM + r0, (size_t)s1 * kTileM + r1, a0, a1);
+              if (t * kTileM + r0 < N) *(float4*)(p.qkv + (size_t)s0 * N + t * kTileM + r0) = a0;
+              if (two && t * kTileM + r1 < N) *(float4*)(p.qkv + (size_t)s1 * N + t * kTileM + r1) = a1;
             }
           } else {
-            // one column chunk per batch: up to 4 segments x 16 partial loads (the
-            // first batch together with the residual) in flight; summed in segment order
-            for (int cc = idx; cc < NC; cc += m) {
-              const int col = cc * 16;
-              float v[16], olda[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = 0.f;
-              if (resid_kind) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                  olda[i] = (n_out < p.d && col + i < p.S) ? __ldcg(p.resid + (size_t)(col + i) * p.d + n_out) : 0.f;
-              }
-              for (int j0 = 0; j0 < nseg; j0 += 4) {
-                float tmp[4][16];
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-                  for (int i = 0; i < 16; ++i)
-                    tmp[jj][i] = (j0 + jj < nseg)
-                                     ? __ldcg(p.gemm_part + seg[j0 + jj] + (size_t)(col + i) * kTileM + r)
-                                     : 0.f;
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-                  if (j0 + jj < nseg) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] += tmp[jj][i];
-                  }
-              }
-              epilogue_apply(p, c, kind, t, r, col, v, last_layer, resid_kind ? olda : nullptr);
+            // item (s, r4): output rows 4r4..4r4+3 of the tile, residual added
+            const int d = p.d, items = p.S * 32;
+#pragma unroll 1
+            for (int i0 = idx * 128 + et; i0 < items; i0 += 2 * step) {
+              const int i1 = i0 + step;
+              const bool two = i1 < items;
+              const int s0 = i0 >> 5, s1 = two ? (i1 >> 5) : s0;
+              const int n0 = t * kTileM + 4 * (i0 & 31), n1 = two ? t * kTileM + 4 * (i1 & 31) : n0;
+              const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+              const float4 old0 = (n0 < d) ? __ldcg((const float4*)(p.resid + (size_t)s0 * d + n0)) : z;
+              const float4 old1 = (n1 < d) ? __ldcg((const float4*)(p.resid + (size_t)s1 * d + n1)) : z;
+              float4 a0, a1;
+              seg_sum2(p.gemm_part, seg, nseg, (size_t)s0 * kTileM + (n0 - t * kTileM),
+                       (size_t)s1 * kTileM + (n1 - t * kTileM), a0, a1);
+              if (n0 < d) resid_store(p, s0, n0, old0, a0, last_layer);
+              if (two && n1 < d) resid_store(p, s1, n1, old1, a1, last_layer);
             }
           }
           named_bar(1, 128);
@@ -1060,7 +1124,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   c.lay = smem_layout();
   c.bar_target = 0;
   c.bar_index = 0;
-  c.ring_it = c.acc_it = c.att_it = 0;
+  c.ring_it = c.acc_it = c.att_it = c.norm_it = 0;
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
@@ -1075,6 +1139,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     for (int w = 0; w < kWarps; ++w)
       for (int st = 0; st < kAttStages; ++st) mbar_init(bar_att(c, w, st), 1);
     mbar_init(bar_drain(c), 1);
+    mbar_init(bar_norm(c), 1);
     fence_mbar_init();
     for (int i = 0; i < 4; ++i) {
       prefetch_tmap(&p.tm_w[i]);
@@ -1097,14 +1162,14 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   for (int i = blockIdx.x * kThreads + threadIdx.x; i < 2048; i += gridDim.x * kThreads)
     p.tile_cnt[i] = 0;
   if (blockIdx.x == gridDim.x - 1) build_pieces(p, c);
-  norm_phase(p, c, p.weights + p.off_g_attn, true);
-  bool ok = grid_sync(p, c);
+  const bool n0 = norm_phase(p, c, p.weights + p.off_g_attn, true);
+  bool ok = grid_sync(p, c) && n0;
 
   for (int l = 0; ok && l < p.L; ++l) {
     const uint16_t* wl = p.weights + (size_t)l * p.layer_elems;
     if (l > 0) {
-      norm_phase(p, c, wl + p.off_g_attn, false);
-      if (!(ok = grid_sync(p, c))) break;
+      const bool nok = norm_phase(p, c, wl + p.off_g_attn, false);
+      if (!(ok = grid_sync(p, c) && nok)) break;
     }
     gemm_phase(p, c, kQKV, l, false);
     if (!(ok = grid_sync(p, c))) break;
@@ -1114,8 +1179,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     if (!(ok = grid_sync(p, c))) break;
     gemm_phase(p, c, kO, l, false);
     if (!(ok = grid_sync(p, c))) break;
-    norm_phase(p, c, wl + p.off_g_mlp, false);
-    if (!(ok = grid_sync(p, c))) break;
+    const bool nok2 = norm_phase(p, c, wl + p.off_g_mlp, false);
+    if (!(ok = grid_sync(p, c) && nok2)) break;
     gemm_phase(p, c, kGU, l, false);
     if (!(ok = grid_sync(p, c))) break;
     gemm_phase(p, c, kDown, l, l == p.L - 1);
