@@ -64,11 +64,9 @@ struct StepParams {
   long long* arrive_ts;  // profiling hook: [barrier][cta] globaltimer at barrier arrival
 };
 
-// CTAs taking part in a stream-K GEMM phase of `tiles` tiles and U units.
-// With at least half a grid of tiles (and no more than a grid), one whole
-// tile per CTA: no split-K partial sums at all.
+// CTAs taking part in a stream-K GEMM phase of `tiles` tiles and U units:
+// every participating span is non-empty and a tile has at most 64 segments.
 __host__ __device__ inline int stream_k_ctas(int grid, long long U, int tiles) {
-  if (2 * tiles >= grid && tiles <= grid) return tiles;
   long long g = grid;
   if (U < g) g = U;
   if (62LL * tiles < g) g = 62LL * tiles;
@@ -84,7 +82,7 @@ int barriers_per_step(int L);
 struct SmemLayout {
   int ring_off, ring_bytes;      // GEMM ring / attention K and V tiles (union)
   int ascale_off;                // attention K/V scales: kWarps x kAttStages x 256 B
-  int xbuf_off;                  // gate/up exchange buffer (64 x 17 fp32)
+  int xbuf_off;                  // prologue scratch (work-list positions), 4352 B
   int qscr_off;                  // per-warp query scratch (kWarps x 512 B)
   int red_off;                   // reduction scratch (256 words)
   int bar_off;                   // mbarriers
@@ -96,7 +94,7 @@ __host__ __device__ inline SmemLayout smem_layout() {
   s.ring_off = 0;
   s.ring_bytes = 200 * 1024;
   s.ascale_off = s.ring_off + s.ring_bytes;
-  s.xbuf_off = s.ascale_off + kWarps * kAttStages * 256;  // 64 x 17 fp32
+  s.xbuf_off = s.ascale_off + kWarps * kAttStages * 256;
   s.qscr_off = s.xbuf_off + 64 * 17 * 4;             // 3 KB: q as f16 hi + lo per warp
   s.red_off = s.qscr_off + kWarps * 512;             // 1 KB: one int per thread
   s.bar_off = s.red_off + 1024;                      // 64 mbarriers

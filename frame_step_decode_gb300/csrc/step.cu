@@ -224,70 +224,18 @@ __device__ void prefetch_gemm_weights(const StepParams& p, int kind, int layer) 
   }
 }
 
-__device__ __forceinline__ void epilogue_apply(const StepParams& p, Ctx& c, int kind, int t, int r,
-                                               int col0, const float* v, bool last_layer) {
-  const int S = p.S;
-  if (kind == kQKV) {
-    const int N = 3 * p.HD, n = t * kTileM + r;
-    if (n < N) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        if (col0 + i < S) p.qkv[(size_t)(col0 + i) * N + n] = v[i];
-    }
-  } else if (kind == kO || kind == kDown) {
-    const int d = p.d, n = t * kTileM + r;
-    if (n < d) {
-      // all loads first, then all stores: keeps the 16 L2 round trips in flight
-      float old[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        old[i] = (col0 + i < S) ? __ldcg(p.resid + (size_t)(col0 + i) * d + n) : 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int s = col0 + i;
-        if (s < S) {
-          const float nr = old[i] + v[i];
-          p.resid[(size_t)s * d + n] = nr;
-          if (last_layer) p.y[(size_t)s * d + n] = f32_to_bf16(nr);
-        }
-      }
-    }
-  } else {  // kGU: rows 0..63 gate, 64..127 up of the same 64 features
-    float* xb = (float*)(c.smem + c.lay.xbuf_off);
-    if (r >= 64) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) xb[(r - 64) * 17 + i] = v[i];
-    }
-    named_bar(2, 128);
-    if (r < 64) {
-      const int F = p.F, n = t * 64 + r;
-      if (n < F) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int s = col0 + i;
-          if (s < S) {
-            float gt = v[i], up = xb[r * 17 + i];
-            float sl = gt / (1.0f + expf(-gt));
-            p.u[(size_t)s * F + n] = f32_to_bf16(sl * up);
-          }
-        }
-      }
-    }
-    named_bar(2, 128);
-  }
-}
-
 __device__ __forceinline__ float4 ld4cg(const float* q) { return __ldcg((const float4*)q); }
 __device__ __forceinline__ void add4(float4& a, const float4& b) {
   a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
 }
 // Sum, in segment order, of the float4 at element offsets o0 / o1 of each of
-// a split tile's partial slots (offsets seg[0..nseg)); the first three
+// a tile's partial slots (the first at `first`, the others at part +
+// seg[1..nseg)); the first three
 // segments' loads in flight together, two more per later pass.
-__device__ __forceinline__ void seg_sum2(const float* part, const long long* seg, int nseg,
-                                         size_t o0, size_t o1, float4& a0, float4& a1) {
-  a0 = ld4cg(part + seg[0] + o0);
-  a1 = ld4cg(part + seg[0] + o1);
+__device__ __forceinline__ void seg_sum2(const float* first, const float* part, const long long* seg,
+                                         int nseg, size_t o0, size_t o1, float4& a0, float4& a1) {
+  a0 = ld4cg(first + o0);
+  a1 = ld4cg(first + o1);
   for (int j = 1; j < nseg; j += 2) {
     float4 t0[2], t1[2];
 #pragma unroll
@@ -306,10 +254,10 @@ __device__ __forceinline__ void seg_sum2(const float* part, const long long* seg
 }
 // The same for four offsets (gate and up rows of two items), one segment per
 // later pass.
-__device__ __forceinline__ void seg_sum4(const float* part, const long long* seg, int nseg,
-                                         size_t o0, size_t o1, size_t o2, size_t o3,
+__device__ __forceinline__ void seg_sum4(const float* first, const float* part, const long long* seg,
+                                         int nseg, size_t o0, size_t o1, size_t o2, size_t o3,
                                          float4& a0, float4& a1, float4& a2, float4& a3) {
-  const float* b = part + seg[0];
+  const float* b = first;
   a0 = ld4cg(b + o0); a1 = ld4cg(b + o1); a2 = ld4cg(b + o2); a3 = ld4cg(b + o3);
   for (int j = 1; j < nseg; ++j) {
     const float* bk = part + seg[j];
@@ -339,6 +287,68 @@ __device__ __forceinline__ void resid_store(const StepParams& p, int s, int n, f
   }
 }
 
+// Finish tile t of GEMM `kind` from its partial sums: the first segment's
+// slot at `first`, the others at part + seg[1..nseg), summed in segment order.
+// Flat float4 items over the valid columns; this thread takes items et,
+// et + step, ...
+__device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t, const float* first,
+                                         const long long* seg, int nseg, int et, int step,
+                                         bool last_layer) {
+  if (kind == kGU) {
+    // item (s, r4): gate rows 4r4..4r4+3 and the up rows 64 below them
+    const int F = p.F, items = p.S * 16;
+#pragma unroll 1
+    for (int i0 = et; i0 < items; i0 += 2 * step) {
+      const int i1 = i0 + step;
+      const bool two = i1 < items;
+      const size_t o0 = (size_t)(i0 >> 4) * kTileM + 4 * (i0 & 15);
+      const size_t o1 = two ? (size_t)(i1 >> 4) * kTileM + 4 * (i1 & 15) : o0;
+      float4 g0, g1, u0, u1;
+      seg_sum4(first, p.gemm_part, seg, nseg, o0, o1, o0 + 64, o1 + 64, g0, g1, u0, u1);
+      swiglu_store(p.u + (size_t)(i0 >> 4) * F, t * 64 + 4 * (i0 & 15), F, g0, u0);
+      if (two) swiglu_store(p.u + (size_t)(i1 >> 4) * F, t * 64 + 4 * (i1 & 15), F, g1, u1);
+    }
+  } else if (kind == kQKV) {
+    // item (s, r4): output rows 4r4..4r4+3 of the tile; four items per pass
+    const int N = 3 * p.HD, items = p.S * 32;
+#pragma unroll 1
+    for (int i0 = et; i0 < items; i0 += 4 * step) {
+      int iv[4];
+      size_t ov[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        iv[k] = (i0 + k * step < items) ? i0 + k * step : i0;
+        ov[k] = (size_t)(iv[k] >> 5) * kTileM + 4 * (iv[k] & 31);
+      }
+      float4 a[4];
+      seg_sum4(first, p.gemm_part, seg, nseg, ov[0], ov[1], ov[2], ov[3], a[0], a[1], a[2], a[3]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int n = t * kTileM + 4 * (iv[k] & 31);
+        if ((k == 0 || iv[k] != i0) && n < N) *(float4*)(p.qkv + (size_t)(iv[k] >> 5) * N + n) = a[k];
+      }
+    }
+  } else {
+    // item (s, r4): output rows 4r4..4r4+3 of the tile, residual added
+    const int d = p.d, items = p.S * 32;
+#pragma unroll 1
+    for (int i0 = et; i0 < items; i0 += 2 * step) {
+      const int i1 = i0 + step;
+      const bool two = i1 < items;
+      const int s0 = i0 >> 5, s1 = two ? (i1 >> 5) : s0;
+      const int n0 = t * kTileM + 4 * (i0 & 31), n1 = two ? t * kTileM + 4 * (i1 & 31) : n0;
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 old0 = (n0 < d) ? __ldcg((const float4*)(p.resid + (size_t)s0 * d + n0)) : z;
+      const float4 old1 = (n1 < d) ? __ldcg((const float4*)(p.resid + (size_t)s1 * d + n1)) : z;
+      float4 a0, a1;
+      seg_sum2(first, p.gemm_part, seg, nseg, (size_t)s0 * kTileM + (n0 - t * kTileM),
+               (size_t)s1 * kTileM + (n1 - t * kTileM), a0, a1);
+      if (n0 < d) resid_store(p, s0, n0, old0, a0, last_layer);
+      if (two && n1 < d) resid_store(p, s1, n1, old1, a1, last_layer);
+    }
+  }
+}
+
 __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, bool last_layer) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KB = p.kblocks[kind];
@@ -358,14 +368,16 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
       const uint64_t pol = policy_evict_first();
       const CUtensorMap* wm = &p.tm_w[kind];
       const CUtensorMap* xm = &p.tm_x[kind];
-      for (long long u = sp.u0; u < sp.u1;) {
+      bool fail = false;
+      for (long long u = sp.u0; !fail && u < sp.u1;) {
         const int t = (int)(u / KB);
         const long long e = min(sp.u1, (long long)(t + 1) * KB);
         for (int kb = (int)(u - (long long)t * KB); kb < (int)(e - (long long)t * KB); ++kb) {
           const uint32_t slot = c.ring_it % nst, ph = (c.ring_it / nst) & 1u;
           if (!mbar_wait(bar_empty(c, slot), ph ^ 1u, p.timeout_ns, p.err)) {
             set_err(p, kErrTimeout);
-            return;
+            fail = true;
+            break;
           }
           const uint32_t fb = bar_full(c, slot);
           mbar_arrive_expect_tx(fb, 16384u + b_bytes);
@@ -386,13 +398,14 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kTileM, S_pad);
-      for (long long u = sp.u0; u < sp.u1;) {
+      bool fail = false;
+      for (long long u = sp.u0; !fail && u < sp.u1;) {
         const int t = (int)(u / KB);
         const long long e = min(sp.u1, (long long)(t + 1) * KB);
         const uint32_t b = c.acc_it & 1u;
         if (!mbar_wait(bar_acce(c, b), ((c.acc_it >> 1) & 1u) ^ 1u, p.timeout_ns, p.err)) {
           set_err(p, kErrTimeout);
-          return;
+          break;
         }
         tc_fence_after();
         const uint32_t dt = c.tmem + b * 128u;
@@ -401,7 +414,8 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
           const uint32_t slot = c.ring_it % nst, ph = (c.ring_it / nst) & 1u;
           if (!mbar_wait(bar_full(c, slot), ph, p.timeout_ns, p.err)) {
             set_err(p, kErrTimeout);
-            return;
+            fail = true;
+            break;
           }
           tc_fence_after();
           const uint32_t a = ring + slot * stride, bs = a + 16384u;
@@ -412,6 +426,7 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
           tc_commit(bar_empty(c, slot));
           c.ring_it++;
         }
+        if (fail) break;
         tc_commit(bar_accf(c, b));
         c.acc_it++;
         u = e;
@@ -428,8 +443,7 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
       const int t = (int)(u / KB);
       const long long tb = (long long)t * KB, te = tb + KB;
       const long long e = min(sp.u1, te);
-      const int c_first = owner_of(U, G, tb), c_last = owner_of(U, G, te - 1);
-      const int nseg = c_last - c_first + 1;
+      const int nseg = owner_of(U, G, te - 1) - owner_of(U, G, tb) + 1;
       const uint32_t b = c.acc_it & 1u;
       // one thread waits, the four warps take the same decision
       volatile int* wflag = misc_word(c, 4 + (int)b);
@@ -438,131 +452,81 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
       named_bar(1, 128);
       if (!*wflag) {
         if (threadIdx.x == 64) set_err(p, kErrTimeout);
-        return;
+        break;
       }
       tc_fence_after();
       const uint32_t tb_addr = c.tmem + ((uint32_t)(q * 32) << 16) + b * 128u;
-      if (nseg == 1) {
-        for (int col = 0; col < S_pad; col += 16) {
-          float v[16];
-          tmem_ld16(tb_addr + col, v);
-          epilogue_apply(p, c, kind, t, r, col, v, last_layer);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_acce(c, b));
-      } else {
-        // Split tile: store this segment's partial.  The CTAs whose spans end
-        // inside the tile then wait (bounded) until every segment has arrived
-        // and each sums, in segment order, its share of the tile's 16-column
-        // chunks; the other contributors move on.
-        float* slot = p.gemm_part + ((size_t)cta * MT + (t - first_tile)) * (size_t)S_pad * kTileM;
-        for (int col = 0; col < S_pad; col += 16) {
-          float v[16];
-          tmem_ld16(tb_addr + col, v);
+      // Store this segment's sums as a partial slot ([column][128 rows] fp32).
+      float* slot = p.gemm_part + ((size_t)cta * MT + (t - first_tile)) * (size_t)S_pad * kTileM;
+      for (int col = 0; col < S_pad; col += 16) {
+        float v[16];
+        tmem_ld16(tb_addr + col, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) slot[(size_t)(col + i) * kTileM + r] = v[i];
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_acce(c, b));
+        for (int i = 0; i < 16; ++i) slot[(size_t)(col + i) * kTileM + r] = v[i];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_acce(c, b));
+      if (nseg == 1) {
+        // whole tile here: the four epilogue warps finish it from the slot
+        named_bar(1, 128);
+        finish_tile(p, kind, t, slot, nullptr, 1, threadIdx.x - 64, 128, last_layer);
+      } else {
+        // split tile: count this segment in
         __threadfence();
         named_bar(1, 128);
-        const bool final_seg = (sp.u1 <= te);
-        if (threadIdx.x == 64) {
-          atomicAdd(p.tile_cnt + t, 1);
-          int ok = 1;
-          if (final_seg) {
-            long long t0 = globaltimer();
-            for (uint32_t it = 0;; ++it) {
-              if ((int)ld_acquire((const unsigned*)(p.tile_cnt + t)) >= nseg) break;
-              if ((it & 15) == 15) {
-                if (*(volatile int*)p.err & kErrTimeout) { ok = 0; break; }
-                if (globaltimer() - t0 > p.timeout_ns) {
-                  set_err(p, kErrTimeout);
-                  ok = 0;
-                  break;
-                }
-              }
-            }
-          }
-          *misc_word(c, 3) = ok;
-        }
-        named_bar(1, 128);
-        if (!*misc_word(c, 3)) return;
-        if (final_seg) {
-          const int m = (c_last - c_first) + (cta_span(U, G, c_last).u1 == te ? 1 : 0);
-          const int idx = cta - c_first;
-          // offsets of the tile's partial slots, in segment order (shared scratch)
-          long long* seg = (long long*)(c.smem + c.lay.red_off);
-          for (int j = threadIdx.x - 64; j < nseg; j += 128) {
-            const int cj = c_first + j;
-            const int ftj = (int)(cta_span(U, G, cj).u0 / KB);
-            seg[j] = ((long long)cj * MT + (t - ftj)) * (long long)S_pad * kTileM;
-          }
-          named_bar(1, 128);
-          // Flat float4 items over the tile's valid columns, dealt to the m
-          // final contributors' 128 epilogue threads; two items per pass, and
-          // all segments of a pass in flight together, summed in segment order.
-          const int et = threadIdx.x - 64, step = m * 128;
-          if (kind == kGU) {
-            // item (s, r4): gate rows 4r4..4r4+3 and the up rows 64 below them
-            const int F = p.F, items = p.S * 16;
-#pragma unroll 1
-            for (int i0 = idx * 128 + et; i0 < items; i0 += 2 * step) {
-              const int i1 = i0 + step;
-              const bool two = i1 < items;
-              const size_t o0 = (size_t)(i0 >> 4) * kTileM + 4 * (i0 & 15);
-              const size_t o1 = two ? (size_t)(i1 >> 4) * kTileM + 4 * (i1 & 15) : o0;
-              float4 g0, g1, u0, u1;
-              seg_sum4(p.gemm_part, seg, nseg, o0, o1, o0 + 64, o1 + 64, g0, g1, u0, u1);
-              swiglu_store(p.u + (size_t)(i0 >> 4) * F, t * 64 + 4 * (i0 & 15), F, g0, u0);
-              if (two) swiglu_store(p.u + (size_t)(i1 >> 4) * F, t * 64 + 4 * (i1 & 15), F, g1, u1);
-            }
-          } else if (kind == kQKV) {
-            // item (s, r4): output rows 4r4..4r4+3 of the tile
-            const int N = 3 * p.HD, items = p.S * 32;
-#pragma unroll 1
-            for (int i0 = idx * 128 + et; i0 < items; i0 += 2 * step) {
-              const int i1 = i0 + step;
-              const bool two = i1 < items;
-              const int s0 = i0 >> 5, s1 = two ? (i1 >> 5) : s0;
-              const int r0 = 4 * (i0 & 31), r1 = two ? 4 * (i1 & 31) : r0;
-              float4 a0, a1;
-              seg_sum2(p.gemm_part, seg, nseg, (size_t)s0 * kTileM + r0, (size_t)s1 * kTileM + r1, a0, a1);
-              if (t * kTileM + r0 < N) *(float4*)(p.qkv + (size_t)s0 * N + t * kTileM + r0) = a0;
-              if (two && t * kTileM + r1 < N) *(float4*)(p.qkv + (size_t)s1 * N + t * kTileM + r1) = a1;
-            }
-          } else {
-            // item (s, r4): output rows 4r4..4r4+3 of the tile, residual added
-            const int d = p.d, items = p.S * 32;
-#pragma unroll 1
-            for (int i0 = idx * 128 + et; i0 < items; i0 += 2 * step) {
-              const int i1 = i0 + step;
-              const bool two = i1 < items;
-              const int s0 = i0 >> 5, s1 = two ? (i1 >> 5) : s0;
-              const int n0 = t * kTileM + 4 * (i0 & 31), n1 = two ? t * kTileM + 4 * (i1 & 31) : n0;
-              const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-              const float4 old0 = (n0 < d) ? __ldcg((const float4*)(p.resid + (size_t)s0 * d + n0)) : z;
-              const float4 old1 = (n1 < d) ? __ldcg((const float4*)(p.resid + (size_t)s1 * d + n1)) : z;
-              float4 a0, a1;
-              seg_sum2(p.gemm_part, seg, nseg, (size_t)s0 * kTileM + (n0 - t * kTileM),
-                       (size_t)s1 * kTileM + (n1 - t * kTileM), a0, a1);
-              if (n0 < d) resid_store(p, s0, n0, old0, a0, last_layer);
-              if (two && n1 < d) resid_store(p, s1, n1, old1, a1, last_layer);
-            }
-          }
-          named_bar(1, 128);
-          // the last final contributor to finish re-arms the tile's counters
-          if (threadIdx.x == 64 && atomicAdd(p.tile_cnt + 1024 + t, 1) == m - 1) {
-            p.tile_cnt[t] = 0;
-            p.tile_cnt[1024 + t] = 0;
-          }
-        }
+        if (threadIdx.x == 64) atomicAdd(p.tile_cnt + t, 1);
       }
       c.acc_it++;
       u = e;
     }
+  }
+
+  // Each CTA finishes the tile its span ends in, when that tile is split: once
+  // every segment has arrived (bounded wait), the CTAs whose spans end inside
+  // the tile (m of them) sum its partials in segment order, all threads taking
+  // a share of the flat float4 items.
+  __syncthreads();
+  if (cta >= G) return;
+  const int t = (int)((sp.u1 - 1) / KB);
+  const long long tb = (long long)t * KB, te = tb + KB;
+  const int c_first = owner_of(U, G, tb), c_last = owner_of(U, G, te - 1);
+  const int nseg = c_last - c_first + 1;
+  if (nseg == 1) return;
+  const int m = (c_last - c_first) + (cta_span(U, G, c_last).u1 == te ? 1 : 0);
+  const int idx = cta - c_first;
+  const int MT = p.max_tiles_per_cta;
+  long long* seg = (long long*)(c.smem + c.lay.red_off);  // partial-slot offsets, segment order
+  for (int j = threadIdx.x; j < nseg; j += kThreads) {
+    const int cj = c_first + j;
+    const int ftj = (int)(cta_span(U, G, cj).u0 / KB);
+    seg[j] = ((long long)cj * MT + (t - ftj)) * (long long)S_pad * kTileM;
+  }
+  if (threadIdx.x == 0) {
+    int ok = (*(volatile int*)p.err & kErrTimeout) ? 0 : 1;
+    const long long t0 = globaltimer();
+    for (uint32_t it = 0; ok; ++it) {
+      if ((int)ld_acquire((const unsigned*)(p.tile_cnt + t)) >= nseg) break;
+      if ((it & 15) == 15) {
+        if (*(volatile int*)p.err & kErrTimeout) { ok = 0; break; }
+        if (globaltimer() - t0 > p.timeout_ns) {
+          set_err(p, kErrTimeout);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    *misc_word(c, 3) = ok;
+  }
+  __syncthreads();
+  if (!*misc_word(c, 3)) return;
+  finish_tile(p, kind, t, p.gemm_part + seg[0], seg, nseg, idx * kThreads + threadIdx.x, m * kThreads,
+              last_layer);
+  __syncthreads();
+  // the last final contributor to finish re-arms the tile's counters
+  if (threadIdx.x == 0 && atomicAdd(p.tile_cnt + 1024 + t, 1) == m - 1) {
+    p.tile_cnt[t] = 0;
+    p.tile_cnt[1024 + t] = 0;
   }
 }
 
