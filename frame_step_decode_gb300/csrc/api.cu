@@ -202,7 +202,7 @@ extern "C" int wave_create(const wave_config* cfg, int S_max, int T_max, wave_t*
       {(void**)&h->attn, (size_t)(SP * HD * 2)},
       {(void**)&h->u, (size_t)(SP * F * 2)},
       {(void**)&h->gemm_part, (size_t)h->grid * mt * SP * kTileM * 4},
-      {(void**)&h->tile_cnt, 2048 * 4},
+      {(void**)&h->tile_cnt, kCounterWords * 4},
       {(void**)&h->att_part, (size_t)(max_pieces * (D + 4) * 4)},
       {(void**)&h->sh_info, (size_t)(S_max * H * 8)},
       {(void**)&h->pieces, (size_t)(max_pieces * 32)},
@@ -410,6 +410,7 @@ extern "C" int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8,
   p.u = h->u;
   p.gemm_part = h->gemm_part;
   p.tile_cnt = h->tile_cnt;
+  p.att_ctr = h->tile_cnt + 2048;
   p.att_part = h->att_part;
   p.sh_info = h->sh_info;
   p.pieces = h->pieces;

@@ -50,6 +50,7 @@ struct StepParams {
   uint16_t* u;           // [S_pad_max][F] bf16 SwiGLU output
   float* gemm_part;      // [G][max_tiles_per_cta][S_pad][128] split-K partials
   int* tile_cnt;         // [2][1024] per tile: segments arrived, final reducers done
+  int* att_ctr;          // [L] attention work counters (tile_cnt + 2048)
   float* att_part;       // [max pieces][D + 4] (acc, m, l) per attention piece
   int2* sh_info;         // [S_max*H] (first partial slot, pieces) per (session, head)
   int4* pieces;          // [2 * max pieces] (sh, c_lo | c_hi << 16, pieces of sh, first slot), (pos, 0, 0, 0)
@@ -66,6 +67,10 @@ struct StepParams {
 
 // CTAs taking part in a stream-K GEMM phase of `tiles` tiles and U units:
 // every participating span is non-empty and a tile has at most 64 segments.
+// Counter words of the workspace: two per GEMM tile (1024 tiles at most),
+// then one attention work counter per layer (1024 layers at most).
+constexpr int kCounterWords = 2048 + 1024;
+
 __host__ __device__ inline int stream_k_ctas(int grid, long long U, int tiles) {
   long long g = grid;
   if (U < g) g = U;

@@ -173,7 +173,7 @@ extern "C" int wave_step_static(const wave_config* cfg, int S_max, int T_max, in
   const size_t sizes[14] = {(size_t)(SP * d * 4),        (size_t)(SP * d * 2),
                             (size_t)(SP * 3 * HD * 4),   (size_t)(SP * HD * 2),
                             (size_t)(SP * F * 2),        (size_t)sms * mt * SP * kTileM * 4,
-                            2048 * 4,                    (size_t)(max_pieces * (D + 4) * 4),
+                            kCounterWords * 4,           (size_t)(max_pieces * (D + 4) * 4),
                             (size_t)(S_max * H * 8),     (size_t)(max_pieces * 32),
                             16,                          (size_t)T_max * (D / 2) * 8,
                             16,                          16};
@@ -193,6 +193,7 @@ extern "C" int wave_step_static(const wave_config* cfg, int S_max, int T_max, in
   p.u = (uint16_t*)(base + offs[4]);
   p.gemm_part = (float*)(base + offs[5]);
   p.tile_cnt = (int*)(base + offs[6]);
+  p.att_ctr = p.tile_cnt + 2048;
   p.att_part = (float*)(base + offs[7]);
   p.sh_info = (int2*)(base + offs[8]);
   p.pieces = (int4*)(base + offs[9]);

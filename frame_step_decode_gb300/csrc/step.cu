@@ -566,11 +566,13 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
   if (warp == kWarps - 1 && lane == 0) prefetch_gemm_weights(p, kO, layer);
   __syncwarp();
 
-  // snake order over the longest-first list: warp gw takes list entries
-  // r*NW + gw for even r and r*NW + NW-1-gw for odd r
-  for (int r = 0;; ++r) {
-    const int pi = r * NW + ((r & 1) ? NW - 1 - gw : gw);
-    if (pi >= n_pieces) break;
+  // Dynamic assignment over the longest-first list: warp gw starts with entry
+  // gw, then takes the next unclaimed entry from the layer's counter, claimed
+  // one piece ahead so that the atomic's latency hides behind the current one.
+  int* ctr = p.att_ctr + layer;
+  for (int pi = gw; pi < n_pieces;) {
+    int nxt = 0;
+    if (lane == 0) nxt = NW + atomicAdd(ctr, 1);
     const int4 pc = __ldcg(p.pieces + 2 * pi);
     const int P = __ldcg(p.pieces + 2 * pi + 1).x;
     const int sh = pc.x, c_lo = pc.y & 0xFFFF, c_hi = pc.y >> 16, np = pc.z, first = pc.w;
@@ -901,6 +903,7 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
         }
       }
     }
+    pi = __shfl_sync(0xffffffffu, nxt, 0);
   }
 }
 
@@ -966,8 +969,8 @@ __device__ void merge_phase(const StepParams& p, Ctx& c) {
 // One CTA turns positions into the attention work list: each (session, head)
 // history of pos+1 slots is cut into pieces of up to kPieceChunks chunks.
 // The list is ordered by piece length, longest first (a counting sort over
-// the kPieceChunks possible lengths), and the attention phase deals it out
-// to warps in snake order, which balances the warps' loads.  A piece's slot
+// the kPieceChunks possible lengths); the attention phase's warps claim its
+// entries in that order, which balances their loads.  A piece's slot
 // for its partial result is first + c_lo / kPieceChunks, first being the
 // first slot of its (session, head).
 static_assert(kThreads <= 256, "the reduction scratch holds one word per thread");
@@ -1072,6 +1075,7 @@ __device__ void build_pieces(const StepParams& p, Ctx& c) {
   for (int s = 0; s < p.S; ++s)
     if (spos[s] < 0)
       for (int i = tid; i < p.HD; i += kThreads) p.attn[(size_t)s * p.HD + i] = 0;
+  fence_proxy_async_smem();  // the ring area is refilled by copies later
   __syncthreads();
 }
 
@@ -1123,7 +1127,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 
   if (p.phase_ts && blockIdx.x == 0 && threadIdx.x == 0) p.phase_ts[0] = globaltimer();
   // phase 0: work list, counter reset, residual and first norm
-  for (int i = blockIdx.x * kThreads + threadIdx.x; i < 2048; i += gridDim.x * kThreads)
+  for (int i = blockIdx.x * kThreads + threadIdx.x; i < kCounterWords; i += gridDim.x * kThreads)
     p.tile_cnt[i] = 0;
   if (blockIdx.x == gridDim.x - 1) build_pieces(p, c);
   const bool n0 = norm_phase(p, c, p.weights + p.off_g_attn, true);
