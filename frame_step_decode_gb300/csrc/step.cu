@@ -910,58 +910,67 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
 // --------------------------------------------------------------- merge
 // Combine the split-T partials of every (session, head) cut into several
 // pieces, in piece order: M = max m_i, L = sum l_i 2^(m_i - M),
-// o = sum acc_i 2^(m_i - M) / L, written as bf16; one warp per (session,
-// head), lane i owning dims [i*D/32, (i+1)*D/32).
-constexpr int kMergeMax = 4;
+// o = sum acc_i 2^(m_i - M) / L, written as bf16.  One warp per (session,
+// head), lane i owning dims [i*D/32, (i+1)*D/32); the warp's work-list
+// entries are read up front (lane k: its k-th entry) and up to kMergeMax
+// pieces' loads are in flight at once.
+constexpr int kMergeMax = 8;
 template <int D>
 __device__ void merge_phase(const StepParams& p, Ctx& c) {
   constexpr int DPL = D / 32;
   const int lane = threadIdx.x & 31;
   const int NW = gridDim.x * kWarps;
+  const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int N = p.S * p.H;
-  for (int sh = blockIdx.x * kWarps + (threadIdx.x >> 5); sh < N; sh += NW) {
-    const int2 info = __ldcg(p.sh_info + sh);
-    const int first = info.x, np = info.y;
-    if (np <= 1) continue;
-    float M = -INFINITY;
-    for (int i0 = 0; i0 < np; i0 += kMergeMax) {
-      float mv[kMergeMax];
+  for (int base = gw; base < N; base += 32 * NW) {
+    const int mine = base + lane * NW;
+    const int2 info_l = (mine < N) ? __ldcg(p.sh_info + mine) : make_int2(0, 0);
+    const int cnt = min(32, (N - base + NW - 1) / NW);
+    for (int k = 0; k < cnt; ++k) {
+      const int sh = base + k * NW;
+      const int first = __shfl_sync(0xffffffffu, info_l.x, k);
+      const int np = __shfl_sync(0xffffffffu, info_l.y, k);
+      if (np <= 1) continue;
+      float M = -INFINITY, Ls = 0.f, o[DPL];
 #pragma unroll
-      for (int i = 0; i < kMergeMax; ++i)
-        mv[i] = (i0 + i < np) ? __ldcg(p.att_part + (size_t)(first + i0 + i) * (D + 4) + D) : -INFINITY;
+      for (int e = 0; e < DPL; ++e) o[e] = 0.f;
+      if (np > kMergeMax) {
+        for (int i = 0; i < np; ++i) M = fmaxf(M, __ldcg(p.att_part + (size_t)(first + i) * (D + 4) + D));
+      }
+      for (int i0 = 0; i0 < np; i0 += kMergeMax) {
+        float mv[kMergeMax], lv[kMergeMax], ov[kMergeMax][DPL];
 #pragma unroll
-      for (int i = 0; i < kMergeMax; ++i) M = fmaxf(M, mv[i]);
-    }
-    float Ls = 0.f, o[DPL];
+        for (int i = 0; i < kMergeMax; ++i) {
+          if (i0 + i < np) {
+            const float* pp = p.att_part + (size_t)(first + i0 + i) * (D + 4);
+            const float2 ml = __ldcg((const float2*)(pp + D));
+            mv[i] = ml.x;
+            lv[i] = ml.y;
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) o[e] = 0.f;
-    for (int i0 = 0; i0 < np; i0 += kMergeMax) {
-      float mv[kMergeMax], lv[kMergeMax], ov[kMergeMax][DPL];
+            for (int e = 0; e < DPL; ++e) ov[i][e] = __ldcg(pp + lane * DPL + e);
+          }
+        }
+        if (np <= kMergeMax) {
 #pragma unroll
-      for (int i = 0; i < kMergeMax; ++i) {
-        if (i0 + i < np) {
-          const float* pp = p.att_part + (size_t)(first + i0 + i) * (D + 4);
-          mv[i] = __ldcg(pp + D);
-          lv[i] = __ldcg(pp + D + 1);
+          for (int i = 0; i < kMergeMax; ++i)
+            if (i < np) M = fmaxf(M, mv[i]);
+        }
 #pragma unroll
-          for (int e = 0; e < DPL; ++e) ov[i][e] = __ldcg(pp + lane * DPL + e);
+        for (int i = 0; i < kMergeMax; ++i) {
+          if (i0 + i < np) {
+            const float wgt = ex2(mv[i] - M);
+            Ls += lv[i] * wgt;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o[e] += ov[i][e] * wgt;
+          }
         }
       }
+      const float inv = 1.0f / Ls;
+      const int s = sh / p.H, h = sh - s * p.H;
+      uint16_t* od = p.attn + (size_t)s * p.HD + h * D + lane * DPL;
 #pragma unroll
-      for (int i = 0; i < kMergeMax; ++i) {
-        if (i0 + i < np) {
-          const float wgt = ex2(mv[i] - M);
-          Ls += lv[i] * wgt;
-#pragma unroll
-          for (int e = 0; e < DPL; ++e) o[e] += ov[i][e] * wgt;
-        }
-      }
+      for (int e = 0; e < DPL; ++e) od[e] = f32_to_bf16(o[e] * inv);
     }
-    const float inv = 1.0f / Ls;
-    const int s = sh / p.H, h = sh - s * p.H;
-    uint16_t* od = p.attn + (size_t)s * p.HD + h * D + lane * DPL;
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) od[e] = f32_to_bf16(o[e] * inv);
   }
 }
 
