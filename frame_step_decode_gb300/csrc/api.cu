@@ -111,7 +111,7 @@ extern "C" const char* wave_strerror(int code) {
     case WAVE_ECUDA: return "CUDA call failed";
     case WAVE_ELAUNCH: return "persistent grid could not be launched co-resident";
     case WAVE_ETIMEOUT: return "a device-side wait timed out";
-    case WAVE_EPOS: return "a session position was outside [0, T_max)";
+    case WAVE_EPOS: return "a session position was at or beyond T_max";
     case WAVE_EDEVICE: return "device is not sm_103";
     case WAVE_ENOMEM: return "device allocation failed";
     default: return "unknown error";

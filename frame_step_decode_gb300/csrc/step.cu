@@ -274,15 +274,20 @@ __device__ __forceinline__ void swiglu_store(uint16_t* urow, int n, int F, const
   o.y = (uint32_t)f32_to_bf16(silu_mul(g.z, u.z)) | ((uint32_t)f32_to_bf16(silu_mul(g.w, u.w)) << 16);
   *(uint2*)(urow + n) = o;
 }
-// resid[s][n..n+3] = old + v (and y = bf16 of it after the last layer).
+// resid[s][n..n+3] = old + v (and y = bf16 of it after the last layer; an
+// empty slot, negative position, passes x through unchanged).
 __device__ __forceinline__ void resid_store(const StepParams& p, int s, int n, float4 old, const float4& v,
                                             bool last_layer) {
   add4(old, v);
   *(float4*)(p.resid + (size_t)s * p.d + n) = old;
   if (last_layer) {
     uint2 o;
-    o.x = (uint32_t)f32_to_bf16(old.x) | ((uint32_t)f32_to_bf16(old.y) << 16);
-    o.y = (uint32_t)f32_to_bf16(old.z) | ((uint32_t)f32_to_bf16(old.w) << 16);
+    if (p.pos[s] < 0) {
+      o = *(const uint2*)(p.x + (size_t)s * p.d + n);
+    } else {
+      o.x = (uint32_t)f32_to_bf16(old.x) | ((uint32_t)f32_to_bf16(old.y) << 16);
+      o.y = (uint32_t)f32_to_bf16(old.z) | ((uint32_t)f32_to_bf16(old.w) << 16);
+    }
     *(uint2*)(p.y + (size_t)s * p.d + n) = o;
   }
 }
@@ -993,9 +998,9 @@ __device__ void build_pieces(const StepParams& p, Ctx& c) {
   const int N = p.S * p.H, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int s = tid; s < p.S; s += kThreads) {
     const int P = p.pos[s];
-    const bool ok = (P >= 0 && P < p.T_max);
-    spos[s] = ok ? P : -1;
-    if (!ok) set_err(p, kErrPos);
+    // a negative position is an empty slot; one at or beyond T_max an error
+    spos[s] = (P >= 0 && P < p.T_max) ? P : -1;
+    if (P >= p.T_max) set_err(p, kErrPos);
   }
   __syncthreads();
   const int b0 = (int)((long long)N * tid / kThreads), b1 = (int)((long long)N * (tid + 1) / kThreads);
@@ -1080,7 +1085,7 @@ __device__ void build_pieces(const StepParams& p, Ctx& c) {
     }
     first += np;
   }
-  // sessions with an invalid position get a zero attention output
+  // empty slots and sessions with an invalid position get a zero attention output
   for (int s = 0; s < p.S; ++s)
     if (spos[s] < 0)
       for (int i = tid; i < p.HD; i += kThreads) p.attn[(size_t)s * p.HD + i] = 0;

@@ -41,7 +41,7 @@ extern "C" {
 #define WAVE_ECUDA (-2)    /* a CUDA runtime/driver call failed */
 #define WAVE_ELAUNCH (-3)  /* the persistent grid could not be made co-resident */
 #define WAVE_ETIMEOUT (-4) /* a device-side wait (grid barrier, async copy) gave up */
-#define WAVE_EPOS (-5)     /* a session's position was outside [0, T_max) */
+#define WAVE_EPOS (-5)     /* a session's position was at or beyond T_max */
 #define WAVE_EDEVICE (-6)  /* the current device is not an sm_103 GPU */
 #define WAVE_ENOMEM (-7)   /* device allocation failed */
 
@@ -99,7 +99,10 @@ size_t wave_weight_offset(const wave_config* cfg, int layer, int which);
  *              (layer, K|V, session, head, token) with value = code * scale.
  *   positions  int32 [S]: pos[s] is the RoPE position of this frame and the
  *              cache slot it writes; attention spans slots 0..pos[s] inclusive.
- *              Input only: the caller advances positions between frames.
+ *              A negative pos[s] marks an empty slot of the fixed-shape batch
+ *              (no session there this frame): its cache is not touched and
+ *              y[s] = x[s] bit for bit.  Input only: the caller advances
+ *              positions between frames.
  *   x          bf16 [S][d] input activations; y bf16 [S][d] output (may alias x);
  *              both 16-byte aligned.
  *
@@ -111,7 +114,7 @@ size_t wave_weight_offset(const wave_config* cfg, int layer, int which);
  * v/scale (fp32 division), all-zero codes and scale 0 for a zero row; softmax
  * scale 1/sqrt(D); SwiGLU silu(gate) * up; no biases, no final norm.
  *
- * A session whose pos is outside [0, T_max) gets no cache write and a zero
+ * A session whose pos is at or beyond T_max gets no cache write and a zero
  * attention output; the step records WAVE_EPOS for wave_status.
  * Returns WAVE_EINVAL for bad arguments (checked on the host before any
  * launch), WAVE_ELAUNCH/WAVE_ECUDA if the launch fails.

@@ -144,7 +144,8 @@ def step(w, weights: np.ndarray, kv: np.ndarray, kv_scales: np.ndarray, pos: np.
     """Run one frame for the sessions held in kv/kv_scales/pos/x (all n of them).
 
     kv [L][2][n][H][T_max][D] uint8 and kv_scales [L][2][n][H][T_max] float32
-    are updated in place at slot pos[s].  Returns (y bf16 bits [n][d],
+    are updated in place at slot pos[s].  A negative pos[s] is an empty slot:
+    y[s] = x[s] and its cache is left alone.  Returns (y bf16 bits [n][d],
     y_exact fp64 [n][d], kv_new fp32 [L][2][n][H][D] or None).
     """
     n = pos.size
@@ -160,7 +161,7 @@ def step(w, weights: np.ndarray, kv: np.ndarray, kv_scales: np.ndarray, pos: np.
                            _p(pos), _p(x), _p(y), _p(y_exact), int(round_acts),
                            _p(kv_new) if kv_new is not None else None)
     if rc != 0:
-        raise ValueError(f"oracle_step: position of session {-rc - 1} outside [0, T_max)")
+        raise ValueError(f"oracle_step: position of session {-rc - 1} at or beyond T_max")
     return y, y_exact, kv_new
 
 
@@ -180,7 +181,7 @@ def prefill_history(w, sessions, pos, poison: bool = True):
     for l in range(L):
         for which in range(2):
             for j, s in enumerate(sessions):
-                P = int(pos[j])
+                P = max(int(pos[j]), 0)  # an empty slot (negative position) has no history
                 raw = synth.kv_raw_host(w, l, which, int(s), 1, P)
                 codes, scales = quantize_rows(raw)
                 kv[l, which, j] = codes[0]

@@ -195,11 +195,13 @@ static int64_t layer_elems(const oracle_cfg* c) {
  * One frame for n independent sessions.  kv is [L][2][n][H][T_max][D] codes,
  * kv_scales [L][2][n][H][T_max]; both are read at slots 0..pos[s]-1 and slot
  * pos[s] is written (then read back quantised).  x, y are [n][d] bf16.
+ * A negative pos[s] marks an empty slot (a fixed-shape batch with a place
+ * not taken by a session): y[s] = x[s] and its cache is not touched.
  * y_exact (nullable) receives the fp64 residual before the final rounding;
  * kv_new (nullable) receives the fp32 K/V values that were quantised,
- * [L][2][n][H][D].  round_acts = 0 skips the bf16 rounding of activations
- * (an fp64 "pure" variant, for information).  Returns 0, or -(s+1) for the
- * first session whose position is outside [0, T_max).
+ * [L][2][n][H][D] (NaN for empty slots).  round_acts = 0 skips the bf16
+ * rounding of activations (an fp64 "pure" variant, for information).
+ * Returns 0, or -(s+1) for the first session whose position is >= T_max.
  */
 int oracle_step(const oracle_cfg* c, int T_max, const uint16_t* weights, int n, uint8_t* kv,
                 float* kv_scales, const int32_t* pos, const uint16_t* x, uint16_t* y,
@@ -208,7 +210,7 @@ int oracle_step(const oracle_cfg* c, int T_max, const uint16_t* weights, int n, 
   const int HD = H * D;
   const int64_t le = layer_elems(c);
   for (int s = 0; s < n; ++s)
-    if (pos[s] < 0 || pos[s] >= T_max) return -(s + 1);
+    if (pos[s] >= T_max) return -(s + 1);
 
   double* r = (double*)malloc(sizeof(double) * d);
   double* xn = (double*)malloc(sizeof(double) * d);
@@ -220,6 +222,20 @@ int oracle_step(const oracle_cfg* c, int T_max, const uint16_t* weights, int n, 
 
   for (int s = 0; s < n; ++s) {
     const int P = pos[s];
+    if (P < 0) {
+      /* empty slot: the session takes no part in the frame; y = x, no cache access */
+      for (int i = 0; i < d; ++i) {
+        y[(int64_t)s * d + i] = x[(int64_t)s * d + i];
+        if (y_exact) y_exact[(int64_t)s * d + i] = oracle_bf16_to_double(x[(int64_t)s * d + i]);
+      }
+      if (kv_new)
+        for (int l = 0; l < L; ++l)
+          for (int which = 0; which < 2; ++which)
+            for (int h = 0; h < H; ++h)
+              for (int i = 0; i < D; ++i)
+                kv_new[((((int64_t)l * 2 + which) * n + s) * H + h) * D + i] = NAN;
+      continue;
+    }
     for (int i = 0; i < d; ++i) r[i] = oracle_bf16_to_double(x[(int64_t)s * d + i]);
     for (int l = 0; l < L; ++l) {
       const uint16_t* Wl = weights + (int64_t)l * le;

@@ -165,6 +165,30 @@ def test_invalid_arguments_are_rejected(tiny):
         fsd.Wave(case.cfg, 4, 62)
 
 
+def test_empty_slots_pass_x_through_and_touch_no_cache():
+    # negative positions: places of the fixed-shape batch with no session
+    w = synth.MID
+    pos = synth.positions(w, w.S).copy()
+    empty = [1, 7, 18]
+    pos[empty] = -1
+    case = DeviceCase(w, pos=pos)
+    wave = fsd.Wave(case.cfg, case.S_max, w.T_max)
+    try:
+        kv0, sc0 = case.kv.clone(), case.sc.clone()
+        case.step(wave)
+        assert wave.status() == fsd.WAVE_OK
+        y = case.y_bits()
+        assert np.array_equal(y[empty], case.x_h[empty])
+        assert torch.equal(case.kv[:, :, empty], kv0[:, :, empty])
+        assert torch.equal(case.sc[:, :, empty].view(torch.int32), sc0[:, :, empty].view(torch.int32))
+        sess = [s for s in range(w.S) if s not in empty]
+        _, y_exact, _, _, _ = oracle_reference(w, sess, pos[sess], case.x_h[sess])
+        ok, worst = y_close(y[sess], y_exact)
+        assert ok, f"worst ratio {worst:.3f}"
+    finally:
+        wave.close()
+
+
 def test_out_of_range_position_is_reported_and_skipped():
     w = synth.TINY
     case = DeviceCase(w)

@@ -117,3 +117,38 @@ def test_step_rejects_out_of_range_position():
     bad[1] = w.T_max
     with pytest.raises(ValueError):
         oracle.step(w, W, kv, sc, bad, x)
+
+
+def test_empty_slot_passes_x_through_and_leaves_the_others_alone():
+    # A negative position marks a place of the fixed-shape batch with no
+    # session in it: y = x bit for bit, its cache untouched, and the other
+    # sessions' results and cache writes equal to a batch without that place.
+    w = synth.TINY
+    W = synth.weights_host(w)
+    pos, x, kv, sc = _inputs(w)
+    pos = pos.copy()
+    pos[1] = -1
+    kv, sc = oracle.prefill_history(w, list(range(w.S)), pos, poison=True)
+    kv0, sc0 = kv.copy(), sc.copy()
+    y, y_exact, kv_new = oracle.step(w, W, kv, sc, pos, x, want_kv_new=True)
+    assert np.array_equal(y[1], x[1])
+    assert np.array_equal(y_exact[1], synth.bf16_bits_to_f32(x[1]).astype(np.float64))
+    assert np.array_equal(kv[:, :, 1], kv0[:, :, 1])
+    assert np.array_equal(sc[:, :, 1].view(np.uint32), sc0[:, :, 1].view(np.uint32))
+    assert np.all(np.isnan(kv_new[:, :, 1]))
+    keep = [0, 2, 3]
+    kv2, sc2 = oracle.prefill_history(w, keep, pos[keep], poison=True)
+    y2, _, _ = oracle.step(w, W, kv2, sc2, pos[keep], x[keep])
+    assert np.array_equal(y[keep], y2)
+    assert np.array_equal(kv[:, :, keep], kv2)
+    assert np.array_equal(sc[:, :, keep].view(np.uint32), sc2.view(np.uint32))
+
+
+def test_position_at_t_max_is_refused():
+    w = synth.TINY
+    W = synth.weights_host(w)
+    pos, x, kv, sc = _inputs(w)
+    pos = pos.copy()
+    pos[2] = w.T_max
+    with pytest.raises(ValueError):
+        oracle.step(w, W, kv, sc, pos, x)
