@@ -7,6 +7,7 @@ in [0, 3000).  Metric: session-frames/s = S / step time, with p50/p99 step
 latency and the HBM roofline fraction of the step kernel.
 
   python bench.py [--gpus N --steps K --warmup W] [--S 80] [--impl reference]
+  python bench.py --sweep 1,8,16,32,48,56,64,80,96,128 --steps 20
 
 Inputs are seeded and synthetic and are drawn on the device (weights and the
 raw history by the generator's device twin, the history quantised by the
@@ -396,6 +397,48 @@ def run_phases(args, w):
     wave.close()
 
 
+def run_sweep(args, w):
+    """Session sweep on one GPU: one history of S_max = max(S) sessions, and
+    for each S the first S of them (positions are the first S of one draw,
+    so the sweeps nest).  One JSON line per S: session-frames/s, p50/p99
+    step ms, algorithmic GB/s and its fraction of the HBM peak."""
+    import torch
+    import frame_step_decode_gb300 as fsd
+    device = torch.device("cuda", 0)
+    sizes = [int(v) for v in args.sweep.split(",")]
+    S_max = max(sizes)
+    weights, kv, sc, pos, pos_h, x, y = build_inputs(w, S_max, device)
+    wave = fsd.Wave(fsd.WaveConfig.of(w), S_max, w.T_max)
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = measured_peaks()
+    for S in sizes:
+        for _ in range(max(3, args.warmup)):
+            wave.step(S, weights, kv, sc, pos, x, y, stream=stream)
+        if wave.status() != fsd.WAVE_OK:
+            raise RuntimeError(f"warm-up failed at S={S}")
+        ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            ev0[i].record(stream)
+            wave.step(S, weights, kv, sc, pos, x, y, stream=stream)
+            ev1[i].record(stream)
+        torch.cuda.synchronize()
+        if wave.status() != fsd.WAVE_OK:
+            raise RuntimeError(f"timed step failed at S={S}")
+        per = [ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)]
+        ms = statistics.mean(per)
+        b = algorithmic_bytes(w, pos_h[:S])
+        gbs = b / (ms * 1e-3) / 1e9
+        print(json.dumps({"sweep": True, "workload": w.name, "S": S, "metric": METRIC,
+                          "value": S / (ms * 1e-3), "ms_per_step": ms,
+                          "p50_ms": statistics.median(per), "p99_ms": float(np.percentile(per, 99)),
+                          "algorithmic_bytes": b, "achieved_gbs": gbs, "peak_gbs": peak,
+                          "peak_kind": peak_kind, "frac": gbs / peak, "frac_of_8000": gbs / 8000.0,
+                          "steps": args.steps}), flush=True)
+    wave.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -406,6 +449,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (profiling a small case)")
     ap.add_argument("--tmax", type=int, default=None, help="shorter history (profiling a small case)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", default=None,
+                    help="comma-separated session counts: one JSON line per S (one GPU)")
     ap.add_argument("--phases", action="store_true",
                     help="print the per-phase time table of one step instead of the JSON line")
     args = ap.parse_args()
@@ -417,7 +462,9 @@ def main():
         T = args.tmax or w.T_max
         w = replace(w, n_layers=args.layers or w.n_layers, T_max=T, pos_hi=min(w.pos_hi, T),
                     name=f"{w.name}-L{args.layers or w.n_layers}-T{T}")
-    if args.phases:
+    if args.sweep:
+        run_sweep(args, w)
+    elif args.phases:
         run_phases(args, w)
     elif args.impl == "reference":
         run_reference(args, w)
