@@ -8,6 +8,7 @@ latency and the HBM roofline fraction of the step kernel.
 
   python bench.py [--gpus N --steps K --warmup W] [--S 80] [--impl reference]
   python bench.py --sweep 1,8,16,32,48,56,64,80,96,128 --steps 20
+  python bench.py --beat 2
 
 Inputs are seeded and synthetic and are drawn on the device (weights and the
 raw history by the generator's device twin, the history quantised by the
@@ -439,6 +440,50 @@ def run_sweep(args, w):
     wave.close()
 
 
+def run_beat(args, w):
+    """Beats of `--beat` frames per launch (the pages' beat is two 80 ms
+    frames with a 160 ms deadline): per-beat CUDA-event times, p50/p99, and
+    late beats.  Positions are held fixed between beats (advance off) so that
+    every timed beat moves the same bytes."""
+    import torch
+    import frame_step_decode_gb300 as fsd
+    device = torch.device("cuda", 0)
+    S, F = args.S, args.beat
+    weights, kv, sc, pos, pos_h, x, y = build_inputs(w, S, device)
+    pos_h = np.minimum(pos_h, w.T_max - F)
+    pos = torch.from_numpy(pos_h).to(device)
+    xs = x.unsqueeze(0).repeat(F, 1, 1).contiguous()
+    ys = torch.empty_like(xs)
+    wave = fsd.Wave(fsd.WaveConfig.of(w), S, w.T_max)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        wave.beat(S, F, weights, kv, sc, pos, xs, ys, advance=False, stream=stream)
+    if wave.status() != fsd.WAVE_OK:
+        raise RuntimeError("warm-up beat failed")
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        ev0[i].record(stream)
+        wave.beat(S, F, weights, kv, sc, pos, xs, ys, advance=False, stream=stream)
+        ev1[i].record(stream)
+    torch.cuda.synchronize()
+    if wave.status() != fsd.WAVE_OK:
+        raise RuntimeError("timed beat failed")
+    per = [ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)]
+    ms = statistics.mean(per)
+    b = sum(algorithmic_bytes(w, pos_h + f) for f in range(F))
+    gbs = b / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    print(json.dumps({"beat": True, "frames_per_launch": F, "workload": w.name, "S": S, "metric": METRIC,
+                      "value": F * S / (ms * 1e-3), "ms_per_beat": ms, "p50_ms": statistics.median(per),
+                      "p99_ms": float(np.percentile(per, 99)),
+                      "late_beats_over_deadline": int(sum(1 for t in per if t > 80.0 * F)),
+                      "deadline_ms": 80.0 * F, "achieved_gbs": gbs, "peak_gbs": peak,
+                      "peak_kind": peak_kind, "frac": gbs / peak, "steps": args.steps}), flush=True)
+    wave.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -449,6 +494,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (profiling a small case)")
     ap.add_argument("--tmax", type=int, default=None, help="shorter history (profiling a small case)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--beat", type=int, default=0,
+                    help="time beats of this many frames per launch (one JSON line, one GPU)")
     ap.add_argument("--sweep", default=None,
                     help="comma-separated session counts: one JSON line per S (one GPU)")
     ap.add_argument("--phases", action="store_true",
@@ -462,7 +509,9 @@ def main():
         T = args.tmax or w.T_max
         w = replace(w, n_layers=args.layers or w.n_layers, T_max=T, pos_hi=min(w.pos_hi, T),
                     name=f"{w.name}-L{args.layers or w.n_layers}-T{T}")
-    if args.sweep:
+    if args.beat:
+        run_beat(args, w)
+    elif args.sweep:
         run_sweep(args, w)
     elif args.phases:
         run_phases(args, w)

@@ -34,7 +34,7 @@ class WaveError(RuntimeError):
 
 
 _lib = None
-EXPORTS = ("wave_create", "wave_destroy", "wave_weights_bytes", "wave_weight_offset", "wave_step",
+EXPORTS = ("wave_create", "wave_destroy", "wave_weights_bytes", "wave_weight_offset", "wave_step", "wave_beat",
            "wave_status", "wave_strerror", "wave_kv_quantize", "wave_fp8_encode", "wave_step_static",
            "wave_set_timeout_ns", "wave_debug_skip_barrier", "wave_debug_dump_kv", "wave_debug_phase_times", "wave_debug_arrival_times",
            "wave_grid_size",
@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
         L.wave_weight_offset.restype = sz
         L.wave_step.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
         L.wave_step.restype = i32
+        L.wave_beat.argtypes = [vp, i32, i32, vp, vp, vp, vp, i32, vp, vp, vp]
+        L.wave_beat.restype = i32
         L.wave_status.argtypes = [vp]
         L.wave_status.restype = i32
         L.wave_strerror.argtypes = [i32]
@@ -133,6 +135,17 @@ class Wave:
                              _ptr(x), _ptr(y), _stream(stream))
         if check and rc != WAVE_OK:
             raise WaveError(rc, "wave_step")
+        return rc
+
+    def beat(self, S, frames, weights, kv, kv_scales, positions, x, y, advance=True, stream=None,
+             check=True) -> int:
+        """`frames` frames in one launch (x, y [frames][S][d]); frame f at
+        positions + f; positions advanced by `frames` on the device when
+        `advance` is set."""
+        rc = lib().wave_beat(self.h, S, frames, _ptr(weights), _ptr(kv), _ptr(kv_scales), _ptr(positions),
+                             int(bool(advance)), _ptr(x), _ptr(y), _stream(stream))
+        if check and rc != WAVE_OK:
+            raise WaveError(rc, "wave_beat")
         return rc
 
     def status(self) -> int:

@@ -341,10 +341,13 @@ static int encode_kv_map(wave_ctx* h, uint8_t* kv, float* scales) {
   return WAVE_OK;
 }
 
-extern "C" int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8, float* kv_scales,
-                         const int32_t* positions, const void* x, void* y, void* stream) {
+// One launch of `frames` frames (positions + f in frame f); positions are
+// advanced by `frames` on the device at the end when `advance` is set.
+static int launch_frames(wave_t* h, int S, int frames, const void* weights, uint8_t* kv_fp8,
+                         float* kv_scales, const int32_t* positions, int32_t* advance, const void* x,
+                         void* y, void* stream) {
   if (!h || !weights || !kv_fp8 || !kv_scales || !positions || !x || !y) return WAVE_EINVAL;
-  if (S < 1 || S > h->S_max) return WAVE_EINVAL;
+  if (S < 1 || S > h->S_max || frames < 1 || frames > kMaxFrames) return WAVE_EINVAL;
   if (((uintptr_t)weights & 15) || ((uintptr_t)kv_fp8 & 15) || ((uintptr_t)kv_scales & 15) ||
       ((uintptr_t)positions & 3) || ((uintptr_t)x & 15) || ((uintptr_t)y & 15))
     return WAVE_EINVAL;
@@ -403,6 +406,8 @@ extern "C" int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8,
   p.pos = positions;
   p.x = (const uint16_t*)x;
   p.y = (uint16_t*)y;
+  p.n_frames = frames;
+  p.pos_advance = advance;
   p.resid = h->resid;
   p.xn = h->xn;
   p.qkv = h->qkv;
@@ -421,15 +426,29 @@ extern "C" int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8,
   p.timeout_ns = h->timeout_ns;
   p.skip_cta = h->skip_cta;
   p.skip_bar = h->skip_bar;
-  p.kv_dump = h->kv_dump;
-  p.phase_ts = h->phase_ts;
-  p.arrive_ts = h->arrive_ts;
+  if (frames == 1) {  // the profiling and testing hooks are sized for one frame
+    p.kv_dump = h->kv_dump;
+    p.phase_ts = h->phase_ts;
+    p.arrive_ts = h->arrive_ts;
+  }
   if (cudaMemsetAsync(h->bar, 0, 4, st) != cudaSuccess) return WAVE_ECUDA;
   cudaError_t e = launch_step(p, h->grid, st);
   h->last_stream = st;
   if (e == cudaErrorCooperativeLaunchTooLarge) return WAVE_ELAUNCH;
   if (e != cudaSuccess) return WAVE_ECUDA;
   return WAVE_OK;
+}
+
+extern "C" int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8, float* kv_scales,
+                         const int32_t* positions, const void* x, void* y, void* stream) {
+  return launch_frames(h, S, 1, weights, kv_fp8, kv_scales, positions, nullptr, x, y, stream);
+}
+
+extern "C" int wave_beat(wave_t* h, int S, int frames, const void* weights, uint8_t* kv_fp8,
+                         float* kv_scales, int32_t* positions, int advance, const void* x, void* y,
+                         void* stream) {
+  return launch_frames(h, S, frames, weights, kv_fp8, kv_scales, positions, advance ? positions : nullptr,
+                       x, y, stream);
 }
 
 extern "C" int wave_status(wave_t* h) {

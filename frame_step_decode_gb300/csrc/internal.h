@@ -40,8 +40,10 @@ struct StepParams {
   uint8_t* kv;
   float* kv_scales;
   const int32_t* pos;
-  const uint16_t* x;
-  uint16_t* y;
+  const uint16_t* x;     // [n_frames][S][d]
+  uint16_t* y;           // [n_frames][S][d]
+  int n_frames;          // frames run back to back in this launch (positions + f in frame f)
+  int32_t* pos_advance;  // if set: positions += n_frames at the end (empty slots stay empty)
   // workspace
   float* resid;          // [S_pad_max][d] fp32 residual stream
   uint16_t* xn;          // [S_pad_max][d] bf16 normed input of QKV / gate-up
@@ -70,6 +72,8 @@ struct StepParams {
 // Counter words of the workspace: two per GEMM tile (1024 tiles at most),
 // then one attention work counter per layer (1024 layers at most).
 constexpr int kCounterWords = 2048 + 1024;
+// Frames one launch may run back to back (wave_beat).
+constexpr int kMaxFrames = 64;
 
 __host__ __device__ inline int stream_k_ctas(int grid, long long U, int tiles) {
   long long g = grid;
@@ -83,6 +87,7 @@ cudaError_t launch_step(const StepParams& p, int grid, cudaStream_t stream);
 cudaError_t configure_step_kernel();
 cudaError_t occupancy_per_sm(int* blocks);
 int barriers_per_step(int L);
+int barriers_per_launch(int L, int frames, bool advance);
 // Dynamic shared memory layout shared by host checks and the kernel.
 struct SmemLayout {
   int ring_off, ring_bytes;      // GEMM ring / attention K and V tiles (union)

@@ -42,6 +42,7 @@ struct Ctx {
   uint32_t acc_it;      // accumulator counter (MMA and epilogue threads)
   uint32_t att_it;      // attention chunk counter (per warp)
   uint32_t norm_it;     // norm-row copy counter (all threads)
+  int frame;            // frame of the launch being computed
   SmemLayout lay;
 };
 
@@ -133,7 +134,7 @@ __device__ bool norm_phase(const StepParams& p, Ctx& c, const uint16_t* g, bool 
       fence_proxy_async_smem();  // earlier generic accesses to this area come first
       mbar_arrive_expect_tx(nbar, (from_x ? 4u : 6u) * (uint32_t)d);  // row + g
       if (from_x)
-        bulk_load(c.sbase + c.lay.ring_off + 6 * d, p.x + (size_t)s * d, 2u * d, nbar);
+        bulk_load(c.sbase + c.lay.ring_off + 6 * d, p.x + ((size_t)c.frame * p.S + s) * d, 2u * d, nbar);
       else
         bulk_load(c.sbase + c.lay.ring_off, p.resid + (size_t)s * d, 4u * d, nbar);
       bulk_load(c.sbase + c.lay.ring_off + 4 * d, g, 2u * d, nbar);
@@ -277,18 +278,19 @@ __device__ __forceinline__ void swiglu_store(uint16_t* urow, int n, int F, const
 // resid[s][n..n+3] = old + v (and y = bf16 of it after the last layer; an
 // empty slot, negative position, passes x through unchanged).
 __device__ __forceinline__ void resid_store(const StepParams& p, int s, int n, float4 old, const float4& v,
-                                            bool last_layer) {
+                                            bool last_layer, int frame) {
   add4(old, v);
   *(float4*)(p.resid + (size_t)s * p.d + n) = old;
   if (last_layer) {
+    const size_t at = ((size_t)frame * p.S + s) * p.d + n;
     uint2 o;
     if (p.pos[s] < 0) {
-      o = *(const uint2*)(p.x + (size_t)s * p.d + n);
+      o = *(const uint2*)(p.x + at);
     } else {
       o.x = (uint32_t)f32_to_bf16(old.x) | ((uint32_t)f32_to_bf16(old.y) << 16);
       o.y = (uint32_t)f32_to_bf16(old.z) | ((uint32_t)f32_to_bf16(old.w) << 16);
     }
-    *(uint2*)(p.y + (size_t)s * p.d + n) = o;
+    *(uint2*)(p.y + at) = o;
   }
 }
 
@@ -298,7 +300,7 @@ __device__ __forceinline__ void resid_store(const StepParams& p, int s, int n, f
 // et + step, ...
 __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t, const float* first,
                                          const long long* seg, int nseg, int et, int step,
-                                         bool last_layer) {
+                                         bool last_layer, int frame) {
   if (kind == kGU) {
     // item (s, r4): gate rows 4r4..4r4+3 and the up rows 64 below them
     const int F = p.F, items = p.S * 16;
@@ -348,8 +350,8 @@ __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t
       float4 a0, a1;
       seg_sum2(first, p.gemm_part, seg, nseg, (size_t)s0 * kTileM + (n0 - t * kTileM),
                (size_t)s1 * kTileM + (n1 - t * kTileM), a0, a1);
-      if (n0 < d) resid_store(p, s0, n0, old0, a0, last_layer);
-      if (two && n1 < d) resid_store(p, s1, n1, old1, a1, last_layer);
+      if (n0 < d) resid_store(p, s0, n0, old0, a0, last_layer, frame);
+      if (two && n1 < d) resid_store(p, s1, n1, old1, a1, last_layer, frame);
     }
   }
 }
@@ -475,7 +477,7 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
       if (nseg == 1) {
         // whole tile here: the four epilogue warps finish it from the slot
         named_bar(1, 128);
-        finish_tile(p, kind, t, slot, nullptr, 1, threadIdx.x - 64, 128, last_layer);
+        finish_tile(p, kind, t, slot, nullptr, 1, threadIdx.x - 64, 128, last_layer, c.frame);
       } else {
         // split tile: count this segment in
         __threadfence();
@@ -526,7 +528,7 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
   __syncthreads();
   if (!*misc_word(c, 3)) return;
   finish_tile(p, kind, t, p.gemm_part + seg[0], seg, nseg, idx * kThreads + threadIdx.x, m * kThreads,
-              last_layer);
+              last_layer, c.frame);
   __syncthreads();
   // the last final contributor to finish re-arms the tile's counters
   if (threadIdx.x == 0 && atomicAdd(p.tile_cnt + 1024 + t, 1) == m - 1) {
@@ -997,7 +999,8 @@ __device__ void build_pieces(const StepParams& p, Ctx& c) {
   int* spos = (int*)(c.smem + c.lay.xbuf_off);   // positions, -1 where invalid
   const int N = p.S * p.H, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int s = tid; s < p.S; s += kThreads) {
-    const int P = p.pos[s];
+    const int P0 = p.pos[s];
+    const int P = (P0 < 0) ? P0 : P0 + c.frame;  // frame f of a launch is at position + f
     // a negative position is an empty slot; one at or beyond T_max an error
     spos[s] = (P >= 0 && P < p.T_max) ? P : -1;
     if (P >= p.T_max) set_err(p, kErrPos);
@@ -1107,6 +1110,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   c.bar_target = 0;
   c.bar_index = 0;
   c.ring_it = c.acc_it = c.att_it = c.norm_it = 0;
+  c.frame = 0;
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
@@ -1140,33 +1144,47 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   c.tmem = *(volatile uint32_t*)(c.smem + c.lay.misc_off);
 
   if (p.phase_ts && blockIdx.x == 0 && threadIdx.x == 0) p.phase_ts[0] = globaltimer();
-  // phase 0: work list, counter reset, residual and first norm
-  for (int i = blockIdx.x * kThreads + threadIdx.x; i < kCounterWords; i += gridDim.x * kThreads)
-    p.tile_cnt[i] = 0;
-  if (blockIdx.x == gridDim.x - 1) build_pieces(p, c);
-  const bool n0 = norm_phase(p, c, p.weights + p.off_g_attn, true);
-  bool ok = grid_sync(p, c) && n0;
+  bool ok = true;
+  for (int f = 0; ok && f < p.n_frames; ++f) {
+    c.frame = f;
+    // the previous frame's last reductions (resid, y) finish before this
+    // frame's prologue reloads the residual
+    if (f > 0 && !(ok = grid_sync(p, c))) break;
+    // phase 0: work list, counter reset, residual and first norm
+    for (int i = blockIdx.x * kThreads + threadIdx.x; i < kCounterWords; i += gridDim.x * kThreads)
+      p.tile_cnt[i] = 0;
+    if (blockIdx.x == gridDim.x - 1) build_pieces(p, c);
+    const bool n0 = norm_phase(p, c, p.weights + p.off_g_attn, true);
+    if (!(ok = grid_sync(p, c) && n0)) break;
 
-  for (int l = 0; ok && l < p.L; ++l) {
-    const uint16_t* wl = p.weights + (size_t)l * p.layer_elems;
-    if (l > 0) {
-      const bool nok = norm_phase(p, c, wl + p.off_g_attn, false);
-      if (!(ok = grid_sync(p, c) && nok)) break;
+    for (int l = 0; ok && l < p.L; ++l) {
+      const uint16_t* wl = p.weights + (size_t)l * p.layer_elems;
+      if (l > 0) {
+        const bool nok = norm_phase(p, c, wl + p.off_g_attn, false);
+        if (!(ok = grid_sync(p, c) && nok)) break;
+      }
+      gemm_phase(p, c, kQKV, l, false);
+      if (!(ok = grid_sync(p, c))) break;
+      if (p.D == 128) attention_phase<128>(p, c, l); else attention_phase<64>(p, c, l);
+      if (!(ok = grid_sync(p, c))) break;
+      if (p.D == 128) merge_phase<128>(p, c); else merge_phase<64>(p, c);
+      if (!(ok = grid_sync(p, c))) break;
+      gemm_phase(p, c, kO, l, false);
+      if (!(ok = grid_sync(p, c))) break;
+      const bool nok2 = norm_phase(p, c, wl + p.off_g_mlp, false);
+      if (!(ok = grid_sync(p, c) && nok2)) break;
+      gemm_phase(p, c, kGU, l, false);
+      if (!(ok = grid_sync(p, c))) break;
+      gemm_phase(p, c, kDown, l, l == p.L - 1);
+      if (l < p.L - 1 && !(ok = grid_sync(p, c))) break;
     }
-    gemm_phase(p, c, kQKV, l, false);
-    if (!(ok = grid_sync(p, c))) break;
-    if (p.D == 128) attention_phase<128>(p, c, l); else attention_phase<64>(p, c, l);
-    if (!(ok = grid_sync(p, c))) break;
-    if (p.D == 128) merge_phase<128>(p, c); else merge_phase<64>(p, c);
-    if (!(ok = grid_sync(p, c))) break;
-    gemm_phase(p, c, kO, l, false);
-    if (!(ok = grid_sync(p, c))) break;
-    const bool nok2 = norm_phase(p, c, wl + p.off_g_mlp, false);
-    if (!(ok = grid_sync(p, c) && nok2)) break;
-    gemm_phase(p, c, kGU, l, false);
-    if (!(ok = grid_sync(p, c))) break;
-    gemm_phase(p, c, kDown, l, l == p.L - 1);
-    if (l < p.L - 1 && !(ok = grid_sync(p, c))) break;
+  }
+  // rolling positions: every frame has read them; advance once all are done
+  if (ok && p.pos_advance) {
+    ok = grid_sync(p, c);
+    if (ok && blockIdx.x == 0)
+      for (int s = threadIdx.x; s < p.S; s += kThreads)
+        if (p.pos_advance[s] >= 0) p.pos_advance[s] += p.n_frames;
   }
 
   if (!ok) {
@@ -1204,6 +1222,9 @@ cudaError_t launch_step(const StepParams& p, int grid, cudaStream_t stream) {
 }
 
 int barriers_per_step(int L) { return 8 * L - 1; }
+int barriers_per_launch(int L, int frames, bool advance) {
+  return frames * (8 * L - 1) + (frames - 1) + (advance ? 1 : 0);
+}
 
 cudaError_t occupancy_per_sm(int* blocks) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel, kThreads,

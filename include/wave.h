@@ -123,7 +123,25 @@ int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8, float* kv_
               const int32_t* positions, const void* x, void* y, void* stream);
 
 /*
- * Synchronise the stream of the last wave_step on this handle, then return
+ * Several frames in one launch: the beat of the dotwave.ai case study ("01 /
+ * The challenge", "Measurement notes": two 80 ms model steps per beat, a
+ * 160 ms deadline; "02 / The solution": state stays ready between beats).
+ * Frame f (0 <= f < frames) reads x[f] and writes y[f] (x, y bf16
+ * [frames][S][d], 16-byte aligned) and runs every session at position
+ * pos[s] + f; a negative pos[s] stays an empty slot in every frame.  The
+ * results equal `frames` wave_step calls with the positions advanced by one
+ * between them.  With advance != 0 the kernel adds `frames` to every
+ * non-negative pos[s] after the last frame (positions roll on the device;
+ * nothing crosses to the host between beats); with advance == 0 positions is
+ * only read.  1 <= frames <= 64; the other arguments, the error behaviour
+ * and the asynchrony are those of wave_step.  The wave_debug_* hooks apply to
+ * single-frame launches only.
+ */
+int wave_beat(wave_t* h, int S, int frames, const void* weights, uint8_t* kv_fp8, float* kv_scales,
+              int32_t* positions, int advance, const void* x, void* y, void* stream);
+
+/*
+ * Synchronise the stream of the last wave_step / wave_beat on this handle, then return
  * and clear the device error word: WAVE_OK, WAVE_ETIMEOUT (a device wait gave
  * up; the step's outputs are undefined, the GPU context stays usable) or
  * WAVE_EPOS.  Returns WAVE_ECUDA if the synchronisation itself failed.

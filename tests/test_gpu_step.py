@@ -189,6 +189,50 @@ def test_empty_slots_pass_x_through_and_touch_no_cache():
         wave.close()
 
 
+@pytest.mark.parametrize("w", [synth.TINY, synth.MID])
+def test_two_frame_beat_equals_two_steps_and_rolls_positions(w):
+    # one launch of two frames against two single-frame launches with the
+    # positions advanced on the host: same kernels, same order -> same bits
+    pos = synth.positions(w, w.S).copy()
+    pos = np.minimum(pos, w.T_max - 2)
+    pos[w.S // 2] = -1  # an empty slot stays empty in both frames
+    a = DeviceCase(w, pos=pos)
+    b = DeviceCase(w, pos=pos)
+    x2 = torch.stack([a.x, a.x.flip(0)])  # frame 1 gets other rows
+    y2 = torch.zeros_like(x2)
+    wave = fsd.Wave(a.cfg, a.S_max, w.T_max)
+    try:
+        wave.beat(w.S, 2, a.weights, a.kv, a.sc, a.pos, x2, y2, advance=True)
+        assert wave.status() == fsd.WAVE_OK
+        ref = []
+        for f in range(2):
+            xf = x2[f].contiguous()
+            yf = torch.zeros_like(xf)
+            wave.step(w.S, b.weights, b.kv, b.sc, b.pos, xf, yf)
+            assert wave.status() == fsd.WAVE_OK
+            ref.append(yf)
+            b.pos += (b.pos >= 0).int()
+        assert torch.equal(y2[0].view(torch.int16), ref[0].view(torch.int16))
+        assert torch.equal(y2[1].view(torch.int16), ref[1].view(torch.int16))
+        assert torch.equal(a.kv, b.kv)
+        assert torch.equal(a.sc.view(torch.int32), b.sc.view(torch.int32))
+        assert torch.equal(a.pos, b.pos)
+        assert a.pos[w.S // 2].item() == -1
+        # and frame 1 against the oracle, from the oracle's own frame-0 state
+        import oracle
+        sess = [s for s in range(w.S) if pos[s] >= 0]
+        kv_o, sc_o = oracle.prefill_history(w, sess, pos[sess], poison=True)
+        W = synth.weights_host(w)
+        x_h = x2.view(torch.int16).cpu().numpy().view(np.uint16)
+        oracle.step(w, W, kv_o, sc_o, pos[sess], np.ascontiguousarray(x_h[0][sess]))
+        _, y1_exact, _ = oracle.step(w, W, kv_o, sc_o, pos[sess] + 1, np.ascontiguousarray(x_h[1][sess]))
+        y1 = y2[1].view(torch.int16).cpu().numpy().view(np.uint16)
+        ok, worst = y_close(y1[sess], y1_exact)
+        assert ok, f"worst ratio {worst:.3f}"
+    finally:
+        wave.close()
+
+
 def test_out_of_range_position_is_reported_and_skipped():
     w = synth.TINY
     case = DeviceCase(w)
