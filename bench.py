@@ -9,6 +9,7 @@ latency and the HBM roofline fraction of the step kernel.
   python bench.py [--gpus N --steps K --warmup W] [--S 80] [--impl reference]
   python bench.py --sweep 1,8,16,32,48,56,64,80,96,128 --steps 20
   python bench.py --beat 2
+  python bench.py --depth
 
 Inputs are seeded and synthetic and are drawn on the device (weights and the
 raw history by the generator's device twin, the history quantised by the
@@ -484,6 +485,60 @@ def run_beat(args, w):
     wave.close()
 
 
+def run_depth(args):
+    """The inner depth loop: 8 dependent steps per frame of the 6-layer
+    d=1024 model, S = 80, one launch per frame (wave_depth).  Per-frame CUDA
+    events; reports frames/s, session-steps/s, p50/p99 frame ms, and the
+    algorithmic bytes per frame (weights once per step + W_p once per chained
+    step + the depth cache read and written) against the HBM peak."""
+    import torch
+    import frame_step_decode_gb300 as fsd
+    w = synth.DEPTH
+    steps = w.extra["depth_steps"]
+    S, d = args.S if args.S != 80 else w.S, w.d_model
+    L, H, T, D = w.n_layers, w.n_heads, w.T_max, w.head_dim
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    weights = torch.empty(synth.weight_elems(w), dtype=torch.bfloat16, device=device)
+    synth.weights_device(w, weights, stream.cuda_stream)
+    wp = torch.empty((d, d), dtype=torch.bfloat16, device=device)
+    synth.proj_device(w, wp.data_ptr(), stream.cuda_stream)
+    x0 = torch.empty((S, d), dtype=torch.bfloat16, device=device)
+    synth.x_device(w, S, x0.data_ptr(), stream.cuda_stream)
+    kv = torch.zeros((L, 2, S, H, T, D), dtype=torch.uint8, device=device)
+    sc = torch.zeros((L, 2, S, H, T), dtype=torch.float32, device=device)
+    xs = torch.empty((steps, S, d), dtype=torch.bfloat16, device=device)
+    y = torch.empty((steps, S, d), dtype=torch.bfloat16, device=device)
+    wave = fsd.Wave(fsd.WaveConfig.of(w), S, T)
+    for _ in range(max(3, args.warmup)):
+        wave.depth(S, steps, weights, wp, kv, sc, x0, xs, y, stream=stream)
+    if wave.status() != fsd.WAVE_OK:
+        raise RuntimeError("warm-up depth loop failed")
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        ev0[i].record(stream)
+        wave.depth(S, steps, weights, wp, kv, sc, x0, xs, y, stream=stream)
+        ev1[i].record(stream)
+    torch.cuda.synchronize()
+    if wave.status() != fsd.WAVE_OK:
+        raise RuntimeError("timed depth loop failed")
+    per = [ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)]
+    ms = statistics.mean(per)
+    b = sum(algorithmic_bytes(w, np.full(S, k)) for k in range(steps)) + (steps - 1) * 2 * d * d
+    gbs = b / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    print(json.dumps({"depth_loop": True, "workload": w.name, "S": S, "steps_per_frame": steps,
+                      "metric": "frames/s", "value": 1000.0 / ms, "session_steps_per_s": S * steps / (ms * 1e-3),
+                      "ms_per_frame": ms, "p50_ms": statistics.median(per), "p99_ms": float(np.percentile(per, 99)),
+                      "us_per_step": 1000.0 * ms / steps, "algorithmic_bytes": b, "achieved_gbs": gbs,
+                      "peak_gbs": peak, "peak_kind": peak_kind, "frac": gbs / peak,
+                      "barriers_per_frame": steps * (8 * L - 1) + 2 * (steps - 1), "steps": args.steps}),
+          flush=True)
+    wave.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -494,6 +549,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (profiling a small case)")
     ap.add_argument("--tmax", type=int, default=None, help="shorter history (profiling a small case)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--depth", action="store_true",
+                    help="time the inner depth loop (8 chained steps of the 6-layer d=1024 model)")
     ap.add_argument("--beat", type=int, default=0,
                     help="time beats of this many frames per launch (one JSON line, one GPU)")
     ap.add_argument("--sweep", default=None,
@@ -509,7 +566,9 @@ def main():
         T = args.tmax or w.T_max
         w = replace(w, n_layers=args.layers or w.n_layers, T_max=T, pos_hi=min(w.pos_hi, T),
                     name=f"{w.name}-L{args.layers or w.n_layers}-T{T}")
-    if args.beat:
+    if args.depth:
+        run_depth(args)
+    elif args.beat:
         run_beat(args, w)
     elif args.sweep:
         run_sweep(args, w)

@@ -34,7 +34,7 @@ class WaveError(RuntimeError):
 
 
 _lib = None
-EXPORTS = ("wave_create", "wave_destroy", "wave_weights_bytes", "wave_weight_offset", "wave_step", "wave_beat",
+EXPORTS = ("wave_create", "wave_destroy", "wave_weights_bytes", "wave_weight_offset", "wave_step", "wave_beat", "wave_depth",
            "wave_status", "wave_strerror", "wave_kv_quantize", "wave_fp8_encode", "wave_step_static",
            "wave_set_timeout_ns", "wave_debug_skip_barrier", "wave_debug_dump_kv", "wave_debug_phase_times", "wave_debug_arrival_times",
            "wave_grid_size",
@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
         L.wave_step.restype = i32
         L.wave_beat.argtypes = [vp, i32, i32, vp, vp, vp, vp, i32, vp, vp, vp]
         L.wave_beat.restype = i32
+        L.wave_depth.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.wave_depth.restype = i32
         L.wave_status.argtypes = [vp]
         L.wave_status.restype = i32
         L.wave_strerror.argtypes = [i32]
@@ -135,6 +137,15 @@ class Wave:
                              _ptr(x), _ptr(y), _stream(stream))
         if check and rc != WAVE_OK:
             raise WaveError(rc, "wave_step")
+        return rc
+
+    def depth(self, S, steps, weights, w_proj, kv, kv_scales, x0, xs, y, stream=None, check=True) -> int:
+        """The inner depth loop: `steps` dependent steps, x_k = bf16(W_p y_{k-1})
+        (xs [steps][S][d] scratch, y [steps][S][d])."""
+        rc = lib().wave_depth(self.h, S, steps, _ptr(weights), _ptr(w_proj), _ptr(kv), _ptr(kv_scales),
+                              _ptr(x0), _ptr(xs), _ptr(y), _stream(stream))
+        if check and rc != WAVE_OK:
+            raise WaveError(rc, "wave_depth")
         return rc
 
     def beat(self, S, frames, weights, kv, kv_scales, positions, x, y, advance=True, stream=None,

@@ -24,7 +24,7 @@ struct wave_ctx {
   wave_config cfg;
   int S_max, S_pad_max, T_max, device, grid;
   long long layer_elems, off[6];
-  int tiles[4], kblocks[4], max_tiles_per_cta;
+  int tiles[kGemmKinds], kblocks[kGemmKinds], max_tiles_per_cta;
   // workspace
   void* ws = nullptr;
   size_t ws_bytes = 0;
@@ -41,7 +41,9 @@ struct wave_ctx {
   unsigned* bar;
   int* err;
   // cached tensor maps
-  CUtensorMap tm_w[4], tm_x[4], tm_kv, tm_sc;
+  CUtensorMap tm_w[kGemmKinds], tm_x[kGemmKinds], tm_kv, tm_sc;
+  const void* maps_wp = nullptr;  // W_p the kProj weight map was encoded for
+  int32_t* zero_pos = nullptr;    // S_max zeros: chained frames start at position 0
   const void* maps_weights = nullptr;
   const void* maps_kv = nullptr;
   const void* maps_sc = nullptr;
@@ -119,9 +121,9 @@ extern "C" const char* wave_strerror(int code) {
 }
 
 // Stream-K split of tiles x kblocks over the grid: the most tiles one CTA touches.
-static int max_tiles_touched(long long tiles, long long kb, int grid) {
+static int max_tiles_touched(long long tiles, long long kb, int grid, int seg_cap) {
   const long long U = tiles * kb;
-  const int G = stream_k_ctas(grid, U, (int)tiles);
+  const int G = stream_k_ctas(grid, U, (int)tiles, seg_cap);
   int mt = 1;
   for (int c = 0; c < G; ++c) {
     const long long u0 = U * c / G, u1 = U * (c + 1) / G;
@@ -133,9 +135,9 @@ static int max_tiles_touched(long long tiles, long long kb, int grid) {
 }
 
 // Most segments (CTAs) any one tile is split into.
-static int max_segments(long long tiles, long long kb, int grid) {
+static int max_segments(long long tiles, long long kb, int grid, int seg_cap) {
   const long long U = tiles * kb;
-  const int G = stream_k_ctas(grid, U, (int)tiles);
+  const int G = stream_k_ctas(grid, U, (int)tiles, seg_cap);
   int ms = 1;
   for (long long t = 0; t < tiles; ++t) {
     const long long a = t * kb, b = (t + 1) * kb - 1;
@@ -175,15 +177,17 @@ extern "C" int wave_create(const wave_config* cfg, int S_max, int T_max, wave_t*
   h->kblocks[kGU] = (d + kKBlk - 1) / kKBlk;
   h->tiles[kDown] = (d + kTileM - 1) / kTileM;
   h->kblocks[kDown] = (F + kKBlk - 1) / kKBlk;
+  h->tiles[kProj] = (d + kTileM - 1) / kTileM;
+  h->kblocks[kProj] = (d + kKBlk - 1) / kKBlk;
   int mt = 1;
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < kGemmKinds; ++k) {
     if (h->tiles[k] > 1024) {
       delete h;
       return WAVE_EINVAL;
     }
-    int m = max_tiles_touched(h->tiles[k], h->kblocks[k], h->grid);
+    int m = max_tiles_touched(h->tiles[k], h->kblocks[k], h->grid, gemm_seg_cap(k));
     if (m > mt) mt = m;
-    if (max_segments(h->tiles[k], h->kblocks[k], h->grid) > 64) {  // kMaxSeg
+    if (max_segments(h->tiles[k], h->kblocks[k], h->grid, gemm_seg_cap(k)) > 64) {  // kMaxSeg
       delete h;
       return WAVE_EINVAL;
     }
@@ -210,6 +214,7 @@ extern "C" int wave_create(const wave_config* cfg, int S_max, int T_max, wave_t*
       {(void**)&h->rope, (size_t)T_max * (D / 2) * 8},
       {(void**)&h->bar, 16},
       {(void**)&h->err, 16},
+      {(void**)&h->zero_pos, (size_t)S_max * 4},
   };
   size_t total = 0;
   for (auto& pt : parts) total += (pt.bytes + 255) & ~(size_t)255;
@@ -345,7 +350,7 @@ static int encode_kv_map(wave_ctx* h, uint8_t* kv, float* scales) {
 // advanced by `frames` on the device at the end when `advance` is set.
 static int launch_frames(wave_t* h, int S, int frames, const void* weights, uint8_t* kv_fp8,
                          float* kv_scales, const int32_t* positions, int32_t* advance, const void* x,
-                         void* y, void* stream) {
+                         void* y, void* stream, uint16_t* x_chain = nullptr) {
   if (!h || !weights || !kv_fp8 || !kv_scales || !positions || !x || !y) return WAVE_EINVAL;
   if (S < 1 || S > h->S_max || frames < 1 || frames > kMaxFrames) return WAVE_EINVAL;
   if (((uintptr_t)weights & 15) || ((uintptr_t)kv_fp8 & 15) || ((uintptr_t)kv_scales & 15) ||
@@ -371,7 +376,7 @@ static int launch_frames(wave_t* h, int S, int frames, const void* weights, uint
   }
   StepParams p;
   memset(&p, 0, sizeof(p));
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < kGemmKinds; ++k) {
     p.tm_w[k] = h->tm_w[k];
     p.tm_x[k] = h->tm_x[k];
     p.tiles[k] = h->tiles[k];
@@ -408,6 +413,8 @@ static int launch_frames(wave_t* h, int S, int frames, const void* weights, uint
   p.y = (uint16_t*)y;
   p.n_frames = frames;
   p.pos_advance = advance;
+  p.depth = x_chain ? 1 : 0;
+  p.x_chain = x_chain;
   p.resid = h->resid;
   p.xn = h->xn;
   p.qkv = h->qkv;
@@ -442,6 +449,36 @@ static int launch_frames(wave_t* h, int S, int frames, const void* weights, uint
 extern "C" int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8, float* kv_scales,
                          const int32_t* positions, const void* x, void* y, void* stream) {
   return launch_frames(h, S, 1, weights, kv_fp8, kv_scales, positions, nullptr, x, y, stream);
+}
+
+extern "C" int wave_depth(wave_t* h, int S, int steps, const void* weights, const void* w_proj,
+                          uint8_t* kv_fp8, float* kv_scales, const void* x0, void* xs, void* y,
+                          void* stream) {
+  if (!h || !w_proj || !x0 || !xs || !y) return WAVE_EINVAL;
+  if (S < 1 || S > h->S_max || steps < 1 || steps > kMaxFrames || steps > h->T_max) return WAVE_EINVAL;
+  if (((uintptr_t)w_proj & 15) || ((uintptr_t)x0 & 15) || ((uintptr_t)xs & 15) || ((uintptr_t)y & 15))
+    return WAVE_EINVAL;
+  const wave_config& c = h->cfg;
+  const cuuint64_t d = c.d_model;
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (w_proj != h->maps_wp) {  // W_p [d][d] as a one-layer stack
+    cuuint64_t dims[3] = {d, d, 1}, str[2] = {d * 2, d * d * 2};
+    cuuint32_t box[3] = {kKBlk, kTileM, 1};
+    if (!enc(&h->tm_w[kProj], BF, 3, (void*)w_proj, dims, str, box, SW)) return WAVE_ECUDA;
+    h->maps_wp = w_proj;
+  }
+  {  // the outputs y [steps * S][d], read back S_pad rows at a time
+    const int S_pad = (S + 15) / 16 * 16;
+    cuuint64_t dims[2] = {d, (cuuint64_t)steps * S}, str[1] = {d * 2};
+    cuuint32_t box[2] = {kKBlk, (cuuint32_t)S_pad};
+    if (!enc(&h->tm_x[kProj], BF, 2, y, dims, str, box, SW)) return WAVE_ECUDA;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  if (xs != x0 && cudaMemcpyAsync(xs, x0, (size_t)S * d * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return WAVE_ECUDA;
+  return launch_frames(h, S, steps, weights, kv_fp8, kv_scales, h->zero_pos, nullptr, xs, y, stream,
+                       (uint16_t*)xs);
 }
 
 extern "C" int wave_beat(wave_t* h, int S, int frames, const void* weights, uint8_t* kv_fp8,

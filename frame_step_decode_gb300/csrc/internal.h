@@ -21,18 +21,19 @@ enum ErrBits : int { kErrTimeout = 1, kErrPos = 2 };
 
 // Device error word bits -> public codes live in api.cu.
 
-enum GemmKind : int { kQKV = 0, kO = 1, kGU = 2, kDown = 3 };
+enum GemmKind : int { kQKV = 0, kO = 1, kGU = 2, kDown = 3, kProj = 4 };
+constexpr int kGemmKinds = 5;
 
 struct StepParams {
-  CUtensorMap tm_w[4];   // weights of the four projections (see GemmKind)
-  CUtensorMap tm_x[4];   // their activation inputs: xn, attn, xn, u (box rows = S_pad)
+  CUtensorMap tm_w[kGemmKinds];  // weights of the projections (see GemmKind)
+  CUtensorMap tm_x[kGemmKinds];  // their activation inputs: xn, attn, xn, u, y (box rows = S_pad)
   CUtensorMap tm_kv;     // the FP8 history as [D][S_max*H*T_max][K|V][L]: one box = a chunk's K and V
   CUtensorMap tm_sc;     // the scales as [S_max*H*T_max][K|V][L]: one box = a chunk's K and V scales
   // shape
   int L, d, H, D, F, HD, S, S_pad, S_max, T_max;
   float eps;
   int nstage;            // GEMM ring depth for this S
-  int tiles[4], kblocks[4];
+  int tiles[kGemmKinds], kblocks[kGemmKinds];
   int max_tiles_per_cta; // partial-sum slots per CTA
   long long layer_elems, off_g_attn, off_g_mlp, off_wo, off_wdown;
   // caller buffers
@@ -44,6 +45,8 @@ struct StepParams {
   uint16_t* y;           // [n_frames][S][d]
   int n_frames;          // frames run back to back in this launch (positions + f in frame f)
   int32_t* pos_advance;  // if set: positions += n_frames at the end (empty slots stay empty)
+  int depth;             // frames chained: x[f] = bf16(W_p y[f-1]) (the kProj GEMM) before frame f
+  uint16_t* x_chain;     // where those inputs go (the buffer x points at)
   // workspace
   float* resid;          // [S_pad_max][d] fp32 residual stream
   uint16_t* xn;          // [S_pad_max][d] bf16 normed input of QKV / gate-up
@@ -75,19 +78,22 @@ constexpr int kCounterWords = 2048 + 1024;
 // Frames one launch may run back to back (wave_beat).
 constexpr int kMaxFrames = 64;
 
-__host__ __device__ inline int stream_k_ctas(int grid, long long U, int tiles) {
+__host__ __device__ inline int stream_k_ctas(int grid, long long U, int tiles, int seg_cap = 62) {
   long long g = grid;
   if (U < g) g = U;
-  if (62LL * tiles < g) g = 62LL * tiles;
+  if ((long long)seg_cap * tiles < g) g = (long long)seg_cap * tiles;
   return (int)g;
 }
+// Per GEMM kind: the depth loop's small projection (latency-bound) is split
+// into at most ~4 segments per tile, so its split-K reduction stays short.
+__host__ __device__ inline int gemm_seg_cap(int kind) { return kind == kProj ? 4 : 62; }
 
 // Host-side launch (step.cu).
 cudaError_t launch_step(const StepParams& p, int grid, cudaStream_t stream);
 cudaError_t configure_step_kernel();
 cudaError_t occupancy_per_sm(int* blocks);
 int barriers_per_step(int L);
-int barriers_per_launch(int L, int frames, bool advance);
+int barriers_per_launch(int L, int frames, bool advance, bool depth);
 // Dynamic shared memory layout shared by host checks and the kernel.
 struct SmemLayout {
   int ring_off, ring_bytes;      // GEMM ring / attention K and V tiles (union)

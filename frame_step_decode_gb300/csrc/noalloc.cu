@@ -152,7 +152,7 @@ extern "C" int wave_step_static(const wave_config* cfg, int S_max, int T_max, in
     off[i] = layer_elems;
     layer_elems += n_off[i];
   }
-  int tiles[4], kblocks[4];
+  int tiles[kGemmKinds] = {0}, kblocks[kGemmKinds] = {0};
   tiles[kQKV] = (3 * HD + kTileM - 1) / kTileM;
   kblocks[kQKV] = (d + kKBlk - 1) / kKBlk;
   tiles[kO] = (d + kTileM - 1) / kTileM;

@@ -231,12 +231,14 @@ __device__ __forceinline__ void add4(float4& a, const float4& b) {
 }
 // Sum, in segment order, of the float4 at element offsets o0 / o1 of each of
 // a tile's partial slots (the first at `first`, the others at part +
-// seg[1..nseg)); the first three
-// segments' loads in flight together, two more per later pass.
+// seg[1..nseg)); the first five segments' loads in flight together, four
+// more per later pass.  kOne: the tile has one segment (no partner slots).
+template <bool kOne>
 __device__ __forceinline__ void seg_sum2(const float* first, const float* part, const long long* seg,
                                          int nseg, size_t o0, size_t o1, float4& a0, float4& a1) {
   a0 = ld4cg(first + o0);
   a1 = ld4cg(first + o1);
+  if (kOne) return;
   for (int j = 1; j < nseg; j += 2) {
     float4 t0[2], t1[2];
 #pragma unroll
@@ -253,13 +255,14 @@ __device__ __forceinline__ void seg_sum2(const float* first, const float* part, 
       }
   }
 }
-// The same for four offsets (gate and up rows of two items), one segment per
-// later pass.
+// The same for four offsets (four items, or gate and up rows of two items),
+// two more segments per later pass.
+template <bool kOne>
 __device__ __forceinline__ void seg_sum4(const float* first, const float* part, const long long* seg,
                                          int nseg, size_t o0, size_t o1, size_t o2, size_t o3,
                                          float4& a0, float4& a1, float4& a2, float4& a3) {
-  const float* b = first;
-  a0 = ld4cg(b + o0); a1 = ld4cg(b + o1); a2 = ld4cg(b + o2); a3 = ld4cg(b + o3);
+  a0 = ld4cg(first + o0); a1 = ld4cg(first + o1); a2 = ld4cg(first + o2); a3 = ld4cg(first + o3);
+  if (kOne) return;
   for (int j = 1; j < nseg; ++j) {
     const float* bk = part + seg[j];
     const float4 t0 = ld4cg(bk + o0), t1 = ld4cg(bk + o1), t2 = ld4cg(bk + o2), t3 = ld4cg(bk + o3);
@@ -298,6 +301,7 @@ __device__ __forceinline__ void resid_store(const StepParams& p, int s, int n, f
 // slot at `first`, the others at part + seg[1..nseg), summed in segment order.
 // Flat float4 items over the valid columns; this thread takes items et,
 // et + step, ...
+template <bool kOne>
 __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t, const float* first,
                                          const long long* seg, int nseg, int et, int step,
                                          bool last_layer, int frame) {
@@ -311,9 +315,34 @@ __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t
       const size_t o0 = (size_t)(i0 >> 4) * kTileM + 4 * (i0 & 15);
       const size_t o1 = two ? (size_t)(i1 >> 4) * kTileM + 4 * (i1 & 15) : o0;
       float4 g0, g1, u0, u1;
-      seg_sum4(first, p.gemm_part, seg, nseg, o0, o1, o0 + 64, o1 + 64, g0, g1, u0, u1);
+      seg_sum4<kOne>(first, p.gemm_part, seg, nseg, o0, o1, o0 + 64, o1 + 64, g0, g1, u0, u1);
       swiglu_store(p.u + (size_t)(i0 >> 4) * F, t * 64 + 4 * (i0 & 15), F, g0, u0);
       if (two) swiglu_store(p.u + (size_t)(i1 >> 4) * F, t * 64 + 4 * (i1 & 15), F, g1, u1);
+    }
+  } else if (kind == kProj) {
+    // item (s, r4): the next frame's input x[frame][s][n..n+3] in bf16; four items per pass
+    const int d = p.d, items = p.S * 32;
+#pragma unroll 1
+    for (int i0 = et; i0 < items; i0 += 4 * step) {
+      int iv[4];
+      size_t ov[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        iv[k] = (i0 + k * step < items) ? i0 + k * step : i0;
+        ov[k] = (size_t)(iv[k] >> 5) * kTileM + 4 * (iv[k] & 31);
+      }
+      float4 a[4];
+      seg_sum4<kOne>(first, p.gemm_part, seg, nseg, ov[0], ov[1], ov[2], ov[3], a[0], a[1], a[2], a[3]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int n = t * kTileM + 4 * (iv[k] & 31);
+        if ((k == 0 || iv[k] != i0) && n < d) {
+          uint2 o;
+          o.x = (uint32_t)f32_to_bf16(a[k].x) | ((uint32_t)f32_to_bf16(a[k].y) << 16);
+          o.y = (uint32_t)f32_to_bf16(a[k].z) | ((uint32_t)f32_to_bf16(a[k].w) << 16);
+          *(uint2*)(p.x_chain + ((size_t)frame * p.S + (iv[k] >> 5)) * d + n) = o;
+        }
+      }
     }
   } else if (kind == kQKV) {
     // item (s, r4): output rows 4r4..4r4+3 of the tile; four items per pass
@@ -328,7 +357,7 @@ __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t
         ov[k] = (size_t)(iv[k] >> 5) * kTileM + 4 * (iv[k] & 31);
       }
       float4 a[4];
-      seg_sum4(first, p.gemm_part, seg, nseg, ov[0], ov[1], ov[2], ov[3], a[0], a[1], a[2], a[3]);
+      seg_sum4<kOne>(first, p.gemm_part, seg, nseg, ov[0], ov[1], ov[2], ov[3], a[0], a[1], a[2], a[3]);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int n = t * kTileM + 4 * (iv[k] & 31);
@@ -348,7 +377,7 @@ __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t
       const float4 old0 = (n0 < d) ? __ldcg((const float4*)(p.resid + (size_t)s0 * d + n0)) : z;
       const float4 old1 = (n1 < d) ? __ldcg((const float4*)(p.resid + (size_t)s1 * d + n1)) : z;
       float4 a0, a1;
-      seg_sum2(first, p.gemm_part, seg, nseg, (size_t)s0 * kTileM + (n0 - t * kTileM),
+      seg_sum2<kOne>(first, p.gemm_part, seg, nseg, (size_t)s0 * kTileM + (n0 - t * kTileM),
                (size_t)s1 * kTileM + (n1 - t * kTileM), a0, a1);
       if (n0 < d) resid_store(p, s0, n0, old0, a0, last_layer, frame);
       if (two && n1 < d) resid_store(p, s1, n1, old1, a1, last_layer, frame);
@@ -363,7 +392,7 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
   // Split over min(grid, units, 62 * tiles) CTAs: every participating span is
   // non-empty, the owners of a tile's units are consecutive CTAs, and a tile
   // has at most 64 segments.
-  const int G = stream_k_ctas(gridDim.x, U, p.tiles[kind]), cta = blockIdx.x;
+  const int G = stream_k_ctas(gridDim.x, U, p.tiles[kind], gemm_seg_cap(kind)), cta = blockIdx.x;
   const Span sp = (cta < G) ? cta_span(U, G, cta) : Span{0, 0};
   const int S_pad = p.S_pad, nst = p.nstage;
   const uint32_t b_bytes = (uint32_t)S_pad * 128u;
@@ -375,6 +404,8 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
       const uint64_t pol = policy_evict_first();
       const CUtensorMap* wm = &p.tm_w[kind];
       const CUtensorMap* xm = &p.tm_x[kind];
+      // the projection between chained frames reads the previous frame's y rows
+      const int xrow0 = (kind == kProj) ? (c.frame - 1) * p.S : 0;
       bool fail = false;
       for (long long u = sp.u0; !fail && u < sp.u1;) {
         const int t = (int)(u / KB);
@@ -395,7 +426,7 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
           } else {
             tma_load_3d(a, wm, kb * kKBlk, t * kTileM, layer, fb, pol);
           }
-          tma_load_2d(a + 16384, xm, kb * kKBlk, 0, fb);
+          tma_load_2d(a + 16384, xm, kb * kKBlk, xrow0, fb);
           c.ring_it++;
         }
         u = e;
@@ -477,7 +508,7 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
       if (nseg == 1) {
         // whole tile here: the four epilogue warps finish it from the slot
         named_bar(1, 128);
-        finish_tile(p, kind, t, slot, nullptr, 1, threadIdx.x - 64, 128, last_layer, c.frame);
+        finish_tile<true>(p, kind, t, slot, nullptr, 1, threadIdx.x - 64, 128, last_layer, c.frame);
       } else {
         // split tile: count this segment in
         __threadfence();
@@ -527,7 +558,7 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
   }
   __syncthreads();
   if (!*misc_word(c, 3)) return;
-  finish_tile(p, kind, t, p.gemm_part + seg[0], seg, nseg, idx * kThreads + threadIdx.x, m * kThreads,
+  finish_tile<false>(p, kind, t, p.gemm_part + seg[0], seg, nseg, idx * kThreads + threadIdx.x, m * kThreads,
               last_layer, c.frame);
   __syncthreads();
   // the last final contributor to finish re-arms the tile's counters
@@ -1127,7 +1158,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     mbar_init(bar_drain(c), 1);
     mbar_init(bar_norm(c), 1);
     fence_mbar_init();
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < (p.depth ? kGemmKinds : 4); ++i) {
       prefetch_tmap(&p.tm_w[i]);
       prefetch_tmap(&p.tm_x[i]);
     }
@@ -1150,6 +1181,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     // the previous frame's last reductions (resid, y) finish before this
     // frame's prologue reloads the residual
     if (f > 0 && !(ok = grid_sync(p, c))) break;
+    // chained frames: this frame's input is the previous output projected
+    if (f > 0 && p.depth) {
+      gemm_phase(p, c, kProj, 0, false);
+      if (!(ok = grid_sync(p, c))) break;
+    }
     // phase 0: work list, counter reset, residual and first norm
     for (int i = blockIdx.x * kThreads + threadIdx.x; i < kCounterWords; i += gridDim.x * kThreads)
       p.tile_cnt[i] = 0;
@@ -1222,8 +1258,8 @@ cudaError_t launch_step(const StepParams& p, int grid, cudaStream_t stream) {
 }
 
 int barriers_per_step(int L) { return 8 * L - 1; }
-int barriers_per_launch(int L, int frames, bool advance) {
-  return frames * (8 * L - 1) + (frames - 1) + (advance ? 1 : 0);
+int barriers_per_launch(int L, int frames, bool advance, bool depth) {
+  return frames * (8 * L - 1) + (frames - 1) * (depth ? 2 : 1) + (advance ? 1 : 0);
 }
 
 cudaError_t occupancy_per_sm(int* blocks) {

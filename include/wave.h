@@ -141,7 +141,26 @@ int wave_beat(wave_t* h, int S, int frames, const void* weights, uint8_t* kv_fp8
               int32_t* positions, int advance, const void* x, void* y, void* stream);
 
 /*
- * Synchronise the stream of the last wave_step / wave_beat on this handle, then return
+ * The inner depth loop: `steps` dependent steps of the model in one launch
+ * (the narilabs blog, "Predictable GPU execution": the Depformer's
+ * autoregressive loop of 8 steps per frame, captured with the frame).  Step
+ * k runs every session at depth position k over a depth cache of T_max >=
+ * steps slots (kv_fp8 / kv_scales as in wave_step; slots 0..k-1 hold this
+ * call's earlier steps, so nothing carries over from an earlier call), and
+ * takes as input
+ *     x_0 = x0,   x_k = bf16(W_p y_{k-1})  (fp32 accumulation),
+ * W_p a bf16 [d][d] matrix (row n = output n, 16-byte aligned).  x0 is bf16
+ * [S][d]; xs is caller scratch bf16 [steps][S][d] that receives x_0..x_{k}
+ * (xs may equal x0); y is bf16 [steps][S][d], the outputs of every step.
+ * 1 <= steps <= min(64, T_max).  Errors and asynchrony as wave_step (it
+ * enqueues one device-to-device copy of x0 before the launch).  The wave_debug_*
+ * hooks apply to single-frame launches only.
+ */
+int wave_depth(wave_t* h, int S, int steps, const void* weights, const void* w_proj, uint8_t* kv_fp8,
+               float* kv_scales, const void* x0, void* xs, void* y, void* stream);
+
+/*
+ * Synchronise the stream of the last launch on this handle, then return
  * and clear the device error word: WAVE_OK, WAVE_ETIMEOUT (a device wait gave
  * up; the step's outputs are undefined, the GPU context stays usable) or
  * WAVE_EPOS.  Returns WAVE_ECUDA if the synchronisation itself failed.

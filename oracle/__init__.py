@@ -64,6 +64,8 @@ def lib():
         L.oracle_attention_head.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp]
         L.oracle_silu.argtypes = [f64]
         L.oracle_silu.restype = f64
+        L.oracle_proj.argtypes = [vp, i32, i32, vp, vp]
+        L.oracle_proj.restype = None
         L.oracle_step.argtypes = [ctypes.POINTER(OracleCfg), i32, vp, i32, vp, vp, vp, vp, vp, vp,
                                   i32, vp]
         L.oracle_step.restype = i32
@@ -190,3 +192,33 @@ def prefill_history(w, sessions, pos, poison: bool = True):
                     kv[l, which, j, :, P:, :] = 0x7F
                     sc[l, which, j, :, P:] = np.nan
     return kv, sc
+
+
+def proj(w, wp: np.ndarray, y: np.ndarray) -> np.ndarray:
+    """x_next = bf16(W_p y) per row (fp64 accumulation), bf16 bits [n][d]."""
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    wp = np.ascontiguousarray(wp, dtype=np.uint16)
+    out = np.empty_like(y)
+    lib().oracle_proj(_p(wp), w.d_model, y.shape[0], _p(y), _p(out))
+    return out
+
+
+def depth_loop(w, weights: np.ndarray, wp: np.ndarray, x0: np.ndarray, steps: int):
+    """The inner depth loop for n sessions: step k at depth position k over a
+    fresh depth cache (every slot it reads was written earlier in the loop),
+    x_0 = x0 and x_k = bf16(W_p y_{k-1}).  Returns (y bits [steps][n][d],
+    y_exact fp64 [steps][n][d], x bits [steps][n][d])."""
+    n = x0.shape[0]
+    L, H, T, D = w.n_layers, w.n_heads, w.T_max, w.head_dim
+    kv = np.full((L, 2, n, H, T, D), 0x7F, dtype=np.uint8)   # NaN codes: never read before written
+    sc = np.full((L, 2, n, H, T), np.nan, dtype=np.float32)
+    ys = np.empty((steps, n, w.d_model), dtype=np.uint16)
+    ye = np.empty((steps, n, w.d_model), dtype=np.float64)
+    xs = np.empty((steps, n, w.d_model), dtype=np.uint16)
+    x = np.ascontiguousarray(x0, dtype=np.uint16)
+    for k in range(steps):
+        xs[k] = x
+        y, y_exact, _ = step(w, weights, kv, sc, np.full(n, k, dtype=np.int32), x)
+        ys[k], ye[k] = y, y_exact
+        x = proj(w, wp, y)
+    return ys, ye, xs

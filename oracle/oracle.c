@@ -297,3 +297,21 @@ int oracle_step(const oracle_cfg* c, int T_max, const uint16_t* weights, int n, 
   free(r); free(xn); free(qkv); free(att); free(tmp); free(u); free(row);
   return 0;
 }
+
+/*
+ * The projection between the dependent steps of the inner depth loop (the
+ * narilabs blog, "Predictable GPU execution": the Depformer's 8-step
+ * autoregressive loop per frame): x_next[s] = bf16(W_p y[s]), W_p a bf16
+ * [d][d] matrix (row = output), fp64 accumulation, one rounding to bf16.
+ */
+void oracle_proj(const uint16_t* wp, int d, int n, const uint16_t* y, uint16_t* x_next) {
+  double* a = (double*)malloc(sizeof(double) * d);
+  double* o = (double*)malloc(sizeof(double) * d);
+  for (int s = 0; s < n; ++s) {
+    for (int i = 0; i < d; ++i) a[i] = oracle_bf16_to_double(y[(int64_t)s * d + i]);
+    oracle_matvec(wp, d, d, a, o);
+    for (int i = 0; i < d; ++i) x_next[(int64_t)s * d + i] = oracle_double_to_bf16(o[i]);
+  }
+  free(a);
+  free(o);
+}

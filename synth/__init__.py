@@ -28,7 +28,7 @@ _HOST_SO = os.path.join(HERE, "libsynth.so")
 _GPU_SO = os.path.join(HERE, "libsynth_gpu.so")
 
 SEED_WEIGHTS, SEED_X, SEED_POS, SEED_KV = 1, 2, 3, 4
-STREAM_X, STREAM_POS = 1, 2
+STREAM_X, STREAM_POS, STREAM_PROJ = 1, 2, 3
 WEIGHT_STREAM_BASE, KV_STREAM_BASE = 1000, 2000
 M_WQKV, M_WO, M_WGU, M_WDOWN = 1, 2, 4, 5
 WEIGHT_STD = 0.02
@@ -204,6 +204,18 @@ def x_bf16(w: Workload, S: int | None = None) -> np.ndarray:
     return normal_bf16(SEED_X, STREAM_X, 0, S * w.d_model, 1.0).reshape(S, w.d_model)
 
 
+def proj_std(w: Workload) -> float:
+    """Scale of the depth loop's projection W_p: N(0, 1/d), so that W_p y keeps
+    the scale of y (1/sqrt(d) is a power of two for the d used here)."""
+    return 1.0 / float(np.sqrt(w.d_model))
+
+
+def proj_host(w: Workload) -> np.ndarray:
+    """W_p [d][d] as bf16 bit patterns (row = output)."""
+    d = w.d_model
+    return normal_bf16(SEED_WEIGHTS, STREAM_PROJ, 0, d * d, proj_std(w)).reshape(d, d)
+
+
 def weights_host(w: Workload) -> np.ndarray:
     """The whole bf16 weight blob (uint16 bit patterns) on the host."""
     lay = layer_layout(w)
@@ -285,4 +297,11 @@ def kv_raw_device(w: Workload, layer: int, which: int, s0: int, ns: int, t_count
 
 def x_device(w: Workload, S: int, out_ptr: int, stream_ptr: int) -> None:
     _check(gpu_lib().synth_gpu_normal_bf16(SEED_X, STREAM_X, 0, S * w.d_model, 1.0, out_ptr,
+                                           stream_ptr), "synth_gpu_normal_bf16")
+
+
+def proj_device(w: Workload, out_ptr: int, stream_ptr: int) -> None:
+    """Device twin of proj_host (d*d bf16 at out_ptr)."""
+    d = w.d_model
+    _check(gpu_lib().synth_gpu_normal_bf16(SEED_WEIGHTS, STREAM_PROJ, 0, d * d, proj_std(w), out_ptr,
                                            stream_ptr), "synth_gpu_normal_bf16")
