@@ -379,7 +379,7 @@ def run_phases(args, w):
     for l in range(w.n_layers):
         if l > 0:
             names.append("norm1")
-        names += ["qkv", "attn", "merge", "o", "norm2", "gu", "down"]
+        names += ["qkv", "attn"] + (["merge"] if -(-w.T_max // 32) > 16 else []) + ["o", "norm2", "gu", "down"]
     d, HD, F = w.d_model, w.HD, w.ffn
     wbytes = {"qkv": 3 * HD * d * 2, "o": d * HD * 2, "gu": 2 * F * d * 2, "down": d * F * 2}
     kvb = sum(2 * w.n_heads * (int(q) + 1) * (w.head_dim + 4) for q in pos_h)

@@ -414,6 +414,7 @@ static int launch_frames(wave_t* h, int S, int frames, const void* weights, uint
   p.n_frames = frames;
   p.pos_advance = advance;
   p.depth = x_chain ? 1 : 0;
+  p.merge = needs_merge(h->T_max) ? 1 : 0;
   p.x_chain = x_chain;
   p.resid = h->resid;
   p.xn = h->xn;
@@ -533,5 +534,5 @@ extern "C" int wave_debug_arrival_times(wave_t* h, long long* dst) {
 extern "C" int wave_grid_size(wave_t* h) { return h ? h->grid : WAVE_EINVAL; }
 
 extern "C" int wave_barriers_per_step(wave_t* h) {
-  return h ? barriers_per_step(h->cfg.n_layers) : WAVE_EINVAL;
+  return h ? barriers_per_step(h->cfg.n_layers, h->T_max) : WAVE_EINVAL;
 }

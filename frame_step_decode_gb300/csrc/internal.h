@@ -46,6 +46,7 @@ struct StepParams {
   int n_frames;          // frames run back to back in this launch (positions + f in frame f)
   int32_t* pos_advance;  // if set: positions += n_frames at the end (empty slots stay empty)
   int depth;             // frames chained: x[f] = bf16(W_p y[f-1]) (the kProj GEMM) before frame f
+  int merge;             // 0 when no (session, head) can need more than one piece (T_max small)
   uint16_t* x_chain;     // where those inputs go (the buffer x points at)
   // workspace
   float* resid;          // [S_pad_max][d] fp32 residual stream
@@ -92,8 +93,11 @@ __host__ __device__ inline int gemm_seg_cap(int kind) { return kind == kProj ? 4
 cudaError_t launch_step(const StepParams& p, int grid, cudaStream_t stream);
 cudaError_t configure_step_kernel();
 cudaError_t occupancy_per_sm(int* blocks);
-int barriers_per_step(int L);
-int barriers_per_launch(int L, int frames, bool advance, bool depth);
+// Whether a history of T_max slots can be cut into several attention pieces
+// (and so needs the merge phase).
+inline bool needs_merge(int T_max) { return (T_max + kChunk - 1) / kChunk > kPieceChunks; }
+int barriers_per_step(int L, int T_max);
+int barriers_per_launch(int L, int T_max, int frames, bool advance, bool depth);
 // Dynamic shared memory layout shared by host checks and the kernel.
 struct SmemLayout {
   int ring_off, ring_bytes;      // GEMM ring / attention K and V tiles (union)

@@ -187,6 +187,7 @@ extern "C" int wave_step_static(const wave_config* cfg, int S_max, int T_max, in
   StepParams p;
   memset(&p, 0, sizeof(p));
   p.n_frames = 1;
+  p.merge = needs_merge(T_max) ? 1 : 0;
   p.resid = (float*)(base + offs[0]);
   p.xn = (uint16_t*)(base + offs[1]);
   p.qkv = (float*)(base + offs[2]);

@@ -1203,8 +1203,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       if (!(ok = grid_sync(p, c))) break;
       if (p.D == 128) attention_phase<128>(p, c, l); else attention_phase<64>(p, c, l);
       if (!(ok = grid_sync(p, c))) break;
-      if (p.D == 128) merge_phase<128>(p, c); else merge_phase<64>(p, c);
-      if (!(ok = grid_sync(p, c))) break;
+      if (p.merge) {  // only when some (session, head) is cut into several pieces
+        if (p.D == 128) merge_phase<128>(p, c); else merge_phase<64>(p, c);
+        if (!(ok = grid_sync(p, c))) break;
+      }
       gemm_phase(p, c, kO, l, false);
       if (!(ok = grid_sync(p, c))) break;
       const bool nok2 = norm_phase(p, c, wl + p.off_g_mlp, false);
@@ -1257,9 +1259,9 @@ cudaError_t launch_step(const StepParams& p, int grid, cudaStream_t stream) {
                                      (size_t)smem_layout().total, stream);
 }
 
-int barriers_per_step(int L) { return 8 * L - 1; }
-int barriers_per_launch(int L, int frames, bool advance, bool depth) {
-  return frames * (8 * L - 1) + (frames - 1) * (depth ? 2 : 1) + (advance ? 1 : 0);
+int barriers_per_step(int L, int T_max) { return (needs_merge(T_max) ? 8 : 7) * L - 1; }
+int barriers_per_launch(int L, int T_max, int frames, bool advance, bool depth) {
+  return frames * barriers_per_step(L, T_max) + (frames - 1) * (depth ? 2 : 1) + (advance ? 1 : 0);
 }
 
 cudaError_t occupancy_per_sm(int* blocks) {
