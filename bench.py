@@ -534,7 +534,7 @@ def run_depth(args):
                       "ms_per_frame": ms, "p50_ms": statistics.median(per), "p99_ms": float(np.percentile(per, 99)),
                       "us_per_step": 1000.0 * ms / steps, "algorithmic_bytes": b, "achieved_gbs": gbs,
                       "peak_gbs": peak, "peak_kind": peak_kind, "frac": gbs / peak,
-                      "barriers_per_frame": steps * (8 * L - 1) + 2 * (steps - 1), "steps": args.steps}),
+                      "barriers_per_frame": steps * (7 * L - 1) + 2 * (steps - 1), "steps": args.steps}),
           flush=True)
     wave.close()
 
