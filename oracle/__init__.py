@@ -64,6 +64,13 @@ def lib():
         L.oracle_attention_head.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp]
         L.oracle_silu.argtypes = [f64]
         L.oracle_silu.restype = f64
+        L.oracle_hybrid_step.argtypes = [ctypes.POINTER(OracleHybridCfg), i32, vp, i32, vp, vp, vp, vp, vp,
+                                         vp, vp]
+        L.oracle_hybrid_step.restype = i32
+        L.oracle_ssm_mixer.argtypes = [ctypes.POINTER(OracleHybridCfg), vp, vp, vp, vp, vp, vp, vp]
+        L.oracle_ssm_mixer.restype = None
+        L.oracle_hybrid_layer_offset.argtypes = [ctypes.POINTER(OracleHybridCfg), i32]
+        L.oracle_hybrid_layer_offset.restype = i64
         L.oracle_proj.argtypes = [vp, i32, i32, vp, vp]
         L.oracle_proj.restype = None
         L.oracle_step.argtypes = [ctypes.POINTER(OracleCfg), i32, vp, i32, vp, vp, vp, vp, vp, vp,
@@ -135,6 +142,18 @@ def attention_head(q, kc, ks, vc, vs, pos: int) -> np.ndarray:
     o = np.empty(D, dtype=np.float64)
     lib().oracle_attention_head(_p(q), _p(kc), _p(ks), _p(vc), _p(vs), pos, D, _p(o))
     return o
+
+
+class OracleHybridCfg(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("d_model", ctypes.c_int), ("attn_every", ctypes.c_int),
+                ("n_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("ssm_heads", ctypes.c_int),
+                ("ssm_head_dim", ctypes.c_int), ("ssm_state", ctypes.c_int), ("rms_eps", ctypes.c_float),
+                ("rope_base", ctypes.c_float)]
+
+
+def hybrid_cfg_of(w) -> OracleHybridCfg:
+    return OracleHybridCfg(w.n_layers, w.d_model, w.attn_every, w.n_heads, w.head_dim, w.ssm_heads,
+                           w.ssm_head_dim, w.ssm_state, w.rms_eps, w.rope_base)
 
 
 def cfg_of(w) -> OracleCfg:
@@ -222,3 +241,50 @@ def depth_loop(w, weights: np.ndarray, wp: np.ndarray, x0: np.ndarray, steps: in
         ys[k], ye[k] = y, y_exact
         x = proj(w, wp, y)
     return ys, ye, xs
+
+
+def hybrid_prefill(w, sessions, pos, poison: bool = True):
+    """The hybrid step's state for the listed sessions: the attention layers'
+    FP8 history (as prefill_history, over the attention layers alone) and
+    the Mamba layers' fp32 state from the shared generator.  Returns (kv,
+    scales, state [Lm][n][Hs][P][N])."""
+    import synth
+    kv, sc = prefill_history(w.attention_view(), sessions, np.maximum(np.asarray(pos), 0), poison=poison)
+    n = len(sessions)
+    st = np.empty((w.n_mamba, n, w.ssm_heads, w.ssm_head_dim, w.ssm_state), dtype=np.float32)
+    for lm in range(w.n_mamba):
+        for j, s in enumerate(sessions):
+            st[lm, j] = synth.hybrid_state_host(w, lm, int(s), 1)[0]
+    return kv, sc, st
+
+
+def hybrid_step(w, weights: np.ndarray, kv: np.ndarray, kv_scales: np.ndarray, state: np.ndarray,
+                pos: np.ndarray, x: np.ndarray):
+    """One frame of the hybrid model for n sessions (see oracle.c): kv,
+    kv_scales and state are updated in place.  Returns (y bits, y_exact)."""
+    n = pos.size
+    pos = np.ascontiguousarray(pos, dtype=np.int32)
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    assert kv.flags["C_CONTIGUOUS"] and kv_scales.flags["C_CONTIGUOUS"] and state.flags["C_CONTIGUOUS"]
+    y = np.empty((n, w.d_model), dtype=np.uint16)
+    y_exact = np.empty((n, w.d_model), dtype=np.float64)
+    c = hybrid_cfg_of(w)
+    rc = lib().oracle_hybrid_step(ctypes.byref(c), w.T_max, _p(weights), n, _p(kv), _p(kv_scales), _p(state),
+                                  _p(pos), _p(x), _p(y), _p(y_exact))
+    if rc != 0:
+        raise ValueError(f"oracle_hybrid_step: position of session {-rc - 1} at or beyond T_max")
+    return y, y_exact
+
+
+def ssm_mixer(w, w_in: np.ndarray, a_log: np.ndarray, dt_bias: np.ndarray, d_skip: np.ndarray,
+              xn: np.ndarray, state: np.ndarray) -> np.ndarray:
+    """One Mamba2-style mixer for one session (see oracle.c): xn fp64 [d],
+    state fp32 [Hs][P][N] updated in place; returns the gated output
+    (unrounded) [d_i]."""
+    c = hybrid_cfg_of(w)
+    out = np.empty(w.d_inner, dtype=np.float64)
+    xn = np.ascontiguousarray(xn, dtype=np.float64)
+    lib().oracle_ssm_mixer(ctypes.byref(c), _p(np.ascontiguousarray(w_in)), _p(np.ascontiguousarray(a_log)),
+                           _p(np.ascontiguousarray(dt_bias)), _p(np.ascontiguousarray(d_skip)), _p(xn),
+                           _p(state), _p(out))
+    return out

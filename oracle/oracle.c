@@ -315,3 +315,162 @@ void oracle_proj(const uint16_t* wp, int d, int n, const uint16_t* y, uint16_t* 
   free(a);
   free(o);
 }
+
+/* ------------------------------------------------------------------ hybrid
+ * The hybrid recurrent step (BASELINE config 5, the NemotronH-style thinker
+ * of the vllm-omni recipe page, "Summary"; "recurrent_state": "FP32" in the
+ * dotwave.ai profile.json).  The pages give no layer definition; readings:
+ * every layer is a pre-norm residual block without an MLP.  Layer l is an
+ * attention block (the decoder's attention half: RMSNorm, QKV, RoPE, FP8
+ * append, attention, O) when l % attn_every == attn_every - 1, else a
+ * Mamba2-style selective-state block:
+ *   zxbcdt = W_in xn, split [z d_i | x d_i | B N | C N | dt Hs] (one group,
+ *   no conv1d); per head: dt = softplus(dt + dt_bias), A = -exp(A_log),
+ *   a = exp(dt A); per head dim p and state n:
+ *   h[p][n] <- a h[p][n] + dt B[n] x[p]  (stored in fp32: the state is fp32),
+ *   y[p] = sum_n C[n] h[p][n] + D x[p];  out = bf16(y * silu(z));
+ *   r += W_out out.
+ * Blob per layer (bf16, [out][in]): Mamba: g, W_in [2 d_i + 2N + Hs][d],
+ * W_out [d][d_i], A_log [Hs], dt_bias [Hs], D [Hs]; attention: g,
+ * Wqkv [3 H D][d], Wo [d][H D].  Layers in order, each group of attn_every
+ * layers = (attn_every - 1) Mamba layers then one attention layer.
+ */
+typedef struct {
+  int n_layers, d_model, attn_every, n_heads, head_dim, ssm_heads, ssm_head_dim, ssm_state;
+  float rms_eps, rope_base;
+} oracle_hybrid_cfg;
+
+int64_t oracle_hybrid_mamba_elems(const oracle_hybrid_cfg* c) {
+  const int64_t d = c->d_model, di = (int64_t)c->ssm_heads * c->ssm_head_dim;
+  return d + (2 * di + 2 * c->ssm_state + c->ssm_heads) * d + d * di + 3 * (int64_t)c->ssm_heads;
+}
+int64_t oracle_hybrid_attn_elems(const oracle_hybrid_cfg* c) {
+  const int64_t d = c->d_model, HD = (int64_t)c->n_heads * c->head_dim;
+  return d + 3 * HD * d + d * HD;
+}
+int64_t oracle_hybrid_layer_offset(const oracle_hybrid_cfg* c, int l) {
+  const int64_t M = oracle_hybrid_mamba_elems(c), A = oracle_hybrid_attn_elems(c);
+  const int e = c->attn_every;
+  return (int64_t)(l / e) * ((e - 1) * M + A) + (int64_t)(l % e) * M;
+}
+
+static double oracle_softplus(double v) { return v > 0 ? v + log1p(exp(-v)) : log1p(exp(v)); }
+
+/* One Mamba2-style block's mixer for one session: xn (bf16-rounded) in, the
+ * gated output out[d_i] (bf16-rounded) and the state [Hs][P][N] updated. */
+void oracle_ssm_mixer(const oracle_hybrid_cfg* c, const uint16_t* w_in, const uint16_t* a_log,
+                      const uint16_t* dt_bias, const uint16_t* dskip, const double* xn,
+                      float* state, double* out) {
+  const int d = c->d_model, Hs = c->ssm_heads, P = c->ssm_head_dim, N = c->ssm_state;
+  const int di = Hs * P, rows = 2 * di + 2 * N + Hs;
+  double* zx = (double*)malloc(sizeof(double) * rows);
+  oracle_matvec(w_in, rows, d, xn, zx);
+  const double* z = zx;
+  const double* xs = zx + di;
+  const double* B = zx + 2 * di;
+  const double* C = zx + 2 * di + N;
+  const double* dtr = zx + 2 * di + 2 * N;
+  for (int hh = 0; hh < Hs; ++hh) {
+    const double dt = oracle_softplus(dtr[hh] + oracle_bf16_to_double(dt_bias[hh]));
+    const double A = -exp(oracle_bf16_to_double(a_log[hh]));
+    const double a = exp(dt * A);
+    const double Dh = oracle_bf16_to_double(dskip[hh]);
+    for (int p = 0; p < P; ++p) {
+      const double xp = xs[hh * P + p];
+      float* hrow = state + ((int64_t)hh * P + p) * N;
+      double acc = 0.0;
+      for (int n = 0; n < N; ++n) {
+        const float hn = (float)(a * (double)hrow[n] + dt * B[n] * xp);
+        hrow[n] = hn;
+        acc += C[n] * (double)hn;
+      }
+      const double y = acc + Dh * xp;
+      out[hh * P + p] = y * oracle_silu(z[hh * P + p]);
+    }
+  }
+  free(zx);
+}
+
+/*
+ * One frame of the hybrid model for n sessions.  kv / kv_scales hold the
+ * attention layers' histories ([La][2][n][H][T_max][D], La = n_layers /
+ * attn_every), state the Mamba layers' ([Lm][n][Hs][P][N] fp32, Lm = n_layers
+ * - La), both updated in place.  Positions as in oracle_step (negative: an
+ * empty slot, y = x, nothing touched).  Returns 0 or -(s+1).
+ */
+int oracle_hybrid_step(const oracle_hybrid_cfg* c, int T_max, const uint16_t* weights, int n, uint8_t* kv,
+                       float* kv_scales, float* state, const int32_t* pos, const uint16_t* x, uint16_t* y,
+                       double* y_exact) {
+  const int L = c->n_layers, d = c->d_model, H = c->n_heads, D = c->head_dim, e = c->attn_every;
+  const int HD = H * D, Hs = c->ssm_heads, P = c->ssm_head_dim, N = c->ssm_state, di = Hs * P;
+  const int rows_in = 2 * di + 2 * N + Hs;
+  for (int s = 0; s < n; ++s)
+    if (pos[s] >= T_max) return -(s + 1);
+  double* r = (double*)malloc(sizeof(double) * d);
+  double* xn = (double*)malloc(sizeof(double) * d);
+  double* qkv = (double*)malloc(sizeof(double) * 3 * HD);
+  double* att = (double*)malloc(sizeof(double) * (HD > di ? HD : di));
+  double* tmp = (double*)malloc(sizeof(double) * d);
+  float* row = (float*)malloc(sizeof(float) * D);
+  for (int s = 0; s < n; ++s) {
+    const int Pp = pos[s];
+    if (Pp < 0) {
+      for (int i = 0; i < d; ++i) {
+        y[(int64_t)s * d + i] = x[(int64_t)s * d + i];
+        if (y_exact) y_exact[(int64_t)s * d + i] = oracle_bf16_to_double(x[(int64_t)s * d + i]);
+      }
+      continue;
+    }
+    for (int i = 0; i < d; ++i) r[i] = oracle_bf16_to_double(x[(int64_t)s * d + i]);
+    for (int l = 0; l < L; ++l) {
+      const uint16_t* Wl = weights + oracle_hybrid_layer_offset(c, l);
+      oracle_rmsnorm(r, Wl, d, c->rms_eps, xn);
+      for (int i = 0; i < d; ++i) xn[i] = oracle_bf16_round(xn[i]);
+      if (l % e == e - 1) {
+        const int la = l / e;
+        const uint16_t* wqkv = Wl + d;
+        const uint16_t* wo = wqkv + (int64_t)3 * HD * d;
+        oracle_matvec(wqkv, 3 * HD, d, xn, qkv);
+        double* q = qkv;
+        double* k = qkv + HD;
+        double* v = qkv + 2 * HD;
+        for (int h = 0; h < H; ++h) {
+          oracle_rope(q + h * D, D, Pp, c->rope_base);
+          oracle_rope(k + h * D, D, Pp, c->rope_base);
+        }
+        for (int which = 0; which < 2; ++which) {
+          const double* src = which ? v : k;
+          for (int h = 0; h < H; ++h) {
+            const int64_t sh = (((int64_t)la * 2 + which) * n + s) * H + h;
+            for (int i = 0; i < D; ++i) row[i] = (float)src[h * D + i];
+            oracle_quantize_row(row, D, kv + (sh * T_max + Pp) * D, kv_scales + sh * T_max + Pp);
+          }
+        }
+        for (int h = 0; h < H; ++h) {
+          const int64_t shk = (((int64_t)la * 2 + 0) * n + s) * H + h;
+          const int64_t shv = (((int64_t)la * 2 + 1) * n + s) * H + h;
+          oracle_attention_head(q + h * D, kv + shk * T_max * D, kv_scales + shk * T_max,
+                                kv + shv * T_max * D, kv_scales + shv * T_max, Pp, D, att + h * D);
+        }
+        for (int i = 0; i < HD; ++i) att[i] = oracle_bf16_round(att[i]);
+        oracle_matvec(wo, d, HD, att, tmp);
+      } else {
+        const int lm = l - l / e;
+        const uint16_t* w_in = Wl + d;
+        const uint16_t* w_out = w_in + (int64_t)rows_in * d;
+        const uint16_t* a_log = w_out + (int64_t)d * di;
+        float* st = state + ((int64_t)lm * n + s) * (int64_t)Hs * P * N;
+        oracle_ssm_mixer(c, w_in, a_log, a_log + Hs, a_log + 2 * Hs, xn, st, att);
+        for (int i = 0; i < di; ++i) att[i] = oracle_bf16_round(att[i]);
+        oracle_matvec(w_out, d, di, att, tmp);
+      }
+      for (int i = 0; i < d; ++i) r[i] += tmp[i];
+    }
+    for (int i = 0; i < d; ++i) {
+      y[(int64_t)s * d + i] = oracle_double_to_bf16(r[i]);
+      if (y_exact) y_exact[(int64_t)s * d + i] = r[i];
+    }
+  }
+  free(r); free(xn); free(qkv); free(att); free(tmp); free(row);
+  return 0;
+}

@@ -30,7 +30,8 @@ _GPU_SO = os.path.join(HERE, "libsynth_gpu.so")
 SEED_WEIGHTS, SEED_X, SEED_POS, SEED_KV = 1, 2, 3, 4
 STREAM_X, STREAM_POS, STREAM_PROJ = 1, 2, 3
 WEIGHT_STREAM_BASE, KV_STREAM_BASE = 1000, 2000
-M_WQKV, M_WO, M_WGU, M_WDOWN = 1, 2, 4, 5
+M_WQKV, M_WO, M_WGU, M_WDOWN, M_WIN, M_WOUT, M_ALOG = 1, 2, 4, 5, 6, 7, 8
+SEED_STATE = 5
 WEIGHT_STD = 0.02
 
 _G = 0x9E3779B97F4A7C15
@@ -72,6 +73,94 @@ SWEEP_S = (1, 8, 16, 32, 48, 56, 64, 80, 96, 128)
 MID = Workload("mid-3L-d512-h4x128-f1376", 3, 512, 4, 128, 1376, S=19, T_max=320, pos_lo=0, pos_hi=320)
 DEPTH = Workload("depth-6L-d1024-h16x64-f2816", 6, 1024, 16, 64, 2816, S=80, T_max=8, pos_lo=0, pos_hi=8,
                  extra={"depth_steps": 8})
+
+
+@dataclass(frozen=True)
+class HybridWorkload:
+    """Shapes and input recipe of the hybrid recurrent step: every
+    attn_every-th layer an attention block, the others Mamba2-style
+    selective-state blocks (no MLP layers)."""
+    name: str
+    n_layers: int
+    d_model: int
+    attn_every: int
+    n_heads: int
+    head_dim: int
+    ssm_heads: int
+    ssm_head_dim: int
+    ssm_state: int
+    S: int
+    T_max: int
+    pos_lo: int
+    pos_hi: int
+    rms_eps: float = 1e-5
+    rope_base: float = 10000.0
+
+    @property
+    def HD(self) -> int:
+        return self.n_heads * self.head_dim
+
+    @property
+    def d_inner(self) -> int:
+        return self.ssm_heads * self.ssm_head_dim
+
+    @property
+    def in_rows(self) -> int:
+        return 2 * self.d_inner + 2 * self.ssm_state + self.ssm_heads
+
+    @property
+    def n_attn(self) -> int:
+        return self.n_layers // self.attn_every
+
+    @property
+    def n_mamba(self) -> int:
+        return self.n_layers - self.n_attn
+
+    def is_attn(self, l: int) -> bool:
+        return l % self.attn_every == self.attn_every - 1
+
+    def attention_view(self) -> Workload:
+        """The attention layers alone, as a Workload (their K/V history is
+        drawn and quantised exactly like the decoder step's)."""
+        return Workload(self.name + "-attn", self.n_attn, self.d_model, self.n_heads, self.head_dim, 0,
+                        S=self.S, T_max=self.T_max, pos_lo=self.pos_lo, pos_hi=self.pos_hi,
+                        rms_eps=self.rms_eps, rope_base=self.rope_base)
+
+
+HYBRID = HybridWorkload("hybrid-48L-d4096-attn6-h32x128-ssm64x64x128", 48, 4096, 6, 32, 128, 64, 64, 128,
+                        S=56, T_max=1500, pos_lo=0, pos_hi=1500)
+# Parity shape: two groups of three layers (two Mamba blocks, one attention
+# block), ragged S, several state heads.
+HYBRID_SMALL = HybridWorkload("hybrid-6L-d256-attn3-h4x64-ssm4x64x128", 6, 256, 3, 4, 64, 4, 64, 128,
+                              S=5, T_max=64, pos_lo=0, pos_hi=64)
+
+
+def hybrid_layout(w: HybridWorkload) -> dict:
+    """Element counts of one layer of each kind and the offsets inside them.
+
+    Mamba block: g[d], W_in[in_rows][d] (z, x, B, C, dt rows), W_out[d][d_i],
+    A_log[Hs], dt_bias[Hs], D[Hs].  Attention block: g[d], Wqkv[3HD][d],
+    Wo[d][HD].  Group of attn_every layers: (attn_every - 1) Mamba blocks,
+    then one attention block."""
+    d, di, Hs, HD = w.d_model, w.d_inner, w.ssm_heads, w.HD
+    m = {"g": 0, "w_in": d, "w_out": d + w.in_rows * d}
+    m["a_log"] = m["w_out"] + d * di
+    m["dt_bias"] = m["a_log"] + Hs
+    m["d_skip"] = m["dt_bias"] + Hs
+    m["size"] = m["d_skip"] + Hs
+    a = {"g": 0, "wqkv": d, "wo": d + 3 * HD * d}
+    a["size"] = a["wo"] + d * HD
+    return {"mamba": m, "attn": a}
+
+
+def hybrid_layer_offset(w: HybridWorkload, l: int) -> int:
+    lay = hybrid_layout(w)
+    M, A, e = lay["mamba"]["size"], lay["attn"]["size"], w.attn_every
+    return (l // e) * ((e - 1) * M + A) + (l % e) * M
+
+
+def hybrid_weight_elems(w: HybridWorkload) -> int:
+    return hybrid_layer_offset(w, w.n_layers)
 
 
 # ------------------------------------------------------- weight blob layout
@@ -233,6 +322,41 @@ def weights_host(w: Workload) -> np.ndarray:
     return blob
 
 
+def hybrid_weights_host(w: HybridWorkload) -> np.ndarray:
+    """The hybrid model's bf16 blob: matrices ~N(0, 0.02), gains 1.0,
+    A_log ~N(0, 1) (A = -exp(A_log)), dt_bias 0, D 1.0."""
+    lay = hybrid_layout(w)
+    blob = np.empty(hybrid_weight_elems(w), dtype=np.uint16)
+    L = lib()
+    d, di, HD = w.d_model, w.d_inner, w.HD
+    for l in range(w.n_layers):
+        base = hybrid_layer_offset(w, l)
+        L.synth_fill_bf16(d, 1.0, blob[base:].ctypes.data)
+        if w.is_attn(l):
+            a = lay["attn"]
+            for name, m, n in (("wqkv", M_WQKV, 3 * HD * d), ("wo", M_WO, d * HD)):
+                L.synth_normal_bf16(SEED_WEIGHTS, WEIGHT_STREAM_BASE + 16 * l + m, 0, n, WEIGHT_STD,
+                                    blob[base + a[name]:].ctypes.data)
+        else:
+            m_ = lay["mamba"]
+            for name, m, n in (("w_in", M_WIN, w.in_rows * d), ("w_out", M_WOUT, d * di)):
+                L.synth_normal_bf16(SEED_WEIGHTS, WEIGHT_STREAM_BASE + 16 * l + m, 0, n, WEIGHT_STD,
+                                    blob[base + m_[name]:].ctypes.data)
+            L.synth_normal_bf16(SEED_WEIGHTS, WEIGHT_STREAM_BASE + 16 * l + M_ALOG, 0, w.ssm_heads, 1.0,
+                                blob[base + m_["a_log"]:].ctypes.data)
+            L.synth_fill_bf16(w.ssm_heads, 0.0, blob[base + m_["dt_bias"]:].ctypes.data)
+            L.synth_fill_bf16(w.ssm_heads, 1.0, blob[base + m_["d_skip"]:].ctypes.data)
+    return blob
+
+
+def hybrid_state_host(w: HybridWorkload, lm: int, s0: int, ns: int) -> np.ndarray:
+    """Initial fp32 state of Mamba layer lm for sessions s0..s0+ns-1:
+    [ns][Hs][P][N] ~N(0, 1)."""
+    blk = w.ssm_heads * w.ssm_head_dim * w.ssm_state
+    return normal_f32(SEED_STATE, lm, s0 * blk, ns * blk).reshape(ns, w.ssm_heads, w.ssm_head_dim,
+                                                                 w.ssm_state)
+
+
 def kv_raw_host(w: Workload, layer: int, which: int, s0: int, ns: int, t_count: int,
                 out_T: int | None = None) -> np.ndarray:
     """Raw fp32 history values [ns][H][out_T][D] for slots t < t_count."""
@@ -305,3 +429,36 @@ def proj_device(w: Workload, out_ptr: int, stream_ptr: int) -> None:
     d = w.d_model
     _check(gpu_lib().synth_gpu_normal_bf16(SEED_WEIGHTS, STREAM_PROJ, 0, d * d, proj_std(w), out_ptr,
                                            stream_ptr), "synth_gpu_normal_bf16")
+
+
+def hybrid_weights_device(w: HybridWorkload, blob, stream_ptr: int) -> None:
+    """Device twin of hybrid_weights_host (a torch bf16 tensor of
+    hybrid_weight_elems(w) elements, filled in place)."""
+    lay = hybrid_layout(w)
+    G = gpu_lib()
+    d, di, HD = w.d_model, w.d_inner, w.HD
+    out_ptr = blob.data_ptr()
+    for l in range(w.n_layers):
+        base = hybrid_layer_offset(w, l)
+        blob[base: base + d].fill_(1.0)
+        if w.is_attn(l):
+            a = lay["attn"]
+            for name, m, n in (("wqkv", M_WQKV, 3 * HD * d), ("wo", M_WO, d * HD)):
+                _check(G.synth_gpu_normal_bf16(SEED_WEIGHTS, WEIGHT_STREAM_BASE + 16 * l + m, 0, n, WEIGHT_STD,
+                                               out_ptr + 2 * (base + a[name]), stream_ptr), "synth_gpu_normal_bf16")
+        else:
+            m_ = lay["mamba"]
+            for name, m, n in (("w_in", M_WIN, w.in_rows * d), ("w_out", M_WOUT, d * di)):
+                _check(G.synth_gpu_normal_bf16(SEED_WEIGHTS, WEIGHT_STREAM_BASE + 16 * l + m, 0, n, WEIGHT_STD,
+                                               out_ptr + 2 * (base + m_[name]), stream_ptr), "synth_gpu_normal_bf16")
+            _check(G.synth_gpu_normal_bf16(SEED_WEIGHTS, WEIGHT_STREAM_BASE + 16 * l + M_ALOG, 0, w.ssm_heads, 1.0,
+                                           out_ptr + 2 * (base + m_["a_log"]), stream_ptr), "synth_gpu_normal_bf16")
+            blob[base + m_["dt_bias"]: base + m_["dt_bias"] + w.ssm_heads].fill_(0.0)
+            blob[base + m_["d_skip"]: base + m_["d_skip"] + w.ssm_heads].fill_(1.0)
+
+
+def hybrid_state_device(w: HybridWorkload, lm: int, s0: int, ns: int, out_ptr: int, stream_ptr: int) -> None:
+    """Device twin of hybrid_state_host: [ns][Hs][P][N] fp32 at out_ptr."""
+    blk = w.ssm_heads * w.ssm_head_dim * w.ssm_state
+    _check(gpu_lib().synth_gpu_normal_f32(SEED_STATE, lm, s0 * blk, ns * blk, out_ptr, stream_ptr),
+           "synth_gpu_normal_f32")
