@@ -10,6 +10,7 @@ latency and the HBM roofline fraction of the step kernel.
   python bench.py --sweep 1,8,16,32,48,56,64,80,96,128 --steps 20
   python bench.py --beat 2
   python bench.py --depth
+  python bench.py --hybrid
 
 Inputs are seeded and synthetic and are drawn on the device (weights and the
 raw history by the generator's device twin, the history quantised by the
@@ -539,6 +540,76 @@ def run_depth(args):
     wave.close()
 
 
+def hybrid_bytes(w, pos) -> int:
+    """Algorithmic bytes of one hybrid step: the weights once, the attention
+    blocks' history read and the appended slot written, and every selective-
+    state block's fp32 state read and written."""
+    La, H, D = w.n_attn, w.n_heads, w.head_dim
+    weights = 2 * synth.hybrid_weight_elems(w)
+    live = [int(p) for p in pos if p >= 0]
+    kv = sum(La * 2 * H * (p + 1) * (D + 4) for p in live) + La * 2 * len(live) * H * (D + 4)
+    state = 2 * w.n_mamba * len(live) * w.ssm_heads * w.ssm_head_dim * w.ssm_state * 4
+    return weights + kv + state
+
+
+def run_hybrid(args):
+    """The hybrid recurrent step (48 layers: selective-state blocks with an
+    attention block every sixth layer), S = 56: per-step CUDA events, p50/p99,
+    session-frames/s and the HBM fraction of its algorithmic bytes."""
+    import torch
+    import frame_step_decode_gb300 as fsd
+    w = synth.HYBRID
+    S = w.S
+    aw = w.attention_view()
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    La, H, T, D = w.n_attn, w.n_heads, w.T_max, w.head_dim
+    weights = torch.empty(synth.hybrid_weight_elems(w), dtype=torch.bfloat16, device=device)
+    synth.hybrid_weights_device(w, weights, stream.cuda_stream)
+    kv = torch.empty((La, 2, S, H, T, D), dtype=torch.uint8, device=device)
+    sc = torch.empty((La, 2, S, H, T), dtype=torch.float32, device=device)
+    raw = torch.empty((S, H, T, D), dtype=torch.float32, device=device)
+    for l in range(La):
+        for which in range(2):
+            synth.kv_raw_device(aw, l, which, 0, S, T, raw.data_ptr(), T, stream.cuda_stream)
+            fsd.kv_quantize(raw, kv[l, which], sc[l, which])
+    del raw
+    state = torch.empty((w.n_mamba, S, w.ssm_heads, w.ssm_head_dim, w.ssm_state), dtype=torch.float32,
+                        device=device)
+    for lm in range(w.n_mamba):
+        synth.hybrid_state_device(w, lm, 0, S, state[lm].data_ptr(), stream.cuda_stream)
+    pos_h = synth.positions(aw, S)
+    pos = torch.from_numpy(pos_h).to(device)
+    x = torch.empty((S, w.d_model), dtype=torch.bfloat16, device=device)
+    synth.x_device(aw, S, x.data_ptr(), stream.cuda_stream)
+    y = torch.empty_like(x)
+    wave = fsd.HybridWave(fsd.WaveHybridConfig.of(w), S, T)
+    for _ in range(max(3, args.warmup)):
+        wave.hybrid_step(S, weights, kv, sc, state, pos, x, y, stream=stream)
+    if wave.status() != fsd.WAVE_OK:
+        raise RuntimeError("warm-up hybrid step failed")
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        ev0[i].record(stream)
+        wave.hybrid_step(S, weights, kv, sc, state, pos, x, y, stream=stream)
+        ev1[i].record(stream)
+    torch.cuda.synchronize()
+    if wave.status() != fsd.WAVE_OK:
+        raise RuntimeError("timed hybrid step failed")
+    per = [ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)]
+    ms = statistics.mean(per)
+    b = hybrid_bytes(w, pos_h)
+    gbs = b / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    print(json.dumps({"hybrid": True, "workload": w.name, "S": S, "metric": METRIC, "value": S / (ms * 1e-3),
+                      "ms_per_step": ms, "p50_ms": statistics.median(per), "p99_ms": float(np.percentile(per, 99)),
+                      "algorithmic_bytes": b, "achieved_gbs": gbs, "peak_gbs": peak, "peak_kind": peak_kind,
+                      "frac": gbs / peak, "frac_of_8000": gbs / 8000.0, "steps": args.steps}), flush=True)
+    wave.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -549,6 +620,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (profiling a small case)")
     ap.add_argument("--tmax", type=int, default=None, help="shorter history (profiling a small case)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--hybrid", action="store_true",
+                    help="time the hybrid recurrent step (48 layers, S = 56)")
     ap.add_argument("--depth", action="store_true",
                     help="time the inner depth loop (8 chained steps of the 6-layer d=1024 model)")
     ap.add_argument("--beat", type=int, default=0,
@@ -566,7 +639,9 @@ def main():
         T = args.tmax or w.T_max
         w = replace(w, n_layers=args.layers or w.n_layers, T_max=T, pos_hi=min(w.pos_hi, T),
                     name=f"{w.name}-L{args.layers or w.n_layers}-T{T}")
-    if args.depth:
+    if args.hybrid:
+        run_hybrid(args)
+    elif args.depth:
         run_depth(args)
     elif args.beat:
         run_beat(args, w)

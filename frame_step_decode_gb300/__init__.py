@@ -27,6 +27,19 @@ class WaveConfig(ctypes.Structure):
         return cls(w.n_layers, w.d_model, w.n_heads, w.head_dim, w.ffn, w.rms_eps, w.rope_base)
 
 
+class WaveHybridConfig(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("d_model", ctypes.c_int), ("attn_every", ctypes.c_int),
+                ("n_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("ssm_heads", ctypes.c_int),
+                ("ssm_head_dim", ctypes.c_int), ("ssm_state", ctypes.c_int), ("rms_eps", ctypes.c_float),
+                ("rope_base", ctypes.c_float)]
+
+    @classmethod
+    def of(cls, w) -> "WaveHybridConfig":
+        """From any object with the hybrid-shape attributes."""
+        return cls(w.n_layers, w.d_model, w.attn_every, w.n_heads, w.head_dim, w.ssm_heads, w.ssm_head_dim,
+                   w.ssm_state, w.rms_eps, w.rope_base)
+
+
 class WaveError(RuntimeError):
     def __init__(self, code: int, what: str):
         super().__init__(f"{what}: {strerror(code)} ({code})")
@@ -37,8 +50,8 @@ _lib = None
 EXPORTS = ("wave_create", "wave_destroy", "wave_weights_bytes", "wave_weight_offset", "wave_step", "wave_beat", "wave_depth",
            "wave_status", "wave_strerror", "wave_kv_quantize", "wave_fp8_encode", "wave_step_static",
            "wave_set_timeout_ns", "wave_debug_skip_barrier", "wave_debug_dump_kv", "wave_debug_phase_times", "wave_debug_arrival_times",
-           "wave_grid_size",
-           "wave_barriers_per_step")
+           "wave_grid_size", "wave_barriers_per_step", "wave_hybrid_create", "wave_hybrid_step",
+           "wave_hybrid_weights_bytes", "wave_hybrid_layer_offset")
 
 
 def lib() -> ctypes.CDLL:
@@ -63,6 +76,14 @@ def lib() -> ctypes.CDLL:
         L.wave_beat.restype = i32
         L.wave_depth.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         L.wave_depth.restype = i32
+        L.wave_hybrid_create.argtypes = [ctypes.POINTER(WaveHybridConfig), i32, i32, ctypes.POINTER(vp)]
+        L.wave_hybrid_create.restype = i32
+        L.wave_hybrid_step.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.wave_hybrid_step.restype = i32
+        L.wave_hybrid_weights_bytes.argtypes = [ctypes.POINTER(WaveHybridConfig)]
+        L.wave_hybrid_weights_bytes.restype = ctypes.c_size_t
+        L.wave_hybrid_layer_offset.argtypes = [ctypes.POINTER(WaveHybridConfig), i32]
+        L.wave_hybrid_layer_offset.restype = ctypes.c_size_t
         L.wave_status.argtypes = [vp]
         L.wave_status.restype = i32
         L.wave_strerror.argtypes = [i32]
@@ -230,3 +251,33 @@ def fp8_encode(inp, out, stream=None, n: int | None = None) -> None:
     rc = lib().wave_fp8_encode(_ptr(inp), n, _ptr(out), _stream(stream))
     if rc != WAVE_OK:
         raise WaveError(rc, "wave_fp8_encode")
+
+
+class HybridWave(Wave):
+    """A hybrid-step context: wave_hybrid_create / wave_hybrid_step (status,
+    hooks and close as Wave)."""
+
+    def __init__(self, cfg: WaveHybridConfig, S_max: int, T_max: int):
+        self.cfg = cfg
+        self.S_max, self.T_max = S_max, T_max
+        h = ctypes.c_void_p()
+        rc = lib().wave_hybrid_create(ctypes.byref(cfg), S_max, T_max, ctypes.byref(h))
+        if rc != WAVE_OK:
+            raise WaveError(rc, "wave_hybrid_create")
+        self.h = h
+
+    def hybrid_step(self, S, weights, kv, kv_scales, ssm_state, positions, x, y, stream=None,
+                    check=True) -> int:
+        rc = lib().wave_hybrid_step(self.h, S, _ptr(weights), _ptr(kv), _ptr(kv_scales), _ptr(ssm_state),
+                                    _ptr(positions), _ptr(x), _ptr(y), _stream(stream))
+        if check and rc != WAVE_OK:
+            raise WaveError(rc, "wave_hybrid_step")
+        return rc
+
+
+def hybrid_weights_bytes(cfg: WaveHybridConfig) -> int:
+    return lib().wave_hybrid_weights_bytes(ctypes.byref(cfg))
+
+
+def hybrid_layer_offset(cfg: WaveHybridConfig, layer: int) -> int:
+    return lib().wave_hybrid_layer_offset(ctypes.byref(cfg), layer)

@@ -54,6 +54,13 @@ struct wave_ctx {
   float* kv_dump = nullptr;
   long long* phase_ts = nullptr;
   long long* arrive_ts = nullptr;
+  // hybrid model (wave_hybrid_create); cfg then describes its attention layers
+  int hybrid = 0;
+  wave_hybrid_config hcfg;
+  long long hyb_M = 0, hyb_G = 0, hyb_off_w_in = 0, hyb_off_w_out = 0, hyb_off_a_log = 0;
+  long long hyb_off_wqkv = 0, hyb_off_wo = 0;  // inside an attention block
+  float* zx = nullptr;
+  uint16_t* ssm_out = nullptr;
 };
 
 static EncodeTiledFn encode_fn() {
@@ -147,26 +154,47 @@ static int max_segments(long long tiles, long long kb, int grid, int seg_cap) {
   return ms;
 }
 
+static int device_check(int* dev, int* sms) {
+  if (cudaGetDevice(dev) != cudaSuccess) return WAVE_ECUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, *dev) != cudaSuccess) return WAVE_ECUDA;
+  if (prop.major != 10 || prop.minor != 3) return WAVE_EDEVICE;
+  if (!encode_fn()) return WAVE_ECUDA;
+  if (configure_step_kernel() != cudaSuccess) return WAVE_ECUDA;
+  *sms = prop.multiProcessorCount;
+  return WAVE_OK;
+}
+
+static int build_ctx(wave_ctx* h, int S_max, int T_max, int in_rows, int d_inner);
+
 extern "C" int wave_create(const wave_config* cfg, int S_max, int T_max, wave_t** out) {
   if (!out || !shape_ok(cfg) || S_max < 1 || S_max > 128 || T_max < 4 || T_max % 4) return WAVE_EINVAL;
   const long long rows = (long long)cfg->n_layers * 2 * S_max * cfg->n_heads * T_max;
   if (rows >= (1LL << 31) || T_max > 65535 * kChunk) return WAVE_EINVAL;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return WAVE_ECUDA;
-  cudaDeviceProp prop;
-  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return WAVE_ECUDA;
-  if (prop.major != 10 || prop.minor != 3) return WAVE_EDEVICE;
-  if (!encode_fn()) return WAVE_ECUDA;
-  if (configure_step_kernel() != cudaSuccess) return WAVE_ECUDA;
-
+  int dev = 0, sms = 0;
+  int rc = device_check(&dev, &sms);
+  if (rc) return rc;
   wave_ctx* h = new wave_ctx();
   h->cfg = *cfg;
+  h->device = dev;
+  h->grid = sms;
+  layout_offsets(cfg, h->off, &h->layer_elems);
+  rc = build_ctx(h, S_max, T_max, 0, 0);
+  if (rc) {
+    delete h;
+    return rc;
+  }
+  *out = h;
+  return WAVE_OK;
+}
+
+// Tiles, workspace and RoPE table of a handle whose cfg (and, for the hybrid
+// model, hcfg) is set.  On failure nothing stays allocated.
+static int build_ctx(wave_ctx* h, int S_max, int T_max, int in_rows, int d_inner) {
+  const wave_config* cfg = &h->cfg;
   h->S_max = S_max;
   h->S_pad_max = (S_max + 15) / 16 * 16;
   h->T_max = T_max;
-  h->device = dev;
-  h->grid = prop.multiProcessorCount;
-  layout_offsets(cfg, h->off, &h->layer_elems);
   const int d = cfg->d_model, HD = cfg->n_heads * cfg->head_dim, F = cfg->ffn, H = cfg->n_heads,
             D = cfg->head_dim;
   h->tiles[kQKV] = (3 * HD + kTileM - 1) / kTileM;
@@ -175,22 +203,20 @@ extern "C" int wave_create(const wave_config* cfg, int S_max, int T_max, wave_t*
   h->kblocks[kO] = (HD + kKBlk - 1) / kKBlk;
   h->tiles[kGU] = (F + 63) / 64;
   h->kblocks[kGU] = (d + kKBlk - 1) / kKBlk;
-  h->tiles[kDown] = (d + kTileM - 1) / kTileM;
+  h->tiles[kDown] = F ? (d + kTileM - 1) / kTileM : 0;
   h->kblocks[kDown] = (F + kKBlk - 1) / kKBlk;
-  h->tiles[kProj] = (d + kTileM - 1) / kTileM;
+  h->tiles[kProj] = h->hybrid ? 0 : (d + kTileM - 1) / kTileM;
   h->kblocks[kProj] = (d + kKBlk - 1) / kKBlk;
+  h->tiles[kIn] = (in_rows + kTileM - 1) / kTileM;
+  h->kblocks[kIn] = (d + kKBlk - 1) / kKBlk;
+  h->tiles[kOut] = d_inner ? (d + kTileM - 1) / kTileM : 0;
+  h->kblocks[kOut] = (d_inner + kKBlk - 1) / kKBlk;
   int mt = 1;
   for (int k = 0; k < kGemmKinds; ++k) {
-    if (h->tiles[k] > 1024) {
-      delete h;
-      return WAVE_EINVAL;
-    }
+    if (h->tiles[k] > 1024) return WAVE_EINVAL;
     int m = max_tiles_touched(h->tiles[k], h->kblocks[k], h->grid, gemm_seg_cap(k));
     if (m > mt) mt = m;
-    if (max_segments(h->tiles[k], h->kblocks[k], h->grid, gemm_seg_cap(k)) > 64) {  // kMaxSeg
-      delete h;
-      return WAVE_EINVAL;
-    }
+    if (max_segments(h->tiles[k], h->kblocks[k], h->grid, gemm_seg_cap(k)) > 64) return WAVE_EINVAL;
   }
   h->max_tiles_per_cta = mt;
 
@@ -215,17 +241,16 @@ extern "C" int wave_create(const wave_config* cfg, int S_max, int T_max, wave_t*
       {(void**)&h->bar, 16},
       {(void**)&h->err, 16},
       {(void**)&h->zero_pos, (size_t)S_max * 4},
+      {(void**)&h->zx, (size_t)(SP * in_rows * 4)},
+      {(void**)&h->ssm_out, (size_t)(SP * d_inner * 2)},
   };
   size_t total = 0;
   for (auto& pt : parts) total += (pt.bytes + 255) & ~(size_t)255;
-  if (cudaMalloc(&h->ws, total) != cudaSuccess) {
-    delete h;
-    return WAVE_ENOMEM;
-  }
+  if (cudaMalloc(&h->ws, total) != cudaSuccess) return WAVE_ENOMEM;
   h->ws_bytes = total;
   if (cudaMemset(h->ws, 0, total) != cudaSuccess) {
     cudaFree(h->ws);
-    delete h;
+    h->ws = nullptr;
     return WAVE_ECUDA;
   }
   size_t o = 0;
@@ -244,15 +269,93 @@ extern "C" int wave_create(const wave_config* cfg, int S_max, int T_max, wave_t*
   if (cudaMemcpy(h->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) !=
       cudaSuccess) {
     cudaFree(h->ws);
-    delete h;
+    h->ws = nullptr;
     return WAVE_ECUDA;
   }
   // co-residency: one CTA per SM must fit
   int per_sm = 0;
   if (occupancy_per_sm(&per_sm) != cudaSuccess || per_sm < 1) {
     cudaFree(h->ws);
-    delete h;
+    h->ws = nullptr;
     return WAVE_ELAUNCH;
+  }
+  return WAVE_OK;
+}
+
+// ---------------------------------------------------------- hybrid model
+static bool hybrid_ok(const wave_hybrid_config* c) {
+  if (!c) return false;
+  if (c->n_layers < 1 || c->n_layers > 1024 || c->attn_every < 1 || c->n_layers % c->attn_every) return false;
+  if (c->d_model < 64 || c->d_model % 64 || c->d_model > 8192) return false;
+  if (c->head_dim != 64 && c->head_dim != 128) return false;
+  if (c->n_heads < 1 || (c->n_heads * c->head_dim) % 64) return false;
+  if (c->ssm_head_dim != kSsmP || c->ssm_state != kSsmN) return false;
+  if (c->ssm_heads < 4 || c->ssm_heads % 4) return false;
+  if (!(c->rms_eps >= 0.f) || !(c->rope_base > 0.f)) return false;
+  return true;
+}
+
+static void hybrid_layout(const wave_hybrid_config* c, long long* M, long long* A, long long* w_in,
+                          long long* w_out, long long* a_log, long long* wqkv, long long* wo) {
+  const long long d = c->d_model, di = (long long)c->ssm_heads * c->ssm_head_dim;
+  const long long HD = (long long)c->n_heads * c->head_dim;
+  const long long rows = 2 * di + 2 * c->ssm_state + c->ssm_heads;
+  *w_in = d;
+  *w_out = d + rows * d;
+  *a_log = *w_out + d * di;
+  *M = *a_log + (3LL * c->ssm_heads + 7) / 8 * 8;
+  *wqkv = d;
+  *wo = d + 3 * HD * d;
+  *A = *wo + d * HD;
+}
+
+extern "C" size_t wave_hybrid_weights_bytes(const wave_hybrid_config* cfg) {
+  if (!hybrid_ok(cfg)) return 0;
+  long long M, A, a, b, c, q, o;
+  hybrid_layout(cfg, &M, &A, &a, &b, &c, &q, &o);
+  const int e = cfg->attn_every;
+  return (size_t)((cfg->n_layers / e) * ((e - 1) * M + A) * 2);
+}
+
+extern "C" size_t wave_hybrid_layer_offset(const wave_hybrid_config* cfg, int layer) {
+  if (!hybrid_ok(cfg) || layer < 0 || layer > cfg->n_layers) return (size_t)-1;
+  long long M, A, a, b, c, q, o;
+  hybrid_layout(cfg, &M, &A, &a, &b, &c, &q, &o);
+  return (size_t)(hyb_layer_offset(M, (cfg->attn_every - 1) * M + A, cfg->attn_every, layer) * 2);
+}
+
+extern "C" int wave_hybrid_create(const wave_hybrid_config* hc, int S_max, int T_max, wave_t** out) {
+  if (!out || !hybrid_ok(hc) || S_max < 1 || S_max > 128 || T_max < 4 || T_max % 4) return WAVE_EINVAL;
+  const int La = hc->n_layers / hc->attn_every;
+  const long long rows = (long long)La * 2 * S_max * hc->n_heads * T_max;
+  if (rows >= (1LL << 31) || T_max > 65535 * kChunk) return WAVE_EINVAL;
+  int dev = 0, sms = 0;
+  int rc = device_check(&dev, &sms);
+  if (rc) return rc;
+  wave_ctx* h = new wave_ctx();
+  h->hybrid = 1;
+  h->hcfg = *hc;
+  // cfg describes the attention layers (their history and maps)
+  h->cfg.n_layers = La;
+  h->cfg.d_model = hc->d_model;
+  h->cfg.n_heads = hc->n_heads;
+  h->cfg.head_dim = hc->head_dim;
+  h->cfg.ffn = 0;
+  h->cfg.rms_eps = hc->rms_eps;
+  h->cfg.rope_base = hc->rope_base;
+  h->device = dev;
+  h->grid = sms;
+  long long A;
+  hybrid_layout(hc, &h->hyb_M, &A, &h->hyb_off_w_in, &h->hyb_off_w_out, &h->hyb_off_a_log, &h->hyb_off_wqkv,
+                &h->hyb_off_wo);
+  h->hyb_G = (hc->attn_every - 1) * h->hyb_M + A;
+  for (int i = 0; i < 6; ++i) h->off[i] = 0;
+  h->layer_elems = h->hyb_G;
+  const int di = hc->ssm_heads * hc->ssm_head_dim;
+  rc = build_ctx(h, S_max, T_max, 2 * di + 2 * hc->ssm_state + hc->ssm_heads, di);
+  if (rc) {
+    delete h;
+    return rc;
   }
   *out = h;
   return WAVE_OK;
@@ -273,7 +376,44 @@ static bool enc(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* base, co
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+static int encode_hybrid_weight_maps(wave_ctx* h, const void* weights) {
+  const wave_hybrid_config& c = h->hcfg;
+  const cuuint64_t d = c.d_model, HD = (cuuint64_t)c.n_heads * c.head_dim;
+  const cuuint64_t di = (cuuint64_t)c.ssm_heads * c.ssm_head_dim;
+  const cuuint64_t rows = 2 * di + 2 * c.ssm_state + c.ssm_heads;
+  const cuuint64_t e = c.attn_every, groups = c.n_layers / c.attn_every;
+  const cuuint64_t M2 = (cuuint64_t)h->hyb_M * 2, G2 = (cuuint64_t)h->hyb_G * 2;
+  char* base = (char*)weights;
+  char* attn0 = base + (e - 1) * M2;  // the first attention block
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  {  // attention Wqkv [La][3HD][d], one attention block per group
+    cuuint64_t dims[3] = {d, 3 * HD, groups}, str[2] = {d * 2, G2};
+    cuuint32_t box[3] = {kKBlk, kTileM, 1};
+    if (!enc(&h->tm_w[kQKV], BF, 3, attn0 + h->hyb_off_wqkv * 2, dims, str, box, SW)) return WAVE_ECUDA;
+  }
+  {  // attention Wo [La][d][HD]
+    cuuint64_t dims[3] = {HD, d, groups}, str[2] = {HD * 2, G2};
+    cuuint32_t box[3] = {kKBlk, kTileM, 1};
+    if (!enc(&h->tm_w[kO], BF, 3, attn0 + h->hyb_off_wo * 2, dims, str, box, SW)) return WAVE_ECUDA;
+  }
+  if (e > 1) {
+    {  // W_in [group][place][rows][d]
+      cuuint64_t dims[4] = {d, rows, e - 1, groups}, str[3] = {d * 2, M2, G2};
+      cuuint32_t box[4] = {kKBlk, kTileM, 1, 1};
+      if (!enc(&h->tm_w[kIn], BF, 4, base + h->hyb_off_w_in * 2, dims, str, box, SW)) return WAVE_ECUDA;
+    }
+    {  // W_out [group][place][d][d_inner]
+      cuuint64_t dims[4] = {di, d, e - 1, groups}, str[3] = {di * 2, M2, G2};
+      cuuint32_t box[4] = {kKBlk, kTileM, 1, 1};
+      if (!enc(&h->tm_w[kOut], BF, 4, base + h->hyb_off_w_out * 2, dims, str, box, SW)) return WAVE_ECUDA;
+    }
+  }
+  return WAVE_OK;
+}
+
 static int encode_weight_maps(wave_ctx* h, const void* weights) {
+  if (h->hybrid) return encode_hybrid_weight_maps(h, weights);
   const wave_config& c = h->cfg;
   const cuuint64_t d = c.d_model, HD = (cuuint64_t)c.n_heads * c.head_dim, F = c.ffn, L = c.n_layers;
   const cuuint64_t ls = (cuuint64_t)h->layer_elems * 2;  // layer stride in bytes
@@ -319,9 +459,15 @@ static int encode_act_maps(wave_ctx* h, int S_pad) {
     cuuint64_t dims[2] = {HD, R}, str[1] = {HD * 2};
     if (!enc(&h->tm_x[kO], BF, 2, h->attn, dims, str, box, SW)) return WAVE_ECUDA;
   }
-  {
+  if (F) {
     cuuint64_t dims[2] = {F, R}, str[1] = {F * 2};
     if (!enc(&h->tm_x[kDown], BF, 2, h->u, dims, str, box, SW)) return WAVE_ECUDA;
+  }
+  if (h->hybrid) {
+    h->tm_x[kIn] = h->tm_x[kQKV];
+    const cuuint64_t di = (cuuint64_t)h->hcfg.ssm_heads * h->hcfg.ssm_head_dim;
+    cuuint64_t dims[2] = {di, R}, str[1] = {di * 2};
+    if (!enc(&h->tm_x[kOut], BF, 2, h->ssm_out, dims, str, box, SW)) return WAVE_ECUDA;
   }
   return WAVE_OK;
 }
@@ -350,7 +496,7 @@ static int encode_kv_map(wave_ctx* h, uint8_t* kv, float* scales) {
 // advanced by `frames` on the device at the end when `advance` is set.
 static int launch_frames(wave_t* h, int S, int frames, const void* weights, uint8_t* kv_fp8,
                          float* kv_scales, const int32_t* positions, int32_t* advance, const void* x,
-                         void* y, void* stream, uint16_t* x_chain = nullptr) {
+                         void* y, void* stream, uint16_t* x_chain = nullptr, float* ssm_state = nullptr) {
   if (!h || !weights || !kv_fp8 || !kv_scales || !positions || !x || !y) return WAVE_EINVAL;
   if (S < 1 || S > h->S_max || frames < 1 || frames > kMaxFrames) return WAVE_EINVAL;
   if (((uintptr_t)weights & 15) || ((uintptr_t)kv_fp8 & 15) || ((uintptr_t)kv_scales & 15) ||
@@ -415,6 +561,26 @@ static int launch_frames(wave_t* h, int S, int frames, const void* weights, uint
   p.pos_advance = advance;
   p.depth = x_chain ? 1 : 0;
   p.merge = needs_merge(h->T_max) ? 1 : 0;
+  if (h->hybrid) {
+    const wave_hybrid_config& hc = h->hcfg;
+    p.hybrid = 1;
+    p.L = hc.n_layers;  // the layer loop; cfg.n_layers counts the attention layers
+    p.attn_every = hc.attn_every;
+    p.ssm_heads = hc.ssm_heads;
+    p.d_inner = hc.ssm_heads * hc.ssm_head_dim;
+    p.in_rows = 2 * p.d_inner + 2 * hc.ssm_state + hc.ssm_heads;
+    p.hyb_M = h->hyb_M;
+    p.hyb_G = h->hyb_G;
+    p.hyb_off_w_in = h->hyb_off_w_in;
+    p.hyb_off_a_log = h->hyb_off_a_log;
+    p.zx = h->zx;
+    p.ssm_out = h->ssm_out;
+    p.ssm_state = ssm_state;
+    // the output projection's L2 prefetch walks attention blocks: one per group
+    p.layer_elems = h->hyb_G;
+    p.off_wo = (hc.attn_every - 1) * h->hyb_M + h->hyb_off_wo;
+    p.off_g_attn = 0;
+  }
   p.x_chain = x_chain;
   p.resid = h->resid;
   p.xn = h->xn;
@@ -449,13 +615,14 @@ static int launch_frames(wave_t* h, int S, int frames, const void* weights, uint
 
 extern "C" int wave_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8, float* kv_scales,
                          const int32_t* positions, const void* x, void* y, void* stream) {
+  if (h && h->hybrid) return WAVE_EINVAL;
   return launch_frames(h, S, 1, weights, kv_fp8, kv_scales, positions, nullptr, x, y, stream);
 }
 
 extern "C" int wave_depth(wave_t* h, int S, int steps, const void* weights, const void* w_proj,
                           uint8_t* kv_fp8, float* kv_scales, const void* x0, void* xs, void* y,
                           void* stream) {
-  if (!h || !w_proj || !x0 || !xs || !y) return WAVE_EINVAL;
+  if (!h || h->hybrid || !w_proj || !x0 || !xs || !y) return WAVE_EINVAL;
   if (S < 1 || S > h->S_max || steps < 1 || steps > kMaxFrames || steps > h->T_max) return WAVE_EINVAL;
   if (((uintptr_t)w_proj & 15) || ((uintptr_t)x0 & 15) || ((uintptr_t)xs & 15) || ((uintptr_t)y & 15))
     return WAVE_EINVAL;
@@ -482,9 +649,18 @@ extern "C" int wave_depth(wave_t* h, int S, int steps, const void* weights, cons
                        (uint16_t*)xs);
 }
 
+extern "C" int wave_hybrid_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8, float* kv_scales,
+                                float* ssm_state, const int32_t* positions, const void* x, void* y,
+                                void* stream) {
+  if (!h || !h->hybrid || !ssm_state || ((uintptr_t)ssm_state & 15)) return WAVE_EINVAL;
+  return launch_frames(h, S, 1, weights, kv_fp8, kv_scales, positions, nullptr, x, y, stream, nullptr,
+                       ssm_state);
+}
+
 extern "C" int wave_beat(wave_t* h, int S, int frames, const void* weights, uint8_t* kv_fp8,
                          float* kv_scales, int32_t* positions, int advance, const void* x, void* y,
                          void* stream) {
+  if (h && h->hybrid) return WAVE_EINVAL;
   return launch_frames(h, S, frames, weights, kv_fp8, kv_scales, positions, advance ? positions : nullptr,
                        x, y, stream);
 }
@@ -534,5 +710,7 @@ extern "C" int wave_debug_arrival_times(wave_t* h, long long* dst) {
 extern "C" int wave_grid_size(wave_t* h) { return h ? h->grid : WAVE_EINVAL; }
 
 extern "C" int wave_barriers_per_step(wave_t* h) {
-  return h ? barriers_per_step(h->cfg.n_layers, h->T_max) : WAVE_EINVAL;
+  if (!h) return WAVE_EINVAL;
+  return h->hybrid ? hybrid_barriers_per_step(h->hcfg.n_layers, h->hcfg.attn_every, h->T_max)
+                   : barriers_per_step(h->cfg.n_layers, h->T_max);
 }

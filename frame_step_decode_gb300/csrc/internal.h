@@ -21,12 +21,17 @@ enum ErrBits : int { kErrTimeout = 1, kErrPos = 2 };
 
 // Device error word bits -> public codes live in api.cu.
 
-enum GemmKind : int { kQKV = 0, kO = 1, kGU = 2, kDown = 3, kProj = 4 };
-constexpr int kGemmKinds = 5;
+enum GemmKind : int { kQKV = 0, kO = 1, kGU = 2, kDown = 3, kProj = 4, kIn = 5, kOut = 6 };
+constexpr int kGemmKinds = 7;
+// Selective-state blocks of the hybrid model: head dim and state size the
+// state phase is laid out for (8 warps x 8 rows, 32 lanes x 4 states).
+constexpr int kSsmP = 64;
+constexpr int kSsmN = 128;
+constexpr int kSsmStages = 4;  // state blocks in flight per CTA (32 KB each)
 
 struct StepParams {
   CUtensorMap tm_w[kGemmKinds];  // weights of the projections (see GemmKind)
-  CUtensorMap tm_x[kGemmKinds];  // their activation inputs: xn, attn, xn, u, y (box rows = S_pad)
+  CUtensorMap tm_x[kGemmKinds];  // their activation inputs: xn, attn, xn, u, y, xn, ssm_out (box rows = S_pad)
   CUtensorMap tm_kv;     // the FP8 history as [D][S_max*H*T_max][K|V][L]: one box = a chunk's K and V
   CUtensorMap tm_sc;     // the scales as [S_max*H*T_max][K|V][L]: one box = a chunk's K and V scales
   // shape
@@ -48,6 +53,13 @@ struct StepParams {
   int depth;             // frames chained: x[f] = bf16(W_p y[f-1]) (the kProj GEMM) before frame f
   int merge;             // 0 when no (session, head) can need more than one piece (T_max small)
   uint16_t* x_chain;     // where those inputs go (the buffer x points at)
+  // hybrid model (selective-state blocks with an attention block every attn_every layers)
+  int hybrid, attn_every, ssm_heads, d_inner, in_rows;
+  long long hyb_M, hyb_G;      // elements of one Mamba block and of one group of attn_every layers
+  long long hyb_off_w_in, hyb_off_a_log;  // inside a Mamba block
+  float* zx;             // [S_pad][in_rows] fp32 in-projection output (z | x | B | C | dt)
+  uint16_t* ssm_out;     // [S_pad][d_inner] bf16 gated mixer output
+  float* ssm_state;      // caller's [Lm][S_max][Hs][P][N] fp32 state
   // workspace
   float* resid;          // [S_pad_max][d] fp32 residual stream
   uint16_t* xn;          // [S_pad_max][d] bf16 normed input of QKV / gate-up
@@ -88,6 +100,11 @@ __host__ __device__ inline int stream_k_ctas(int grid, long long U, int tiles, i
 // Per GEMM kind: the depth loop's small projection (latency-bound) is split
 // into at most ~4 segments per tile, so its split-K reduction stays short.
 __host__ __device__ inline int gemm_seg_cap(int kind) { return kind == kProj ? 4 : 62; }
+// Element offset of layer l in a hybrid blob (groups of attn_every layers:
+// attn_every - 1 Mamba blocks, then the attention block).
+__host__ __device__ inline long long hyb_layer_offset(long long M, long long G, int e, int l) {
+  return (long long)(l / e) * G + (long long)(l % e) * M;
+}
 
 // Host-side launch (step.cu).
 cudaError_t launch_step(const StepParams& p, int grid, cudaStream_t stream);
@@ -98,6 +115,7 @@ cudaError_t occupancy_per_sm(int* blocks);
 inline bool needs_merge(int T_max) { return (T_max + kChunk - 1) / kChunk > kPieceChunks; }
 int barriers_per_step(int L, int T_max);
 int barriers_per_launch(int L, int T_max, int frames, bool advance, bool depth);
+int hybrid_barriers_per_step(int L, int attn_every, int T_max);
 // Dynamic shared memory layout shared by host checks and the kernel.
 struct SmemLayout {
   int ring_off, ring_bytes;      // GEMM ring / attention K and V tiles (union)

@@ -43,6 +43,7 @@ struct Ctx {
   uint32_t att_it;      // attention chunk counter (per warp)
   uint32_t norm_it;     // norm-row copy counter (all threads)
   int frame;            // frame of the launch being computed
+  uint32_t ssm_it;      // state-block copy counter (all threads)
   SmemLayout lay;
 };
 
@@ -60,7 +61,10 @@ __device__ __forceinline__ uint32_t bar_drain(const Ctx& c) {
 __device__ __forceinline__ uint32_t bar_norm(const Ctx& c) {
   return c.sbase + c.lay.bar_off + 168 + 8 * kWarps * kAttStages;
 }
-static_assert(176 + 8 * kWarps * kAttStages <= 64 * 8, "mbarrier slots exceed their region");
+__device__ __forceinline__ uint32_t bar_ssm(const Ctx& c, int i) {
+  return c.sbase + c.lay.bar_off + 176 + 8 * kWarps * kAttStages + 8 * i;
+}
+static_assert(176 + 8 * kWarps * kAttStages + 8 * kSsmStages <= 64 * 8, "mbarrier slots exceed their region");
 __device__ __forceinline__ volatile int* misc_word(const Ctx& c, int i) {
   return (volatile int*)(c.smem + c.lay.misc_off + 4 * i);
 }
@@ -344,9 +348,10 @@ __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t
         }
       }
     }
-  } else if (kind == kQKV) {
-    // item (s, r4): output rows 4r4..4r4+3 of the tile; four items per pass
-    const int N = 3 * p.HD, items = p.S * 32;
+  } else if (kind == kQKV || kind == kIn) {
+    // item (s, r4): output rows 4r4..4r4+3 of the tile (fp32); four items per pass
+    const int N = (kind == kQKV) ? 3 * p.HD : p.in_rows, items = p.S * 32;
+    float* dst = (kind == kQKV) ? p.qkv : p.zx;
 #pragma unroll 1
     for (int i0 = et; i0 < items; i0 += 4 * step) {
       int iv[4];
@@ -361,7 +366,7 @@ __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int n = t * kTileM + 4 * (iv[k] & 31);
-        if ((k == 0 || iv[k] != i0) && n < N) *(float4*)(p.qkv + (size_t)(iv[k] >> 5) * N + n) = a[k];
+        if ((k == 0 || iv[k] != i0) && n < N) *(float4*)(dst + (size_t)(iv[k] >> 5) * N + n) = a[k];
       }
     }
   } else {
@@ -423,6 +428,8 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
           if (kind == kGU) {
             tma_load_4d(a, wm, kb * kKBlk, t * 64, 0, layer, fb, pol);
             tma_load_4d(a + 8192, wm, kb * kKBlk, t * 64, 1, layer, fb, pol);
+          } else if (kind == kIn || kind == kOut) {  // hybrid Mamba blocks: (place in group, group)
+            tma_load_4d(a, wm, kb * kKBlk, t * kTileM, layer % p.attn_every, layer / p.attn_every, fb, pol);
           } else {
             tma_load_3d(a, wm, kb * kKBlk, t * kTileM, layer, fb, pol);
           }
@@ -945,6 +952,98 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
   }
 }
 
+// ------------------------------------------------------- selective state
+// The Mamba2-style mixer of hybrid layer l (its lm-th selective-state block)
+// for every (session, head): dt = softplus(dt + dt_bias), a = exp(-exp(A_log)
+// dt); per head dim p and state n: h = a h + dt x_p B_n (the fp32 state,
+// written back in place); y_p = sum_n C_n h + D x_p; out = bf16(y_p silu(z_p)).
+// (session, head) items are dealt round-robin to CTAs; a CTA's 8 warps work
+// on one item together (warp w: rows 8w..8w+7, lane: states 4 lane..+3)
+// while thread 0 keeps kSsmStages of its next items' 32 KB state blocks in
+// flight by bulk copy.  An empty slot (negative position) leaves its state
+// alone and writes zeros.  Returns false if a copy wait gave up.
+__device__ __forceinline__ bool ssm_phase(const StepParams& p, Ctx& c, int lm, int l) {
+  static_assert(kWarps * 8 == kSsmP && 32 * 4 == kSsmN, "state phase layout");
+  constexpr uint32_t kBlk = kSsmP * kSsmN * 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hs = p.ssm_heads, di = p.d_inner, R = p.in_rows, N = kSsmN;
+  const int items = p.S * Hs;
+  const int my = (items > (int)blockIdx.x) ? (items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const uint16_t* prm = p.weights + hyb_layer_offset(p.hyb_M, p.hyb_G, p.attn_every, l) + p.hyb_off_a_log;
+  float* state_l = p.ssm_state + (size_t)lm * p.S_max * Hs * kSsmP * kSsmN;
+  const uint32_t ring_s = c.sbase + c.lay.ring_off;
+  const float* ring = (const float*)(c.smem + c.lay.ring_off);
+  auto issue = [&](int k) {  // thread 0
+    const int i = (int)blockIdx.x + k * (int)gridDim.x, s = i / Hs;
+    const uint32_t st = (c.ssm_it + (uint32_t)k) % kSsmStages, b = bar_ssm(c, st);
+    if (p.pos[s] < 0) {
+      mbar_arrive(b);  // nothing to copy for an empty slot
+    } else {
+      mbar_arrive_expect_tx(b, kBlk);
+      bulk_load(ring_s + st * kBlk, state_l + (size_t)i * kSsmP * kSsmN, kBlk, b);
+    }
+  };
+  if (threadIdx.x == 0)
+    for (int k = 0; k < min(my, kSsmStages); ++k) issue(k);
+  for (int k = 0; k < my; ++k) {
+    const int i = (int)blockIdx.x + k * (int)gridDim.x, s = i / Hs, hh = i - s * Hs;
+    const uint32_t st = (c.ssm_it + (uint32_t)k) % kSsmStages;
+    if (threadIdx.x == 0) {
+      const bool ok0 = mbar_wait(bar_ssm(c, st), ((c.ssm_it + (uint32_t)k) / kSsmStages) & 1u, p.timeout_ns, p.err);
+      if (!ok0) set_err(p, kErrTimeout);
+      *misc_word(c, 7) = ok0 ? 1 : 0;
+    }
+    __syncthreads();
+    if (!*misc_word(c, 7)) return false;
+    uint16_t* orow = p.ssm_out + (size_t)s * di + hh * kSsmP + warp * 8;
+    if (p.pos[s] < 0) {
+      if (lane < 8) orow[lane] = 0;
+    } else {
+      const float* zrow = p.zx + (size_t)s * R;
+      const float dtr = zrow[2 * di + 2 * N + hh] + bf16_to_f32(prm[Hs + hh]);
+      const float dt = dtr > 0.f ? dtr + log1pf(expf(-dtr)) : log1pf(expf(dtr));
+      const float a = expf(-expf(bf16_to_f32(prm[hh])) * dt);
+      const float Dh = bf16_to_f32(prm[2 * Hs + hh]);
+      const float4 B4 = *(const float4*)(zrow + 2 * di + 4 * lane);
+      const float4 C4 = *(const float4*)(zrow + 2 * di + N + 4 * lane);
+      const float* blk = ring + st * (kBlk / 4);
+      float* gst = state_l + (size_t)i * kSsmP * kSsmN;
+      float yv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int pr = warp * 8 + j;
+        const float tx = dt * zrow[di + hh * kSsmP + pr];
+        float4 h = *(const float4*)(blk + pr * N + 4 * lane);
+        h.x = fmaf(a, h.x, tx * B4.x);
+        h.y = fmaf(a, h.y, tx * B4.y);
+        h.z = fmaf(a, h.z, tx * B4.z);
+        h.w = fmaf(a, h.w, tx * B4.w);
+        *(float4*)(gst + pr * N + 4 * lane) = h;
+        yv[j] = C4.x * h.x + C4.y * h.y + C4.z * h.z + C4.w * h.w;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) yv[j] += __shfl_xor_sync(0xffffffffu, yv[j], o);
+      if (lane < 8) {
+        float yj = yv[0];
+#pragma unroll
+        for (int j = 1; j < 8; ++j)
+          if (lane == j) yj = yv[j];
+        const int pr = warp * 8 + lane;
+        const float xp = zrow[di + hh * kSsmP + pr], zp = zrow[hh * kSsmP + pr];
+        const float yp = yj + Dh * xp;
+        orow[lane] = f32_to_bf16(yp * zp / (1.0f + expf(-zp)));
+      }
+    }
+    fence_proxy_async_smem();  // this stage's reads come before its next copy
+    __syncthreads();
+    if (threadIdx.x == 0 && k + kSsmStages < my) issue(k + kSsmStages);
+  }
+  c.ssm_it += (uint32_t)my;
+  return true;
+}
+
 // --------------------------------------------------------------- merge
 // Combine the split-T partials of every (session, head) cut into several
 // pieces, in piece order: M = max m_i, L = sum l_i 2^(m_i - M),
@@ -1128,6 +1227,9 @@ __device__ void build_pieces(const StepParams& p, Ctx& c) {
 }
 
 // ------------------------------------------------------------------ kernel
+// kHybrid selects the hybrid model's layer loop at compile time, so that each
+// model's kernel is register-allocated for its own phases only.
+template <bool kHybrid>
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepParams p) {
   extern __shared__ uint8_t smem_raw[];
   Ctx c;
@@ -1142,6 +1244,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   c.bar_index = 0;
   c.ring_it = c.acc_it = c.att_it = c.norm_it = 0;
   c.frame = 0;
+  c.ssm_it = 0;
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
@@ -1157,6 +1260,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       for (int st = 0; st < kAttStages; ++st) mbar_init(bar_att(c, w, st), 1);
     mbar_init(bar_drain(c), 1);
     mbar_init(bar_norm(c), 1);
+    for (int i = 0; i < kSsmStages; ++i) mbar_init(bar_ssm(c, i), 1);
     fence_mbar_init();
     for (int i = 0; i < (p.depth ? kGemmKinds : 4); ++i) {
       prefetch_tmap(&p.tm_w[i]);
@@ -1182,9 +1286,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     // frame's prologue reloads the residual
     if (f > 0 && !(ok = grid_sync(p, c))) break;
     // chained frames: this frame's input is the previous output projected
-    if (f > 0 && p.depth) {
-      gemm_phase(p, c, kProj, 0, false);
-      if (!(ok = grid_sync(p, c))) break;
+    if constexpr (!kHybrid) {
+      if (f > 0 && p.depth) {
+        gemm_phase(p, c, kProj, 0, false);
+        if (!(ok = grid_sync(p, c))) break;
+      }
     }
     // phase 0: work list, counter reset, residual and first norm
     for (int i = blockIdx.x * kThreads + threadIdx.x; i < kCounterWords; i += gridDim.x * kThreads)
@@ -1194,27 +1300,44 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     if (!(ok = grid_sync(p, c) && n0)) break;
 
     for (int l = 0; ok && l < p.L; ++l) {
-      const uint16_t* wl = p.weights + (size_t)l * p.layer_elems;
+      // decoder layer: attention half + MLP half; hybrid model: an attention
+      // block every attn_every layers, selective-state blocks otherwise, no MLP
+      constexpr bool hyb = kHybrid;
+      const int e = hyb ? p.attn_every : 1;
+      const bool attn_layer = !hyb || (l % e == e - 1);
+      const int li = (hyb && attn_layer) ? l / e : l;  // attention weights / history index
+      const bool last = (l == p.L - 1);
+      const uint16_t* wl = hyb ? p.weights + hyb_layer_offset(p.hyb_M, p.hyb_G, e, l)
+                               : p.weights + (size_t)l * p.layer_elems;
       if (l > 0) {
         const bool nok = norm_phase(p, c, wl + p.off_g_attn, false);
         if (!(ok = grid_sync(p, c) && nok)) break;
       }
-      gemm_phase(p, c, kQKV, l, false);
+      // the block's input projection: QKV, or the selective-state in-projection
+      gemm_phase(p, c, attn_layer ? kQKV : kIn, li, false);
       if (!(ok = grid_sync(p, c))) break;
-      if (p.D == 128) attention_phase<128>(p, c, l); else attention_phase<64>(p, c, l);
-      if (!(ok = grid_sync(p, c))) break;
-      if (p.merge) {  // only when some (session, head) is cut into several pieces
-        if (p.D == 128) merge_phase<128>(p, c); else merge_phase<64>(p, c);
+      if (attn_layer) {
+        if (p.D == 128) attention_phase<128>(p, c, li); else attention_phase<64>(p, c, li);
         if (!(ok = grid_sync(p, c))) break;
+        if (p.merge) {  // only when some (session, head) is cut into several pieces
+          if (p.D == 128) merge_phase<128>(p, c); else merge_phase<64>(p, c);
+          if (!(ok = grid_sync(p, c))) break;
+        }
+      } else if constexpr (kHybrid) {
+        const bool sok = ssm_phase(p, c, l - l / e, l);
+        if (!(ok = grid_sync(p, c) && sok)) break;
       }
-      gemm_phase(p, c, kO, l, false);
-      if (!(ok = grid_sync(p, c))) break;
-      const bool nok2 = norm_phase(p, c, wl + p.off_g_mlp, false);
-      if (!(ok = grid_sync(p, c) && nok2)) break;
-      gemm_phase(p, c, kGU, l, false);
-      if (!(ok = grid_sync(p, c))) break;
-      gemm_phase(p, c, kDown, l, l == p.L - 1);
-      if (l < p.L - 1 && !(ok = grid_sync(p, c))) break;
+      // and its output projection + residual: O, or the selective-state out-projection
+      gemm_phase(p, c, attn_layer ? kO : kOut, li, hyb && last);
+      if constexpr (!kHybrid) {
+        if (!(ok = grid_sync(p, c))) break;
+        const bool nok2 = norm_phase(p, c, wl + p.off_g_mlp, false);
+        if (!(ok = grid_sync(p, c) && nok2)) break;
+        gemm_phase(p, c, kGU, l, false);
+        if (!(ok = grid_sync(p, c))) break;
+        gemm_phase(p, c, kDown, l, last);
+      }
+      if (!last && !(ok = grid_sync(p, c))) break;
     }
   }
   // rolling positions: every frame has read them; advance once all are done
@@ -1249,24 +1372,43 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 }
 
 cudaError_t configure_step_kernel() {
-  return cudaFuncSetAttribute(step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(step_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_layout().total);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(step_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               smem_layout().total);
 }
 
 cudaError_t launch_step(const StepParams& p, int grid, cudaStream_t stream) {
   void* args[] = {(void*)&p};
-  return cudaLaunchCooperativeKernel((const void*)step_kernel, dim3(grid), dim3(kThreads), args,
-                                     (size_t)smem_layout().total, stream);
+  const void* fn = p.hybrid ? (const void*)step_kernel<true> : (const void*)step_kernel<false>;
+  return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), args, (size_t)smem_layout().total,
+                                     stream);
 }
 
 int barriers_per_step(int L, int T_max) { return (needs_merge(T_max) ? 8 : 7) * L - 1; }
+int hybrid_barriers_per_step(int L, int attn_every, int T_max) {
+  int n = 1;  // prologue
+  for (int l = 0; l < L; ++l) {
+    n += (l > 0) ? 1 : 0;                                                       // norm
+    n += (l % attn_every == attn_every - 1) ? (needs_merge(T_max) ? 3 : 2) : 2;  // phases before the last
+    n += (l < L - 1) ? 1 : 0;                                                   // after the last
+  }
+  return n;
+}
 int barriers_per_launch(int L, int T_max, int frames, bool advance, bool depth) {
   return frames * barriers_per_step(L, T_max) + (frames - 1) * (depth ? 2 : 1) + (advance ? 1 : 0);
 }
 
 cudaError_t occupancy_per_sm(int* blocks) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel, kThreads,
-                                                       (size_t)smem_layout().total);
+  int a = 0, b = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, step_kernel<false>, kThreads,
+                                                                (size_t)smem_layout().total);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, step_kernel<true>, kThreads,
+                                                    (size_t)smem_layout().total);
+  *blocks = a < b ? a : b;
+  return e;
 }
 
 }  // namespace wave

@@ -160,6 +160,51 @@ int wave_depth(wave_t* h, int S, int steps, const void* weights, const void* w_p
                float* kv_scales, const void* x0, void* xs, void* y, void* stream);
 
 /*
+ * The hybrid recurrent step (BASELINE-style config: the NemotronH-style
+ * thinker of the vllm-omni recipe page, "Summary", whose recurrent state is
+ * FP32 per the dotwave.ai profile.json): n_layers pre-norm residual blocks
+ * without MLPs; layer l is an attention block (RMSNorm, QKV, RoPE, FP8 K/V
+ * append, attention over the history, O; as wave_step's attention half) when
+ * l % attn_every == attn_every - 1, else a Mamba2-style selective-state
+ * block: zxbcdt = W_in xn split [z d_i | x d_i | B N | C N | dt Hs] (one
+ * group, no conv1d); per head dt = softplus(dt + dt_bias), a = exp(-exp(A_log)
+ * dt); per head dim p and state n: h = a h + dt x_p B_n (fp32 state, in
+ * place), y_p = sum_n C_n h + D x_p; r += W_out bf16(y silu(z)).
+ * Constraints: n_layers % attn_every == 0, ssm_head_dim 64, ssm_state 128,
+ * ssm_heads a multiple of 4, the attention shapes of wave_config.
+ */
+typedef struct {
+  int n_layers, d_model, attn_every;  /* layers; width; an attention block every attn_every layers */
+  int n_heads, head_dim;              /* attention blocks (head_dim 64 or 128) */
+  int ssm_heads, ssm_head_dim, ssm_state;
+  float rms_eps, rope_base;
+} wave_hybrid_config;
+
+/* Bytes of the hybrid bf16 weight blob and of the start of layer `layer`
+ * (layer == n_layers gives the total).  Per layer, [out][in] matrices:
+ * selective-state block: g[d], W_in[2 d_i + 2 N + Hs][d] (z, x, B, C, dt
+ * rows), W_out[d][d_i], A_log[Hs], dt_bias[Hs], D[Hs] (this last block padded
+ * to 8 elements); attention block: g[d], Wqkv[3 H D][d], Wo[d][H D].  Groups
+ * of attn_every layers: (attn_every - 1) selective-state blocks, then one
+ * attention block.  0 / (size_t)-1 for an invalid config or layer. */
+size_t wave_hybrid_weights_bytes(const wave_hybrid_config* cfg);
+size_t wave_hybrid_layer_offset(const wave_hybrid_config* cfg, int layer);
+
+/* A handle for the hybrid step (the attention blocks' history as in
+ * wave_create, with n_layers / attn_every layers).  Release with
+ * wave_destroy.  wave_step / wave_beat / wave_depth refuse a hybrid handle. */
+int wave_hybrid_create(const wave_hybrid_config* cfg, int S_max, int T_max, wave_t** out);
+
+/* One frame of the hybrid model for sessions 0..S-1.  kv_fp8 / kv_scales:
+ * the attention blocks' history ([La][2][S_max][H][T_max][D], La = n_layers /
+ * attn_every; as wave_step).  ssm_state: fp32 [Lm][S_max][Hs][64][128]
+ * (Lm = n_layers - La), 16-byte aligned, read and written in place; an empty
+ * slot's (negative position) state is not touched.  Other arguments, errors
+ * and asynchrony as wave_step. */
+int wave_hybrid_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8, float* kv_scales,
+                     float* ssm_state, const int32_t* positions, const void* x, void* y, void* stream);
+
+/*
  * Synchronise the stream of the last launch on this handle, then return
  * and clear the device error word: WAVE_OK, WAVE_ETIMEOUT (a device wait gave
  * up; the step's outputs are undefined, the GPU context stays usable) or

@@ -86,3 +86,62 @@ def y_close(y_gpu_bits, y_ref_exact, atol=1e-3, rtol=2e-2):
     err = np.abs(y - y_ref_exact)
     bound = atol + rtol * np.abs(y_ref_exact)
     return bool(np.all(err <= bound)), float(np.max(err / bound))
+
+
+class HybridCase:
+    """Device buffers of the hybrid step at S sessions: the bf16 blob, the
+    attention blocks' FP8 history (the library's own quantiser, poisoned
+    beyond pos), the selective-state blocks' fp32 state, positions, x, y."""
+
+    def __init__(self, w, pos=None, device_gen=False, poison=True):
+        self.w = w
+        self.S = self.S_max = w.S
+        aw = w.attention_view()
+        self.cfg = fsd.WaveHybridConfig.of(w)
+        La, H, T, D = w.n_attn, w.n_heads, w.T_max, w.head_dim
+        P, N, Hs = w.ssm_head_dim, w.ssm_state, w.ssm_heads
+        dev = "cuda"
+        stream = torch.cuda.current_stream().cuda_stream
+        self.pos_h = synth.positions(aw, self.S) if pos is None else np.asarray(pos, dtype=np.int32)
+        self.pos = torch.from_numpy(self.pos_h).to(dev)
+        self.x_h = synth.x_bf16(aw, self.S)
+        self.x = torch.from_numpy(self.x_h.view(np.int16)).to(dev).view(torch.bfloat16)
+        self.y = torch.zeros_like(self.x)
+        n_w = synth.hybrid_weight_elems(w)
+        if device_gen:
+            self.weights = torch.empty(n_w, dtype=torch.bfloat16, device=dev)
+            synth.hybrid_weights_device(w, self.weights, stream)
+        else:
+            self.W_h = synth.hybrid_weights_host(w)
+            self.weights = torch.from_numpy(self.W_h.view(np.int16)).to(dev).view(torch.bfloat16)
+        self.kv = torch.zeros((La, 2, self.S_max, H, T, D), dtype=torch.uint8, device=dev)
+        self.sc = torch.zeros((La, 2, self.S_max, H, T), dtype=torch.float32, device=dev)
+        raw = torch.empty((self.S, H, T, D), dtype=torch.float32, device=dev)
+        for l in range(La):
+            for which in range(2):
+                if device_gen:
+                    synth.kv_raw_device(aw, l, which, 0, self.S, T, raw.data_ptr(), T, stream)
+                else:
+                    raw.copy_(torch.from_numpy(synth.kv_raw_host(aw, l, which, 0, self.S, T)))
+                fsd.kv_quantize(raw, self.kv[l, which, :self.S], self.sc[l, which, :self.S])
+        del raw
+        if poison:
+            t = torch.arange(T, device=dev)
+            mask = t[None, :] >= self.pos.long().clamp(min=0)[:, None]
+            m5 = mask[None, None, :, None, :].expand(La, 2, self.S, H, T)
+            self.kv[:, :, :self.S][m5] = POISON_CODE
+            self.sc[:, :, :self.S][m5] = float("nan")
+        self.state = torch.empty((w.n_mamba, self.S_max, Hs, P, N), dtype=torch.float32, device=dev)
+        for lm in range(w.n_mamba):
+            if device_gen:
+                synth.hybrid_state_device(w, lm, 0, self.S, self.state[lm].data_ptr(), stream)
+            else:
+                self.state[lm].copy_(torch.from_numpy(synth.hybrid_state_host(w, lm, 0, self.S)))
+        torch.cuda.synchronize()
+
+    def y_bits(self) -> np.ndarray:
+        return self.y.view(torch.int16).cpu().numpy().view(np.uint16)
+
+    def step(self, wave, stream=None):
+        return wave.hybrid_step(self.S, self.weights, self.kv, self.sc, self.state, self.pos, self.x, self.y,
+                                stream=stream)

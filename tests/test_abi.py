@@ -3,7 +3,10 @@ include/wave.h declares (no compute call: there may be no GPU here)."""
 import os
 import re
 
+import pytest
+
 import frame_step_decode_gb300 as fsd
+import synth
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -39,3 +42,14 @@ def test_strerror_and_bad_layout_queries():
     bad = fsd.WaveConfig(2, 256, 4, 96, 688, 1e-5, 1e4)
     assert fsd.weights_bytes(bad) == 0
     assert fsd.weight_offset(bad, 0, 0) == (1 << 64) - 1
+
+
+@pytest.mark.parametrize("w", [synth.HYBRID_SMALL, synth.HYBRID])
+def test_hybrid_blob_layout_matches_the_generator(w):
+    cfg = fsd.WaveHybridConfig.of(w)
+    assert fsd.hybrid_weights_bytes(cfg) == 2 * synth.hybrid_weight_elems(w)
+    for l in range(w.n_layers + 1):
+        assert fsd.hybrid_layer_offset(cfg, l) == 2 * synth.hybrid_layer_offset(w, l)
+    bad = fsd.WaveHybridConfig.of(w)
+    bad.ssm_state = 64
+    assert fsd.hybrid_weights_bytes(bad) == 0

@@ -1,0 +1,154 @@
+"""GPU parity of the hybrid recurrent step (wave_hybrid_step) against the
+oracle: a small shape with every part ragged enough to matter (6 layers, two
+groups of two selective-state blocks and one attention block, S = 5), and
+the full config (48 layers, d 4096, an attention block every sixth layer,
+64 state heads x 64 x 128, S = 56, positions in [0, 1500)) on sampled
+sessions, where the model is chaotic (see the full-size test).
+
+Even the small shape is ill-conditioned the way the 7B-class step is: the
+oracle's own output, for a one-ulp change of one element of x, exceeds the
+element-wise 1e-3 + 2e-2|y| bound by up to 2x on near-zero elements.  So y
+is held, normwise, to three times the oracle's own one-ulp response (never
+above 5e-2), while the parts before any cascade are held tightly: the first
+selective-state block's new state within 1e-3 normwise (its input xn can
+differ from the oracle's by a bf16 flip, which moves the state by ~1e-4),
+and every appended FP8 code and scale bit for bit against the oracle's
+quantiser on the GPU's own rows."""
+import numpy as np
+import pytest
+import torch
+
+import frame_step_decode_gb300 as fsd
+import oracle
+import synth
+from gpu_case import HybridCase, bf16_to_f64, y_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _normwise(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-30))
+
+
+def _y_within_oracle_sensitivity(w, W, sessions, pos, x, y_bits, elements=(3, 5, 100, 200), cap=5e-2):
+    """Normwise y error per session against three times the oracle's own
+    response to a one-ulp change of one element of x (the largest over a few
+    elements), and at most `cap`."""
+    kv, sc, st = oracle.hybrid_prefill(w, list(sessions), pos)
+    _, y_exact = oracle.hybrid_step(w, W, kv, sc, st, pos, x)
+    scale = np.max(np.abs(y_exact), axis=1)
+    floor = np.zeros(len(pos))
+    for el in elements:
+        kv, sc, st = oracle.hybrid_prefill(w, list(sessions), pos)
+        x_p = x.copy()
+        x_p[:, el % w.d_model] += 1
+        _, y_pert = oracle.hybrid_step(w, W, kv, sc, st, pos, x_p)
+        floor = np.maximum(floor, np.max(np.abs(y_pert - y_exact), axis=1) / scale)
+    err = np.max(np.abs(bf16_to_f64(y_bits) - y_exact), axis=1) / scale
+    ok, worst = y_close(y_bits, y_exact)
+    print("normwise y error:", err, "oracle one-ulp response:", floor, "element-wise ratio:", worst)
+    assert np.all(err <= np.maximum(3 * floor, 1e-3)) and np.all(err <= cap)
+
+
+def _run(case, sessions):
+    w = case.w
+    La, H, D = w.n_attn, w.n_heads, w.head_dim
+    wave = fsd.HybridWave(case.cfg, case.S_max, w.T_max)
+    dump = torch.full((La, 2, case.S_max, H, D), float("nan"), device="cuda")
+    try:
+        kv0, sc0, st0 = case.kv.clone(), case.sc.clone(), case.state.clone()
+        wave.debug_dump_kv(dump)
+        case.step(wave)
+        assert wave.status() == fsd.WAVE_OK
+    finally:
+        wave.debug_dump_kv(None)
+        wave.close()
+    return kv0, sc0, st0, dump.cpu().numpy()
+
+
+def test_small_hybrid_step_matches_oracle():
+    w = synth.HYBRID_SMALL
+    case = HybridCase(w)
+    kv0, sc0, st0, dump = _run(case, range(w.S))
+    sess = list(range(w.S))
+    W = synth.hybrid_weights_host(w)
+    _y_within_oracle_sensitivity(w, W, sess, case.pos_h, case.x_h, case.y_bits())
+    kv_o, sc_o, st_o = oracle.hybrid_prefill(w, sess, case.pos_h)
+    oracle.hybrid_step(w, W, kv_o, sc_o, st_o, case.pos_h, case.x_h)
+    st_g = case.state.cpu().numpy()
+    assert _normwise(st_g[0], st_o[0]) <= 1e-3                  # first block: a bf16 flip of xn at most
+    for lm in range(w.n_mamba):
+        assert _normwise(st_g[lm], st_o[lm]) <= 2e-2, lm
+    # appended codes: the oracle's quantiser on the GPU's own pre-quantisation rows
+    for s in sess:
+        P = int(case.pos_h[s])
+        codes, scales = oracle.quantize_rows(np.ascontiguousarray(dump[:, :, s]))
+        assert np.array_equal(case.kv[:, :, s, :, P].cpu().numpy(), codes)
+        assert np.array_equal(case.sc[:, :, s, :, P].cpu().numpy().view(np.uint32), scales.view(np.uint32))
+    # no other history byte moved
+    mask = torch.ones_like(case.kv, dtype=torch.bool)
+    for s in sess:
+        mask[:, :, s, :, int(case.pos_h[s])] = False
+    assert torch.equal(case.kv[mask], kv0[mask])
+
+
+def test_hybrid_empty_slot_leaves_its_state_and_passes_x():
+    w = synth.HYBRID_SMALL
+    pos = synth.positions(w.attention_view(), w.S).copy()
+    pos[2] = -1
+    case = HybridCase(w, pos=pos)
+    kv0, sc0, st0, _ = _run(case, range(w.S))
+    assert np.array_equal(case.y_bits()[2], case.x_h[2])
+    assert torch.equal(case.state[:, 2].view(torch.int32), st0[:, 2].view(torch.int32))
+    assert torch.equal(case.kv[:, :, 2], kv0[:, :, 2])
+    keep = [0, 1, 3, 4]
+    W = synth.hybrid_weights_host(w)
+    _y_within_oracle_sensitivity(w, W, keep, pos[keep], np.ascontiguousarray(case.x_h[keep]),
+                                 case.y_bits()[keep])
+
+
+@pytest.fixture(scope="module")
+def full():
+    w = synth.HYBRID
+    if torch.cuda.mem_get_info()[0] < 40e9:
+        pytest.skip("needs ~20 GB of device memory")
+    case = HybridCase(w, device_gen=True, poison=False)
+    yield case
+    del case
+    torch.cuda.empty_cache()
+
+
+def test_full_hybrid_step_matches_oracle_on_sampled_sessions(full):
+    case = full
+    w = case.w
+    sess = [0, 23, 55]
+    st_before = case.state[:, sess].cpu().numpy()
+    La, H, D = w.n_attn, w.n_heads, w.head_dim
+    dump = torch.full((La, 2, case.S_max, H, D), float("nan"), device="cuda")
+    wave = fsd.HybridWave(case.cfg, case.S_max, w.T_max)
+    try:
+        wave.debug_dump_kv(dump)
+        case.step(wave)
+        assert wave.status() == fsd.WAVE_OK
+    finally:
+        wave.debug_dump_kv(None)
+        wave.close()
+    dump = dump.cpu().numpy()
+    for s in sess:  # every appended code and scale: the oracle's quantiser on the GPU's own rows
+        P = int(case.pos_h[s])
+        codes, scales = oracle.quantize_rows(np.ascontiguousarray(dump[:, :, s]))
+        assert np.array_equal(case.kv[:, :, s, :, P].cpu().numpy(), codes)
+        assert np.array_equal(case.sc[:, :, s, :, P].cpu().numpy().view(np.uint32), scales.view(np.uint32))
+    W = synth.hybrid_weights_host(w)
+    kv_o, sc_o, st_o = oracle.hybrid_prefill(w, sess, case.pos_h[sess], poison=False)
+    assert np.array_equal(st_o, st_before)                       # the generators agree
+    # At this depth the model is chaotic: the oracle's own output moves by
+    # 25-55% (normwise) for a one-ulp change of one element of x, so no cap
+    # below that response is attainable; y is held to three times it.
+    _y_within_oracle_sensitivity(w, W, sess, case.pos_h[sess], np.ascontiguousarray(case.x_h[sess]),
+                                 case.y_bits()[sess], elements=(5, 1000), cap=np.inf)
+    oracle.hybrid_step(w, W, kv_o, sc_o, st_o, case.pos_h[sess], case.x_h[sess])
+    st_g = case.state[:, sess].cpu().numpy()
+    assert _normwise(st_g[0], st_o[0]) <= 1e-3                   # first block: a bf16 flip of xn at most
