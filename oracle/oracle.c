@@ -331,7 +331,9 @@ void oracle_proj(const uint16_t* wp, int d, int n, const uint16_t* y, uint16_t* 
  *   y[p] = sum_n C[n] h[p][n] + D x[p];  out = bf16(y * silu(z));
  *   r += W_out out.
  * Blob per layer (bf16, [out][in]): Mamba: g, W_in [2 d_i + 2N + Hs][d],
- * W_out [d][d_i], A_log [Hs], dt_bias [Hs], D [Hs]; attention: g,
+ * W_out [d][d_i], A_log [Hs], dt_bias [Hs], D [Hs] (this last block padded to
+ * a multiple of 8 elements, so that every layer starts 16-byte aligned);
+ * attention: g,
  * Wqkv [3 H D][d], Wo [d][H D].  Layers in order, each group of attn_every
  * layers = (attn_every - 1) Mamba layers then one attention layer.
  */
@@ -342,7 +344,7 @@ typedef struct {
 
 int64_t oracle_hybrid_mamba_elems(const oracle_hybrid_cfg* c) {
   const int64_t d = c->d_model, di = (int64_t)c->ssm_heads * c->ssm_head_dim;
-  return d + (2 * di + 2 * c->ssm_state + c->ssm_heads) * d + d * di + 3 * (int64_t)c->ssm_heads;
+  return d + (2 * di + 2 * c->ssm_state + c->ssm_heads) * d + d * di + (3 * (int64_t)c->ssm_heads + 7) / 8 * 8;
 }
 int64_t oracle_hybrid_attn_elems(const oracle_hybrid_cfg* c) {
   const int64_t d = c->d_model, HD = (int64_t)c->n_heads * c->head_dim;

@@ -139,7 +139,8 @@ def hybrid_layout(w: HybridWorkload) -> dict:
     """Element counts of one layer of each kind and the offsets inside them.
 
     Mamba block: g[d], W_in[in_rows][d] (z, x, B, C, dt rows), W_out[d][d_i],
-    A_log[Hs], dt_bias[Hs], D[Hs].  Attention block: g[d], Wqkv[3HD][d],
+    A_log[Hs], dt_bias[Hs], D[Hs] (padded to a multiple of 8 elements).
+    Attention block: g[d], Wqkv[3HD][d],
     Wo[d][HD].  Group of attn_every layers: (attn_every - 1) Mamba blocks,
     then one attention block."""
     d, di, Hs, HD = w.d_model, w.d_inner, w.ssm_heads, w.HD
@@ -147,7 +148,7 @@ def hybrid_layout(w: HybridWorkload) -> dict:
     m["a_log"] = m["w_out"] + d * di
     m["dt_bias"] = m["a_log"] + Hs
     m["d_skip"] = m["dt_bias"] + Hs
-    m["size"] = m["d_skip"] + Hs
+    m["size"] = m["a_log"] + (3 * Hs + 7) // 8 * 8   # parameter block padded to 16 bytes
     a = {"g": 0, "wqkv": d, "wo": d + 3 * HD * d}
     a["size"] = a["wo"] + d * HD
     return {"mamba": m, "attn": a}
