@@ -588,6 +588,35 @@ def run_hybrid(args):
         wave.hybrid_step(S, weights, kv, sc, state, pos, x, y, stream=stream)
     if wave.status() != fsd.WAVE_OK:
         raise RuntimeError("warm-up hybrid step failed")
+    if args.phases:
+        ts = torch.zeros(wave.barriers_per_step + 2, dtype=torch.int64, device=device)
+        wave.debug_phase_times(ts)
+        runs = []
+        for _ in range(3):
+            wave.hybrid_step(S, weights, kv, sc, state, pos, x, y, stream=stream)
+            if wave.status() != fsd.WAVE_OK:
+                raise RuntimeError("step failed")
+            runs.append(np.diff(ts.cpu().numpy().astype(np.float64)) / 1000.0)
+        wave.debug_phase_times(None)
+        t = np.mean(runs, axis=0)
+        names = ["prologue"]
+        merge = -(-T // 32) > 16
+        for l in range(w.n_layers):
+            if l > 0:
+                names.append("norm")
+            names += (["qkv", "attn"] + (["merge"] if merge else []) + ["o"]) if w.is_attn(l) else ["in", "ssm", "out"]
+        print(f"{w.name} S={S}: step {t.sum():.1f} us (phase = work + the grid barrier after it)")
+        agg = {}
+        for n, v in zip(names, t):
+            agg.setdefault(n, []).append(v)
+        blk = w.ssm_heads * w.ssm_head_dim * w.ssm_state * 4 * 2 * S
+        for n, v in agg.items():
+            m = float(np.mean(v))
+            extra = f"  {blk / m / 1e3:6.0f} GB/s of state" if n == "ssm" else ""
+            print(f"  {n:8s} x{len(v):3d}  mean {m:8.1f} us  total {np.sum(v):9.1f} us "
+                  f"({100 * np.sum(v) / t.sum():5.1f}%){extra}")
+        wave.close()
+        return
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     torch.cuda.synchronize()

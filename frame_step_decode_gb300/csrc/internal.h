@@ -27,7 +27,7 @@ constexpr int kGemmKinds = 7;
 // state phase is laid out for (8 warps x 8 rows, 32 lanes x 4 states).
 constexpr int kSsmP = 64;
 constexpr int kSsmN = 128;
-constexpr int kSsmStages = 4;  // state blocks in flight per CTA (32 KB each)
+constexpr int kSsmStages = 5;  // state items in flight per CTA (34 KB each)
 
 struct StepParams {
   CUtensorMap tm_w[kGemmKinds];  // weights of the projections (see GemmKind)

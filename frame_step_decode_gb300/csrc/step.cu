@@ -65,6 +65,7 @@ __device__ __forceinline__ uint32_t bar_ssm(const Ctx& c, int i) {
   return c.sbase + c.lay.bar_off + 176 + 8 * kWarps * kAttStages + 8 * i;
 }
 static_assert(176 + 8 * kWarps * kAttStages + 8 * kSsmStages <= 64 * 8, "mbarrier slots exceed their region");
+static_assert(kSsmStages * (kSsmP * kSsmN + 512) * 4 <= 200 * 1024, "state stages exceed the ring");
 __device__ __forceinline__ volatile int* misc_word(const Ctx& c, int i) {
   return (volatile int*)(c.smem + c.lay.misc_off + 4 * i);
 }
@@ -959,12 +960,17 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
 // written back in place); y_p = sum_n C_n h + D x_p; out = bf16(y_p silu(z_p)).
 // (session, head) items are dealt round-robin to CTAs; a CTA's 8 warps work
 // on one item together (warp w: rows 8w..8w+7, lane: states 4 lane..+3)
-// while thread 0 keeps kSsmStages of its next items' 32 KB state blocks in
-// flight by bulk copy.  An empty slot (negative position) leaves its state
-// alone and writes zeros.  Returns false if a copy wait gave up.
+// while thread 0 keeps kSsmStages of its next items in flight by bulk copy:
+// the 32 KB state block and the item's x, z, B, C and dt from the in-
+// projection output, so that an item's arithmetic reads shared memory only.
+// An empty slot (negative position) leaves its state alone and writes zeros.
+// Returns false if a copy wait gave up.
+constexpr int kSsmSide = 64 + 64 + kSsmN + kSsmN + 4;              // x, z, B, C, dt group (floats)
+constexpr int kSsmStageF = kSsmP * kSsmN + ((kSsmSide + 31) / 32) * 32;  // floats per stage
 __device__ __forceinline__ bool ssm_phase(const StepParams& p, Ctx& c, int lm, int l) {
   static_assert(kWarps * 8 == kSsmP && 32 * 4 == kSsmN, "state phase layout");
   constexpr uint32_t kBlk = kSsmP * kSsmN * 4;
+  constexpr uint32_t kTx = kBlk + (64 + 64 + kSsmN + kSsmN + 4) * 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hs = p.ssm_heads, di = p.d_inner, R = p.in_rows, N = kSsmN;
   const int items = p.S * Hs;
@@ -973,18 +979,30 @@ __device__ __forceinline__ bool ssm_phase(const StepParams& p, Ctx& c, int lm, i
   float* state_l = p.ssm_state + (size_t)lm * p.S_max * Hs * kSsmP * kSsmN;
   const uint32_t ring_s = c.sbase + c.lay.ring_off;
   const float* ring = (const float*)(c.smem + c.lay.ring_off);
+  // A_log, dt_bias, D of every head, once per phase, after the stages
+  float* prm_s = (float*)(c.smem + c.lay.ring_off) + kSsmStages * kSsmStageF;
   auto issue = [&](int k) {  // thread 0
-    const int i = (int)blockIdx.x + k * (int)gridDim.x, s = i / Hs;
+    const int i = (int)blockIdx.x + k * (int)gridDim.x, s = i / Hs, hh = i - s * Hs;
     const uint32_t st = (c.ssm_it + (uint32_t)k) % kSsmStages, b = bar_ssm(c, st);
     if (p.pos[s] < 0) {
       mbar_arrive(b);  // nothing to copy for an empty slot
     } else {
-      mbar_arrive_expect_tx(b, kBlk);
-      bulk_load(ring_s + st * kBlk, state_l + (size_t)i * kSsmP * kSsmN, kBlk, b);
+      const uint32_t dst = ring_s + st * kSsmStageF * 4;
+      const float* zrow = p.zx + (size_t)s * R;
+      mbar_arrive_expect_tx(b, kTx);
+      bulk_load(dst, state_l + (size_t)i * kSsmP * kSsmN, kBlk, b);
+      bulk_load(dst + kBlk, zrow + di + hh * kSsmP, 64 * 4, b);                 // x
+      bulk_load(dst + kBlk + 256, zrow + hh * kSsmP, 64 * 4, b);                // z
+      bulk_load(dst + kBlk + 512, zrow + 2 * di, kSsmN * 4, b);                 // B
+      bulk_load(dst + kBlk + 512 + kSsmN * 4, zrow + 2 * di + N, kSsmN * 4, b);  // C
+      bulk_load(dst + kBlk + 512 + 2 * kSsmN * 4, zrow + 2 * di + 2 * N + (hh & ~3), 16, b);  // dt
     }
   };
-  if (threadIdx.x == 0)
+  if (threadIdx.x == 0) {
+    fence_proxy_async_smem();  // earlier generic accesses to the ring come first
     for (int k = 0; k < min(my, kSsmStages); ++k) issue(k);
+  }
+  for (int i = threadIdx.x; i < 3 * Hs; i += kThreads) prm_s[i] = bf16_to_f32(prm[i]);
   for (int k = 0; k < my; ++k) {
     const int i = (int)blockIdx.x + k * (int)gridDim.x, s = i / Hs, hh = i - s * Hs;
     const uint32_t st = (c.ssm_it + (uint32_t)k) % kSsmStages;
@@ -999,20 +1017,24 @@ __device__ __forceinline__ bool ssm_phase(const StepParams& p, Ctx& c, int lm, i
     if (p.pos[s] < 0) {
       if (lane < 8) orow[lane] = 0;
     } else {
-      const float* zrow = p.zx + (size_t)s * R;
-      const float dtr = zrow[2 * di + 2 * N + hh] + bf16_to_f32(prm[Hs + hh]);
+      const float* blk = ring + st * kSsmStageF;
+      const float* xs = blk + kSsmP * kSsmN;
+      const float* zs = xs + 64;
+      const float* Bs = zs + 64;
+      const float* Cs = Bs + kSsmN;
+      const float* dts = Cs + kSsmN;
+      const float dtr = dts[hh & 3] + prm_s[Hs + hh];
       const float dt = dtr > 0.f ? dtr + log1pf(expf(-dtr)) : log1pf(expf(dtr));
-      const float a = expf(-expf(bf16_to_f32(prm[hh])) * dt);
-      const float Dh = bf16_to_f32(prm[2 * Hs + hh]);
-      const float4 B4 = *(const float4*)(zrow + 2 * di + 4 * lane);
-      const float4 C4 = *(const float4*)(zrow + 2 * di + N + 4 * lane);
-      const float* blk = ring + st * (kBlk / 4);
+      const float a = expf(-expf(prm_s[hh]) * dt);
+      const float Dh = prm_s[2 * Hs + hh];
+      const float4 B4 = ((const float4*)Bs)[lane];
+      const float4 C4 = ((const float4*)Cs)[lane];
       float* gst = state_l + (size_t)i * kSsmP * kSsmN;
       float yv[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int pr = warp * 8 + j;
-        const float tx = dt * zrow[di + hh * kSsmP + pr];
+        const float tx = dt * xs[pr];
         float4 h = *(const float4*)(blk + pr * N + 4 * lane);
         h.x = fmaf(a, h.x, tx * B4.x);
         h.y = fmaf(a, h.y, tx * B4.y);
@@ -1031,7 +1053,7 @@ __device__ __forceinline__ bool ssm_phase(const StepParams& p, Ctx& c, int lm, i
         for (int j = 1; j < 8; ++j)
           if (lane == j) yj = yv[j];
         const int pr = warp * 8 + lane;
-        const float xp = zrow[di + hh * kSsmP + pr], zp = zrow[hh * kSsmP + pr];
+        const float xp = xs[pr], zp = zs[pr];
         const float yp = yj + Dh * xp;
         orow[lane] = f32_to_bf16(yp * zp / (1.0f + expf(-zp)));
       }
@@ -1041,6 +1063,7 @@ __device__ __forceinline__ bool ssm_phase(const StepParams& p, Ctx& c, int lm, i
     if (threadIdx.x == 0 && k + kSsmStages < my) issue(k + kSsmStages);
   }
   c.ssm_it += (uint32_t)my;
+  fence_proxy_async_smem();  // the next phase's copies overwrite the ring
   return true;
 }
 
