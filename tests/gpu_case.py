@@ -93,9 +93,10 @@ class HybridCase:
     attention blocks' FP8 history (the library's own quantiser, poisoned
     beyond pos), the selective-state blocks' fp32 state, positions, x, y."""
 
-    def __init__(self, w, pos=None, device_gen=False, poison=True):
+    def __init__(self, w, pos=None, device_gen=False, poison=True, S=None, S_max=None):
         self.w = w
-        self.S = self.S_max = w.S
+        self.S = w.S if S is None else S
+        self.S_max = self.S if S_max is None else S_max
         aw = w.attention_view()
         self.cfg = fsd.WaveHybridConfig.of(w)
         La, H, T, D = w.n_attn, w.n_heads, w.T_max, w.head_dim
@@ -136,7 +137,7 @@ class HybridCase:
             if device_gen:
                 synth.hybrid_state_device(w, lm, 0, self.S, self.state[lm].data_ptr(), stream)
             else:
-                self.state[lm].copy_(torch.from_numpy(synth.hybrid_state_host(w, lm, 0, self.S)))
+                self.state[lm, :self.S].copy_(torch.from_numpy(synth.hybrid_state_host(w, lm, 0, self.S)))
         torch.cuda.synchronize()
 
     def y_bits(self) -> np.ndarray:

@@ -80,3 +80,30 @@ def test_depth_loop_matches_oracle_on_sampled_sessions(run):
         floor = np.max(np.abs(ye_p[k] - ye[k]), axis=1) / scale
         print(f"step {k}: normwise error {err}, oracle one-ulp response {floor}")
         assert np.all(err <= np.maximum(3 * floor, 1e-2)) and np.all(err <= 5e-2)
+
+
+def test_depth_loop_on_a_ragged_prefix_batch():
+    # S = 19 sessions of an S_max = 80 handle; sessions are independent, so
+    # each equals its own run in the full batch bit for bit
+    w = W
+    S, d = 19, w.d_model
+    L, H, T, D = w.n_layers, w.n_heads, w.T_max, w.head_dim
+    Wh = synth.weights_host(w)
+    dev = "cuda"
+    weights = torch.from_numpy(Wh.view(np.int16)).to(dev).view(torch.bfloat16)
+    wp = torch.from_numpy(synth.proj_host(w).view(np.int16)).to(dev).view(torch.bfloat16)
+    x0 = torch.from_numpy(synth.x_bf16(w, w.S).view(np.int16)).to(dev).view(torch.bfloat16)
+    outs = []
+    for n in (S, w.S):
+        kv = torch.full((L, 2, w.S, H, T, D), 0x7F, dtype=torch.uint8, device=dev)
+        sc = torch.full((L, 2, w.S, H, T), float("nan"), dtype=torch.float32, device=dev)
+        xs = torch.zeros((STEPS, n, d), dtype=torch.bfloat16, device=dev)
+        y = torch.zeros((STEPS, n, d), dtype=torch.bfloat16, device=dev)
+        wave = fsd.Wave(fsd.WaveConfig.of(w), w.S, T)
+        try:
+            wave.depth(n, STEPS, weights, wp, kv, sc, x0[:n].contiguous(), xs, y)
+            assert wave.status() == fsd.WAVE_OK
+        finally:
+            wave.close()
+        outs.append(y)
+    assert torch.equal(outs[0].view(torch.int16), outs[1][:, :S].view(torch.int16))

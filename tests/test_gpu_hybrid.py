@@ -109,6 +109,21 @@ def test_hybrid_empty_slot_leaves_its_state_and_passes_x():
                                  case.y_bits()[keep])
 
 
+def test_hybrid_prefix_batch_in_a_larger_handle_matches_oracle():
+    # S < S_max: the state and history are indexed by S_max-strided sessions
+    w = synth.HYBRID_SMALL
+    case = HybridCase(w, S=3, S_max=7)
+    _run(case, range(3))
+    W = synth.hybrid_weights_host(w)
+    _y_within_oracle_sensitivity(w, W, [0, 1, 2], case.pos_h, np.ascontiguousarray(case.x_h), case.y_bits())
+    kv_o, sc_o, st_o = oracle.hybrid_prefill(w, [0, 1, 2], case.pos_h)
+    oracle.hybrid_step(w, W, kv_o, sc_o, st_o, case.pos_h, case.x_h)
+    st_g = case.state[:, :3].cpu().numpy()
+    assert _normwise(st_g[0], st_o[0]) <= 1e-3
+    for lm in range(w.n_mamba):
+        assert _normwise(st_g[lm], st_o[lm]) <= 2e-2, lm
+
+
 @pytest.fixture(scope="module")
 def full():
     w = synth.HYBRID

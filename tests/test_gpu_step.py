@@ -233,6 +233,38 @@ def test_two_frame_beat_equals_two_steps_and_rolls_positions(w):
         wave.close()
 
 
+def test_beat_without_advance_and_with_a_frame_past_t_max():
+    # frame 1 runs at position + 1: a session at T_max - 1 is out of range
+    # there (WAVE_EPOS, nothing written in that frame); positions stay as
+    # given when the advance is off; the other sessions match two steps
+    w = synth.TINY
+    pos = synth.positions(w, w.S).copy()
+    pos = np.minimum(pos, w.T_max - 2)
+    pos[1] = w.T_max - 1
+    a = DeviceCase(w, pos=pos)
+    b = DeviceCase(w, pos=pos)
+    x2 = torch.stack([a.x, a.x.flip(0)])
+    y2 = torch.zeros_like(x2)
+    wave = fsd.Wave(a.cfg, a.S_max, w.T_max)
+    try:
+        wave.beat(w.S, 2, a.weights, a.kv, a.sc, a.pos, x2, y2, advance=False)
+        assert wave.status() == fsd.WAVE_EPOS
+        assert torch.equal(a.pos.cpu(), torch.from_numpy(pos))
+        ys = []
+        for f in range(2):
+            yf = torch.zeros_like(x2[f])
+            wave.step(w.S, b.weights, b.kv, b.sc, b.pos, x2[f].contiguous(), yf)
+            wave.status()
+            ys.append(yf)
+            b.pos += 1
+        for f in range(2):
+            keep = [s for s in range(w.S) if f == 0 or s != 1]
+            assert torch.equal(y2[f][keep].view(torch.int16), ys[f][keep].view(torch.int16))
+        assert torch.equal(a.kv, b.kv)
+    finally:
+        wave.close()
+
+
 def test_out_of_range_position_is_reported_and_skipped():
     w = synth.TINY
     case = DeviceCase(w)
