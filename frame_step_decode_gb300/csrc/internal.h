@@ -91,15 +91,16 @@ constexpr int kCounterWords = 2048 + 1024;
 // Frames one launch may run back to back (wave_beat).
 constexpr int kMaxFrames = 64;
 
-__host__ __device__ inline int stream_k_ctas(int grid, long long U, int tiles, int seg_cap = 62) {
+__host__ __device__ inline int stream_k_ctas(int grid, long long U, int tiles, int seg_cap) {
   long long g = grid;
   if (U < g) g = U;
   if ((long long)seg_cap * tiles < g) g = (long long)seg_cap * tiles;
   return (int)g;
 }
-// Per GEMM kind: the depth loop's small projection (latency-bound) is split
-// into at most ~4 segments per tile, so its split-K reduction stays short.
-__host__ __device__ inline int gemm_seg_cap(int kind) { return kind == kProj ? 4 : 62; }
+// Segments per tile at most: a tile split many ways (small models) pays one
+// L2 round trip per pair of segments in its reduction, more than the extra
+// streaming a few CTAs more per tile would save; the depth loop's W_p, at ~4.
+__host__ __device__ inline int gemm_seg_cap(int kind) { return kind == kProj ? 4 : 8; }
 // Element offset of layer l in a hybrid blob (groups of attn_every layers:
 // attn_every - 1 Mamba blocks, then the attention block).
 __host__ __device__ inline long long hyb_layer_offset(long long M, long long G, int e, int l) {

@@ -75,9 +75,9 @@ __global__ void k_rope_table(float2* tab, int T_max, int half, int D, double bas
   }
 }
 
-int max_tiles(long long tiles, long long kb, int grid) {
+int max_tiles(long long tiles, long long kb, int grid, int seg_cap) {
   const long long U = tiles * kb;
-  const int G = stream_k_ctas(grid, U, (int)tiles);
+  const int G = stream_k_ctas(grid, U, (int)tiles, seg_cap);
   int mt = 1;
   for (int c = 0; c < G; ++c) {
     const long long u0 = U * c / G, u1 = U * (c + 1) / G;
@@ -88,9 +88,9 @@ int max_tiles(long long tiles, long long kb, int grid) {
   return mt;
 }
 
-int max_segs(long long tiles, long long kb, int grid) {
+int max_segs(long long tiles, long long kb, int grid, int seg_cap) {
   const long long U = tiles * kb;
-  const int G = stream_k_ctas(grid, U, (int)tiles);
+  const int G = stream_k_ctas(grid, U, (int)tiles, seg_cap);
   int ms = 1;
   for (long long t = 0; t < tiles; ++t) {
     const long long a = t * kb, b = (t + 1) * kb - 1;
@@ -163,8 +163,8 @@ extern "C" int wave_step_static(const wave_config* cfg, int S_max, int T_max, in
   kblocks[kDown] = (F + kKBlk - 1) / kKBlk;
   int mt = 1;
   for (int k = 0; k < 4; ++k) {
-    if (tiles[k] > 1024 || max_segs(tiles[k], kblocks[k], sms) > 64) return WAVE_EINVAL;
-    const int m = max_tiles(tiles[k], kblocks[k], sms);
+    if (tiles[k] > 1024 || max_segs(tiles[k], kblocks[k], sms, gemm_seg_cap(k)) > 64) return WAVE_EINVAL;
+    const int m = max_tiles(tiles[k], kblocks[k], sms, gemm_seg_cap(k));
     if (m > mt) mt = m;
   }
   const long long SP = (S_max + 15) / 16 * 16;

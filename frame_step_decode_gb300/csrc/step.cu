@@ -213,7 +213,7 @@ __device__ __forceinline__ int owner_of(long long U, int G, long long u) {
 __device__ void prefetch_gemm_weights(const StepParams& p, int kind, int layer) {
   const int KB = p.kblocks[kind], T = p.tiles[kind];
   const long long U = (long long)T * KB;
-  const int G = stream_k_ctas(gridDim.x, U, T), cta = blockIdx.x;
+  const int G = stream_k_ctas(gridDim.x, U, T, gemm_seg_cap(kind)), cta = blockIdx.x;
   if (cta >= G) return;
   const Span sp = cta_span(U, G, cta);
   const int K = (kind == kO) ? p.HD : p.F;   // O and down only
