@@ -1,9 +1,10 @@
 // step.cu -- the persistent frame-step kernel: one cooperative launch runs
-// every decoder layer for all S sessions, phases separated by device-side
-// grid barriers (no CPU round trip between operations: dotwave.ai case study,
+// every layer for all S sessions, phases separated by device-side grid
+// barriers (no CPU round trip between operations: dotwave.ai case study,
 // "02 / The solution" and "04 / Under the hood").
 //
-// Phases per layer l (8 grid barriers per layer):
+// Decoder layer l (8 grid barriers per layer; 7 when no history is long
+// enough to be split into several attention pieces):
 //   norm     RMSNorm rows of the fp32 residual -> bf16 xn           (CUDA cores)
 //   QKV      xn . Wqkv^T -> fp32 q,k,v                              (tcgen05, stream-K)
 //   attn     per (session, head) piece: RoPE(q); the piece holding the
@@ -16,11 +17,19 @@
 //   norm     RMSNorm -> xn
 //   GU       u = bf16(silu(xn . Wg^T) * (xn . Wu^T))               (tcgen05, stream-K)
 //   down     resid += u . Wdown^T (y = bf16(resid) after the last layer)
+// Around the layers: a prologue (work list, residual from x, first norm);
+// several frames per launch (beats) with positions + f; chained frames (the
+// depth loop) with x_f = bf16(W_p y_{f-1}) between them.  The hybrid model
+// (step_kernel<true>) replaces the MLP half by nothing and, in all but every
+// attn_every-th layer, attention by a selective-state block: in-projection,
+// state update, out-projection + residual.
 //
-// Roles inside a 6-warp CTA during GEMM phases: warp 0 issues TMA loads of
+// Roles inside the 8-warp CTA during GEMM phases: warp 0 issues TMA loads of
 // weight/activation tiles into a shared-memory ring, warp 1 issues tcgen05
-// MMAs into a double-buffered TMEM accumulator, warps 2..5 drain TMEM and run
-// the fused epilogue.  Every wait is bounded (globaltimer) and reports
+// MMAs into a double-buffered TMEM accumulator, warps 2..5 drain TMEM into
+// split-K partial slots; the split tile a CTA's span ends in is then summed
+// by all its threads.  Attention, the norms, the merge and the state update
+// use all 8 warps.  Every wait is bounded (globaltimer) and reports
 // WAVE_ETIMEOUT through the device error word instead of hanging.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
