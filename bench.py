@@ -65,7 +65,8 @@ def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         try:
-            d = json.load(open(path))
+            with open(path) as f:
+                d = json.load(f)
             for k in ("hbm_gbs", "hbm_GBps", "hbm"):
                 if k in d:
                     return float(d[k]), "measured"
@@ -80,11 +81,14 @@ def traffic_per_launch():
     if not os.path.exists(PROFILE_TRAFFIC):
         return None
     vals = {}
-    for line in open(PROFILE_TRAFFIC):
+    with open(PROFILE_TRAFFIC) as f:
+        lines = f.readlines()
+    for line in lines:
         if ":" in line:
             k, v = line.split(":", 1)
             vals[k.strip()] = v.strip()
-    src_sha = hashlib.sha256(open(STEP_SRC, "rb").read()).hexdigest()[:16]
+    with open(STEP_SRC, "rb") as f:
+        src_sha = hashlib.sha256(f.read()).hexdigest()[:16]
     if vals.get("step_cu_sha256_16") != src_sha:
         return None
     try:

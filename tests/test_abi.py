@@ -12,7 +12,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def declared_symbols():
-    txt = open(os.path.join(ROOT, "include", "wave.h")).read()
+    with open(os.path.join(ROOT, "include", "wave.h")) as f:
+        txt = f.read()
     txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
     return sorted(set(re.findall(r"\b(wave_[a-z_0-9]+)\s*\(", txt)))
 
