@@ -95,8 +95,11 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
 
 // ------------------------------------------------------------- grid barrier
 // All CTAs arrive on one counter (zeroed before the launch) and wait until it
-// reaches (barrier index + 1) * grid.  The wait gives up after timeout_ns or
-// when another CTA has recorded an error.
+// reaches (barrier index + 1) * grid.  Every thread's generic writes are made
+// visible to the async proxy first (the next phase reads some of them by TMA)
+// and released with the arrival; the waiting thread's acquire load orders the
+// next phase after the other CTAs' writes.  The wait gives up after
+// timeout_ns or when another CTA has recorded an error.
 __device__ bool grid_sync(const StepParams& p, Ctx& c) {
   fence_proxy_async_global();
   __syncthreads();
@@ -118,15 +121,12 @@ __device__ bool grid_sync(const StepParams& p, Ctx& c) {
         break;
       }
     }
-    __threadfence();
-    *misc_word(c, 2) = ok;
+    *misc_word(c, 2) = ok;  // the acquire load above orders what follows
     if (p.phase_ts && blockIdx.x == 0) p.phase_ts[1 + c.bar_index] = globaltimer();
   }
   c.bar_index++;
   __syncthreads();
-  bool ok = *misc_word(c, 2) != 0;
-  fence_proxy_async_global();
-  return ok;
+  return *misc_word(c, 2) != 0;
 }
 
 // ------------------------------------------------------------------- norm
