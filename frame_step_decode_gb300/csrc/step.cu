@@ -527,10 +527,13 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
         named_bar(1, 128);
         finish_tile<true>(p, kind, t, slot, nullptr, 1, threadIdx.x - 64, 128, last_layer, c.frame);
       } else {
-        // split tile: count this segment in
-        __threadfence();
+        // split tile: count this segment in (one thread releases the four
+        // warps' stores, which the named barrier orders before it)
         named_bar(1, 128);
-        if (threadIdx.x == 64) atomicAdd(p.tile_cnt + t, 1);
+        if (threadIdx.x == 64) {
+          __threadfence();
+          atomicAdd(p.tile_cnt + t, 1);
+        }
       }
       c.acc_it++;
       u = e;
