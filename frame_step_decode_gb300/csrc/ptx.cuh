@@ -103,6 +103,15 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "l"((uint64_t)src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// The same with an L2 cache-policy hint (e.g. evict-first for data read once).
+__device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                               uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"((uint64_t)src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

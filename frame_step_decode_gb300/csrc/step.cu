@@ -1002,7 +1002,7 @@ __device__ __forceinline__ bool ssm_phase(const StepParams& p, Ctx& c, int lm, i
       const uint32_t dst = ring_s + st * kSsmStageF * 4;
       const float* zrow = p.zx + (size_t)s * R;
       mbar_arrive_expect_tx(b, kTx);
-      bulk_load(dst, state_l + (size_t)i * kSsmP * kSsmN, kBlk, b);
+      bulk_load_hint(dst, state_l + (size_t)i * kSsmP * kSsmN, kBlk, b, policy_evict_first());
       bulk_load(dst + kBlk, zrow + di + hh * kSsmP, 64 * 4, b);                 // x
       bulk_load(dst + kBlk + 256, zrow + hh * kSsmP, 64 * 4, b);                // z
       bulk_load(dst + kBlk + 512, zrow + 2 * di, kSsmN * 4, b);                 // B
@@ -1052,7 +1052,7 @@ __device__ __forceinline__ bool ssm_phase(const StepParams& p, Ctx& c, int lm, i
         h.y = fmaf(a, h.y, tx * B4.y);
         h.z = fmaf(a, h.z, tx * B4.z);
         h.w = fmaf(a, h.w, tx * B4.w);
-        *(float4*)(gst + pr * N + 4 * lane) = h;
+        __stcs((float4*)(gst + pr * N + 4 * lane), h);  // streamed: read again only next frame
         yv[j] = C4.x * h.x + C4.y * h.y + C4.z * h.z + C4.w * h.w;
       }
 #pragma unroll
