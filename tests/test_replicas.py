@@ -30,7 +30,7 @@ def _rank(rank, world, port, out):
 
 def test_two_gloo_ranks_agree_on_the_slowest_replica():
     world, port = 2, 29517 + os.getpid() % 1000
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_rank, args=(world, port, out), nprocs=world, join=True)
     for r in range(world):
