@@ -146,3 +146,36 @@ class HybridCase:
     def step(self, wave, stream=None):
         return wave.hybrid_step(self.S, self.weights, self.kv, self.sc, self.state, self.pos, self.x, self.y,
                                 stream=stream)
+
+
+def codes_vs_oracle(gpu_codes, gpu_pre, ora_codes, ora_scales, ora_pre):
+    """End-to-end check of one session's appended FP8 codes ([L][2][H][D])
+    against the oracle's own codes.  The two paths' pre-quantisation rows
+    differ (fp32 against fp64 arithmetic), so where a code differs it must
+    be the code of a value within that difference of the oracle's: of some
+    v/scale in [u - e, u + e], u the oracle's value in code units and e
+    twice the row's measured difference in code units (once for the value,
+    once for the row's scale through amax).  With rows that agree closely
+    this allows one code step at a rounding boundary and nothing else.
+    Returns the number of differing codes."""
+    import oracle
+    g = np.asarray(gpu_codes, dtype=np.int64)
+    o = np.asarray(ora_codes, dtype=np.int64)
+    mis = g != o
+    n = int(np.count_nonzero(mis))
+    if n == 0:
+        return 0
+    sc = np.asarray(ora_scales, dtype=np.float64)[..., None]
+    pre_o = np.asarray(ora_pre, dtype=np.float64)
+    safe = np.where(sc > 0, sc, 1.0)
+    u = np.where(sc > 0, pre_o / safe, 0.0)
+    err_u = np.where(sc > 0, np.max(np.abs(np.asarray(gpu_pre, dtype=np.float64) - pre_o), axis=-1,
+                                    keepdims=True) / safe, 0.0)
+    e = 2.02 * np.broadcast_to(err_u, u.shape)[mis] + 1e-5 * np.abs(u[mis]) + 1e-12
+    lo = oracle.e4m3_encode((u[mis] - e).astype(np.float32)).astype(np.int64)
+    hi = oracle.e4m3_encode((u[mis] + e).astype(np.float32)).astype(np.int64)
+    signed = lambda c: np.where(c & 0x80, -(c & 0x7F), c & 0x7F)
+    gs = signed(g[mis])
+    assert np.all((signed(lo) <= gs) & (gs <= signed(hi))), \
+        "a code differs by more than the two paths' difference can explain"
+    return n

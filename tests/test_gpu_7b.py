@@ -21,7 +21,7 @@ import torch
 import frame_step_decode_gb300 as fsd
 import oracle
 import synth
-from gpu_case import DeviceCase, y_close
+from gpu_case import DeviceCase, codes_vs_oracle, y_close
 
 pytestmark = pytest.mark.gpu
 
@@ -87,13 +87,18 @@ def test_full_size_step_matches_oracle_on_sampled_sessions(big):
     print("normwise y error per sampled session:", gpu_err, "oracle one-ulp sensitivity:", floor)
     assert np.all(gpu_err <= np.maximum(3 * floor, 1e-3)) and np.all(gpu_err <= 5e-2)
     dump_h = dump.cpu().numpy()
+    n_diff = 0
     for j, s in enumerate(sess):
         P = int(case.pos_h[s])
         pre = np.ascontiguousarray(dump_h[:, :, s])          # [L][2][H][D]
         codes, scales = oracle.quantize_rows(pre)
         assert np.array_equal(case.kv[:, :, s, :, P].cpu().numpy(), codes)
+        # end to end against the oracle's own codes (written into kv_o by its step)
+        n_diff += codes_vs_oracle(codes, pre, kv_o[:, :, j, :, P], sc_o[:, :, j, :, P], kv_new[:, :, j])
         assert np.array_equal(case.sc[:, :, s, :, P].cpu().numpy().view(np.uint32), scales.view(np.uint32))
         err = np.max(np.abs(pre.astype(np.float64) - kv_new[:, :, j]), axis=-1)
         ref = np.max(np.abs(kv_new[:, :, j].astype(np.float64)), axis=-1)
         assert np.all(err[0] <= 1e-4 * ref[0] + 1e-6)   # layer 0: before any cascade
         assert np.all(err <= 5e-2 * ref + 1e-6)
+    print(f"{n_diff} of {len(sess) * L * 2 * H * D} appended codes differ from the oracle's own "
+          "(each within the two paths' measured difference of the oracle's value)")

@@ -10,7 +10,7 @@ import torch
 
 import frame_step_decode_gb300 as fsd
 import synth
-from gpu_case import DeviceCase, oracle_reference, y_close
+from gpu_case import DeviceCase, codes_vs_oracle, oracle_reference, y_close
 
 pytestmark = pytest.mark.gpu
 
@@ -41,7 +41,8 @@ def _check_case(case: DeviceCase, wave, sessions=None, normwise=False):
     response to a one-ulp change of x exceeds the element-wise bound); every
     appended code and scale equal, bit for bit, to the oracle quantiser
     applied to the GPU's own pre-quantisation K/V rows; those rows close to
-    the oracle's; no other history byte moved."""
+    the oracle's; the codes against the oracle's own end to end (one step
+    at most, and only at a rounding boundary); no other history byte moved."""
     import oracle
     w = case.w
     sessions = list(range(case.S)) if sessions is None else sessions
@@ -61,7 +62,8 @@ def _check_case(case: DeviceCase, wave, sessions=None, normwise=False):
     W = synth.weights_host(w) if W is None else W
     kv_o, sc_o = oracle.prefill_history(w, sessions, pos, poison=True)
     x_s = np.ascontiguousarray(case.x_h[sessions])
-    _, y_exact, kv_new = oracle.step(w, W, kv_o.copy(), sc_o.copy(), pos, x_s, want_kv_new=True)
+    kv_w, sc_w = kv_o.copy(), sc_o.copy()
+    _, y_exact, kv_new = oracle.step(w, W, kv_w, sc_w, pos, x_s, want_kv_new=True)
     if normwise:
         _y_within_sensitivity(w, W, pos, x_s, y[sessions], kv_o, sc_o)
     else:
@@ -79,6 +81,13 @@ def _check_case(case: DeviceCase, wave, sessions=None, normwise=False):
     ref_codes, ref_sc = oracle.quantize_rows(pre)
     assert np.array_equal(got_codes, ref_codes), "appended codes differ from the oracle quantiser"
     assert np.array_equal(got_sc.view(np.uint32), ref_sc.view(np.uint32))
+    # end to end against the oracle's own codes (one step, at boundaries only)
+    n_diff = 0
+    for j, s in enumerate(sessions):
+        Pj = int(pos[j])
+        n_diff += codes_vs_oracle(got_codes[s], pre[s], kv_w[:, :, j, :, Pj], sc_w[:, :, j, :, Pj], kv_new[:, :, j])
+    print(f"{w.name}: {n_diff} of {got_codes[sessions].size} appended codes differ from the oracle's own "
+          "(each within the two paths' measured difference of the oracle's value)")
     # the GPU's pre-quantisation rows against the oracle's (fp64 path)
     for j, s in enumerate(sessions):
         a = pre[s].astype(np.float64)
