@@ -198,19 +198,19 @@ static int build_ctx(wave_ctx* h, int S_max, int T_max, int in_rows, int d_inner
   const int d = cfg->d_model, HD = cfg->n_heads * cfg->head_dim, F = cfg->ffn, H = cfg->n_heads,
             D = cfg->head_dim;
   h->tiles[kQKV] = (3 * HD + kTileM - 1) / kTileM;
-  h->kblocks[kQKV] = (d + kKBlk - 1) / kKBlk;
+  h->kblocks[kQKV] = (d + kKUnit - 1) / kKUnit;
   h->tiles[kO] = (d + kTileM - 1) / kTileM;
-  h->kblocks[kO] = (HD + kKBlk - 1) / kKBlk;
+  h->kblocks[kO] = (HD + kKUnit - 1) / kKUnit;
   h->tiles[kGU] = (F + 63) / 64;
-  h->kblocks[kGU] = (d + kKBlk - 1) / kKBlk;
+  h->kblocks[kGU] = (d + kKUnit - 1) / kKUnit;
   h->tiles[kDown] = F ? (d + kTileM - 1) / kTileM : 0;
-  h->kblocks[kDown] = (F + kKBlk - 1) / kKBlk;
+  h->kblocks[kDown] = (F + kKUnit - 1) / kKUnit;
   h->tiles[kProj] = h->hybrid ? 0 : (d + kTileM - 1) / kTileM;
-  h->kblocks[kProj] = (d + kKBlk - 1) / kKBlk;
+  h->kblocks[kProj] = (d + kKUnit - 1) / kKUnit;
   h->tiles[kIn] = (in_rows + kTileM - 1) / kTileM;
-  h->kblocks[kIn] = (d + kKBlk - 1) / kKBlk;
+  h->kblocks[kIn] = (d + kKUnit - 1) / kKUnit;
   h->tiles[kOut] = d_inner ? (d + kTileM - 1) / kTileM : 0;
-  h->kblocks[kOut] = (d_inner + kKBlk - 1) / kKBlk;
+  h->kblocks[kOut] = (d_inner + kKUnit - 1) / kKUnit;
   int mt = 1;
   for (int k = 0; k < kGemmKinds; ++k) {
     if (h->tiles[k] > 1024) return WAVE_EINVAL;
@@ -542,8 +542,8 @@ static int launch_frames(wave_t* h, int S, int frames, const void* weights, uint
   p.S_max = h->S_max;
   p.T_max = h->T_max;
   p.eps = c.rms_eps;
-  const int stride = 16384 + ((S_pad * 128 + 1023) & ~1023);
-  int nst = smem_layout().ring_bytes / stride;
+  const int stride = gemm_stage_bytes(S_pad);
+  int nst = smem_layout().gemm_ring_bytes / stride;
   p.nstage = nst > kMaxStages ? kMaxStages : nst;
   p.max_tiles_per_cta = h->max_tiles_per_cta;
   p.layer_elems = h->layer_elems;

@@ -10,7 +10,9 @@ constexpr int kThreads = 256;     // 8 warps: TMA producer, MMA issuer, 4 epilog
                                   // (all 8 run attention and the norms)
 constexpr int kWarps = kThreads / 32;
 constexpr int kTileM = 128;       // weight rows per GEMM tile = tcgen05 M
-constexpr int kKBlk = 64;         // K elements per pipeline stage (128 B of bf16)
+constexpr int kKBlk = 64;         // K elements per TMA box (128 B of bf16, the swizzle span)
+constexpr int kKStage = 2;        // boxes per ring stage: a stream-K unit is kKUnit K elements
+constexpr int kKUnit = kKBlk * kKStage;
 constexpr int kChunk = 32;        // attention tokens per async-copy chunk (2 x 16)
 constexpr int kAttStages = 3;     // stages per attention warp (two in flight while one is read)
 constexpr int kPieceChunks = 16;  // chunks per attention work piece (512 tokens)
@@ -119,7 +121,9 @@ int barriers_per_launch(int L, int T_max, int frames, bool advance, bool depth);
 int hybrid_barriers_per_step(int L, int attn_every, int T_max);
 // Dynamic shared memory layout shared by host checks and the kernel.
 struct SmemLayout {
-  int ring_off, ring_bytes;      // GEMM ring / attention K and V tiles (union)
+  int ring_off, ring_bytes;      // attention K and V tiles / state blocks / norm rows (union)
+  int gemm_ring_bytes;           // the GEMM ring: ring, attention scales, prologue scratch and
+                                 // query scratch together (none of those is live in a GEMM phase)
   int ascale_off;                // attention K/V scales: kWarps x kAttStages x 256 B
   int xbuf_off;                  // prologue scratch (work-list positions), 4352 B
   int qscr_off;                  // per-warp query scratch (kWarps x 512 B)
@@ -139,7 +143,15 @@ __host__ __device__ inline SmemLayout smem_layout() {
   s.bar_off = s.red_off + 1024;                      // 64 mbarriers
   s.misc_off = s.bar_off + 64 * 8;
   s.total = s.misc_off + 64 + 1024;                  // + alignment slack
+  s.gemm_ring_bytes = s.red_off - s.ring_off;
   return s;
+}
+// Bytes of one GEMM ring stage at S_pad sessions: kKStage weight boxes
+// (128 rows x 128 B) and kKStage activation boxes (S_pad rows x 128 B, each
+// padded to the 1024-byte swizzle atom).
+__host__ __device__ inline int gemm_act_box_stride(int S_pad) { return (S_pad * 128 + 1023) & ~1023; }
+__host__ __device__ inline int gemm_stage_bytes(int S_pad) {
+  return kKStage * (16384 + gemm_act_box_stride(S_pad));
 }
 __host__ __device__ inline int attn_stage_bytes(int D) {  // K tile + V tile (scales live apart)
   return 2 * kChunk * D;

@@ -154,13 +154,13 @@ extern "C" int wave_step_static(const wave_config* cfg, int S_max, int T_max, in
   }
   int tiles[kGemmKinds] = {0}, kblocks[kGemmKinds] = {0};
   tiles[kQKV] = (3 * HD + kTileM - 1) / kTileM;
-  kblocks[kQKV] = (d + kKBlk - 1) / kKBlk;
+  kblocks[kQKV] = (d + kKUnit - 1) / kKUnit;
   tiles[kO] = (d + kTileM - 1) / kTileM;
-  kblocks[kO] = (HD + kKBlk - 1) / kKBlk;
+  kblocks[kO] = (HD + kKUnit - 1) / kKUnit;
   tiles[kGU] = (F + 63) / 64;
-  kblocks[kGU] = (d + kKBlk - 1) / kKBlk;
+  kblocks[kGU] = (d + kKUnit - 1) / kKUnit;
   tiles[kDown] = (d + kTileM - 1) / kTileM;
-  kblocks[kDown] = (F + kKBlk - 1) / kKBlk;
+  kblocks[kDown] = (F + kKUnit - 1) / kKUnit;
   int mt = 1;
   for (int k = 0; k < 4; ++k) {
     if (tiles[k] > 1024 || max_segs(tiles[k], kblocks[k], sms, gemm_seg_cap(k)) > 64) return WAVE_EINVAL;
@@ -270,8 +270,8 @@ extern "C" int wave_step_static(const wave_config* cfg, int S_max, int T_max, in
     p.tiles[k] = tiles[k];
     p.kblocks[k] = kblocks[k];
   }
-  const int stride = 16384 + ((S_pad * 128 + 1023) & ~1023);
-  const int nst = smem_layout().ring_bytes / stride;
+  const int stride = gemm_stage_bytes(S_pad);
+  const int nst = smem_layout().gemm_ring_bytes / stride;
   p.nstage = nst > kMaxStages ? kMaxStages : nst;
   p.max_tiles_per_cta = mt;
   p.layer_elems = layer_elems;

@@ -102,6 +102,7 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
 // timeout_ns or when another CTA has recorded an error.
 __device__ bool grid_sync(const StepParams& p, Ctx& c) {
   fence_proxy_async_global();
+  fence_proxy_async_smem();  // this phase's generic shared accesses before the next one's copies
   __syncthreads();
   if (threadIdx.x == 0) {
     c.bar_target += gridDim.x;
@@ -232,7 +233,7 @@ __device__ void prefetch_gemm_weights(const StepParams& p, int kind, int layer) 
   for (long long u = sp.u0; u < sp.u1;) {
     const int t = (int)(u / KB);
     const long long e = min(sp.u1, (long long)(t + 1) * KB);
-    const int k0 = (int)(u - (long long)t * KB) * kKBlk, k1 = min(K, (int)(e - (long long)t * KB) * kKBlk);
+    const int k0 = (int)(u - (long long)t * KB) * kKUnit, k1 = min(K, (int)(e - (long long)t * KB) * kKUnit);
     for (int r = t * kTileM; r < min(N, (t + 1) * kTileM); ++r)
       bulk_prefetch_l2(W + (size_t)r * K + k0, (uint32_t)(k1 - k0) * 2u);
     u = e;
@@ -410,8 +411,10 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
   const int G = stream_k_ctas(gridDim.x, U, p.tiles[kind], gemm_seg_cap(kind)), cta = blockIdx.x;
   const Span sp = (cta < G) ? cta_span(U, G, cta) : Span{0, 0};
   const int S_pad = p.S_pad, nst = p.nstage;
+  // a stage: kKStage weight boxes, then kKStage activation boxes
   const uint32_t b_bytes = (uint32_t)S_pad * 128u;
-  const uint32_t stride = 16384u + ((b_bytes + 1023u) & ~1023u);
+  const uint32_t b_stride = (uint32_t)gemm_act_box_stride(S_pad);
+  const uint32_t stride = (uint32_t)gemm_stage_bytes(S_pad);
   const uint32_t ring = c.sbase + c.lay.ring_off;
 
   if (warp == 0) {
@@ -433,17 +436,23 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
             break;
           }
           const uint32_t fb = bar_full(c, slot);
-          mbar_arrive_expect_tx(fb, 16384u + b_bytes);
+          mbar_arrive_expect_tx(fb, (uint32_t)kKStage * (16384u + b_bytes));
           const uint32_t a = ring + slot * stride;
-          if (kind == kGU) {
-            tma_load_4d(a, wm, kb * kKBlk, t * 64, 0, layer, fb, pol);
-            tma_load_4d(a + 8192, wm, kb * kKBlk, t * 64, 1, layer, fb, pol);
-          } else if (kind == kIn || kind == kOut) {  // hybrid Mamba blocks: (place in group, group)
-            tma_load_4d(a, wm, kb * kKBlk, t * kTileM, layer % p.attn_every, layer / p.attn_every, fb, pol);
-          } else {
-            tma_load_3d(a, wm, kb * kKBlk, t * kTileM, layer, fb, pol);
+#pragma unroll
+          for (int bx = 0; bx < kKStage; ++bx) {
+            // K beyond the matrix (a ragged last unit) reads as zeros
+            const int k = (kb * kKStage + bx) * kKBlk;
+            const uint32_t wa = a + (uint32_t)bx * 16384u;
+            if (kind == kGU) {
+              tma_load_4d(wa, wm, k, t * 64, 0, layer, fb, pol);
+              tma_load_4d(wa + 8192, wm, k, t * 64, 1, layer, fb, pol);
+            } else if (kind == kIn || kind == kOut) {  // hybrid Mamba blocks: (place in group, group)
+              tma_load_4d(wa, wm, k, t * kTileM, layer % p.attn_every, layer / p.attn_every, fb, pol);
+            } else {
+              tma_load_3d(wa, wm, k, t * kTileM, layer, fb, pol);
+            }
+            tma_load_2d(a + (uint32_t)kKStage * 16384u + (uint32_t)bx * b_stride, xm, k, xrow0, fb);
           }
-          tma_load_2d(a + 16384, xm, kb * kKBlk, xrow0, fb);
           c.ring_it++;
         }
         u = e;
@@ -473,11 +482,13 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
             break;
           }
           tc_fence_after();
-          const uint32_t a = ring + slot * stride, bs = a + 16384u;
+          const uint32_t a = ring + slot * stride, bs = a + (uint32_t)kKStage * 16384u;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_bf16(dt, sdesc_sw128(a + kk * 32), sdesc_sw128(bs + kk * 32), idesc,
+          for (int kk = 0; kk < 4 * kKStage; ++kk) {
+            const uint32_t bx = (uint32_t)kk >> 2, off = (uint32_t)(kk & 3) * 32u;
+            tc_mma_bf16(dt, sdesc_sw128(a + bx * 16384u + off), sdesc_sw128(bs + bx * b_stride + off), idesc,
                         (kb > k0 || kk > 0) ? 1u : 0u);
+          }
           tc_commit(bar_empty(c, slot));
           c.ring_it++;
         }
