@@ -290,7 +290,7 @@ static bool hybrid_ok(const wave_hybrid_config* c) {
   if (c->head_dim != 64 && c->head_dim != 128) return false;
   if (c->n_heads < 1 || (c->n_heads * c->head_dim) % 64) return false;
   if (c->ssm_head_dim != kSsmP || c->ssm_state != kSsmN) return false;
-  if (c->ssm_heads < 4 || c->ssm_heads % 4) return false;
+  if (c->ssm_heads < 4 || c->ssm_heads % 4 || c->ssm_heads > kSsmMaxHeads) return false;
   if (!(c->rms_eps >= 0.f) || !(c->rope_base > 0.f)) return false;
   return true;
 }

@@ -30,6 +30,11 @@ constexpr int kGemmKinds = 7;
 constexpr int kSsmP = 64;
 constexpr int kSsmN = 128;
 constexpr int kSsmStages = 5;  // state items in flight per CTA (34 KB each)
+// A_log, dt_bias and D of every head are staged after the items in flight:
+// 5 x 34 KB + 3 x 1024 x 4 B fit the 200 KB ring.
+constexpr int kSsmMaxHeads = 1024;
+static_assert(kSsmStages * (kSsmP * kSsmN + 512) * 4 + 3 * kSsmMaxHeads * 4 <= 200 * 1024,
+              "state stages and per-head parameters exceed the ring");
 
 struct StepParams {
   CUtensorMap tm_w[kGemmKinds];  // weights of the projections (see GemmKind)

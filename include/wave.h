@@ -171,7 +171,7 @@ int wave_depth(wave_t* h, int S, int steps, const void* weights, const void* w_p
  * dt); per head dim p and state n: h = a h + dt x_p B_n (fp32 state, in
  * place), y_p = sum_n C_n h + D x_p; r += W_out bf16(y silu(z)).
  * Constraints: n_layers % attn_every == 0, ssm_head_dim 64, ssm_state 128,
- * ssm_heads a multiple of 4, the attention shapes of wave_config.
+ * ssm_heads a multiple of 4 and at most 1024, the attention shapes of wave_config.
  */
 typedef struct {
   int n_layers, d_model, attn_every;  /* layers; width; an attention block every attn_every layers */
