@@ -54,3 +54,9 @@ def test_hybrid_blob_layout_matches_the_generator(w):
     bad = fsd.WaveHybridConfig.of(w)
     bad.ssm_state = 64
     assert fsd.hybrid_weights_bytes(bad) == 0
+    # the per-head parameters are staged in shared memory: at most 1024 heads
+    many = fsd.WaveHybridConfig.of(w)
+    many.ssm_heads = 1028
+    assert fsd.hybrid_weights_bytes(many) == 0
+    many.ssm_heads = 1024
+    assert fsd.hybrid_weights_bytes(many) > 0
