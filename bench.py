@@ -53,6 +53,32 @@ def algorithmic_bytes(w, pos) -> int:
     return weights + kv_read + kv_write
 
 
+# The read-bound model of ttlab "voice-agent principles", §2 "Conversational
+# LLM": a step reads every weight once, so it cannot be shorter than its bytes
+# over the memory bandwidth; batching adds 2 flops per parameter per request
+# but no reads.  The page works examples of each relation;
+# tests/golden/roofline_examples.txt holds them.
+def read_bound_per_s(bandwidth_gbs, gb_per_unit):
+    """Units (tokens, steps) per second at most when each reads gb_per_unit GB."""
+    return bandwidth_gbs / gb_per_unit
+
+
+def fixed_cost_ms(rate_per_s, gb_per_unit, bandwidth_gbs):
+    """Time per unit beyond reading its bytes: 1 / rate - bytes / bandwidth (ms)."""
+    return 1e3 / rate_per_s - 1e3 * gb_per_unit / bandwidth_gbs
+
+
+def compute_bound_concurrency(tflops, bandwidth_gbs, bytes_per_param):
+    """Requests sharing one weight read past which their 2 flops per parameter
+    outrun the read: F * bytes_per_param / (2 * BW)."""
+    return tflops * 1e12 * bytes_per_param / (2.0 * bandwidth_gbs * 1e9)
+
+
+def matmul_tflops(params, rate_per_s):
+    """2 flops per parameter per token at rate_per_s tokens/s, in TFLOP/s."""
+    return 2.0 * params * rate_per_s / 1e12
+
+
 def algorithmic_flops(w, pos) -> int:
     L, H, D, d, F = w.n_layers, w.n_heads, w.head_dim, w.d_model, w.ffn
     HD = H * D
@@ -351,6 +377,7 @@ def run_gpu(args, w):
                          "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
                          "frac_of_8000": achieved / 8000.0,
                          "algorithmic_bytes_per_launch": bytes_step,
+                         "ceiling_value": S * world * read_bound_per_s(peak, bytes_step / 1e9),
                          "tflops": flops_step / (kern_ms * 1e-3) / 1e12},
             "e2e": {"value": job_throughput(world, S, e2e_ms), "unit": METRIC, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
