@@ -123,3 +123,64 @@ def test_sessions_are_independent_and_an_empty_slot_passes_through():
     y1, _ = oracle.hybrid_step(w, blob, kv1, sc1, st1, pos[keep], x[keep])
     assert np.array_equal(y[keep], y1)
     assert np.array_equal(st[:, keep], st1)
+
+
+def _blob_with_live_parameters(w, seed=11):
+    """The synthetic blob with every selective-state block's dt_bias and D
+    drawn away from their defaults (0 and 1), so that each enters the
+    frame with a non-trivial value; W_out and A_log as generated."""
+    blob = synth.hybrid_weights_host(w)
+    lay = synth.hybrid_layout(w)["mamba"]
+    rng = np.random.default_rng(seed)
+    for l in range(w.n_layers):
+        if w.is_attn(l):
+            continue
+        b = synth.hybrid_layer_offset(w, l)
+        blob[b + lay["dt_bias"]: b + lay["dt_bias"] + w.ssm_heads] = _bf16(rng.normal(0, 0.7, w.ssm_heads))
+        blob[b + lay["d_skip"]: b + lay["d_skip"] + w.ssm_heads] = _bf16(rng.normal(1, 0.5, w.ssm_heads))
+    return blob
+
+
+def test_hybrid_step_matches_independent_torch_restatement():
+    # every block at work: non-zero W_out, A_log ~ N(0, 1), dt_bias and D
+    # away from their defaults; the restatement has its own layout arithmetic,
+    # softplus, state update and FP8 codec (PyTorch's float8_e4m3fn)
+    import torch_ref
+    w = W
+    blob = _blob_with_live_parameters(w)
+    aw = w.attention_view()
+    pos = synth.positions(aw, w.S).copy()
+    pos[3] = -1  # an empty slot too
+    x = synth.x_bf16(aw, w.S)
+    kv, sc, st = oracle.hybrid_prefill(w, list(range(w.S)), pos)
+    kv2, sc2, st2 = kv.copy(), sc.copy(), st.copy()
+    _, ye = oracle.hybrid_step(w, blob, kv, sc, st, pos, x)
+    ref = torch_ref.hybrid_step(w, blob, kv2, sc2, st2, pos, x)
+    assert np.allclose(ye, ref, rtol=1e-9, atol=1e-9), float(np.max(np.abs(ye - ref)))
+    assert np.array_equal(kv, kv2)
+    assert np.array_equal(np.nan_to_num(sc, nan=-1.0), np.nan_to_num(sc2, nan=-1.0))
+    assert np.allclose(st, st2, rtol=2.0 ** -22, atol=0), float(np.max(np.abs(st - st2)))
+
+
+def test_selective_state_blocks_carry_weight_in_the_pinned_frame():
+    # the comparison above is not vacuous: dropping every selective-state
+    # block's output (W_out = 0) or its state (zeros) moves y far beyond the
+    # restatement's agreement
+    w = W
+    blob = _blob_with_live_parameters(w)
+    aw = w.attention_view()
+    pos = synth.positions(aw, w.S)
+    x = synth.x_bf16(aw, w.S)
+    kv, sc, st = oracle.hybrid_prefill(w, list(range(w.S)), pos)
+    _, ye = oracle.hybrid_step(w, blob, kv.copy(), sc.copy(), st.copy(), pos, x)
+    cut = blob.copy()
+    m = synth.hybrid_layout(w)["mamba"]
+    for l in range(w.n_layers):
+        if not w.is_attn(l):
+            b = synth.hybrid_layer_offset(w, l) + m["w_out"]
+            cut[b: b + w.d_model * w.d_inner] = 0
+    _, ye_cut = oracle.hybrid_step(w, cut, kv.copy(), sc.copy(), st.copy(), pos, x)
+    _, ye_zero = oracle.hybrid_step(w, blob, kv.copy(), sc.copy(), np.zeros_like(st), pos, x)
+    scale = np.max(np.abs(ye))
+    assert np.max(np.abs(ye - ye_cut)) > 1e-2 * scale
+    assert np.max(np.abs(ye - ye_zero)) > 1e-2 * scale
