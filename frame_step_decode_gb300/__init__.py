@@ -49,7 +49,8 @@ class WaveError(RuntimeError):
 _lib = None
 EXPORTS = ("wave_create", "wave_destroy", "wave_weights_bytes", "wave_weight_offset", "wave_step", "wave_beat", "wave_depth",
            "wave_status", "wave_strerror", "wave_kv_quantize", "wave_fp8_encode", "wave_step_static",
-           "wave_set_timeout_ns", "wave_debug_skip_barrier", "wave_debug_dump_kv", "wave_debug_phase_times", "wave_debug_arrival_times",
+           "wave_set_timeout_ns", "wave_debug_skip_barrier", "wave_debug_dump_kv", "wave_debug_dump_acts",
+           "wave_debug_act_record_floats", "wave_debug_phase_times", "wave_debug_arrival_times",
            "wave_grid_size", "wave_barriers_per_step", "wave_hybrid_create", "wave_hybrid_step",
            "wave_hybrid_weights_bytes", "wave_hybrid_layer_offset")
 
@@ -100,6 +101,10 @@ def lib() -> ctypes.CDLL:
         L.wave_debug_skip_barrier.restype = i32
         L.wave_debug_dump_kv.argtypes = [vp, vp]
         L.wave_debug_dump_kv.restype = i32
+        L.wave_debug_dump_acts.argtypes = [vp, vp, i32]
+        L.wave_debug_dump_acts.restype = i32
+        L.wave_debug_act_record_floats.argtypes = [vp]
+        L.wave_debug_act_record_floats.restype = ctypes.c_longlong
         L.wave_debug_phase_times.argtypes = [vp, vp]
         L.wave_debug_phase_times.restype = i32
         L.wave_debug_arrival_times.argtypes = [vp, vp]
@@ -180,7 +185,13 @@ class Wave:
             raise WaveError(rc, "wave_beat")
         return rc
 
-    def status(self) -> int:
+    def status(self, sync: bool = True) -> int:
+        """wave_status.  The C call synchronises nothing and reports the
+        launches already finished; with sync (the default) the device is
+        synchronised first, so that it reports every launch made so far."""
+        if sync:
+            import torch
+            torch.cuda.synchronize()
         return lib().wave_status(self.h)
 
     def set_timeout_ns(self, ns: int) -> None:
@@ -195,6 +206,18 @@ class Wave:
         """Testing hook: later steps write their pre-quantisation K/V rows
         into dst ([L][2][S_max][H][D] fp32 on the device); None disables."""
         lib().wave_debug_dump_kv(self.h, _ptr(dst))
+
+    def debug_dump_acts(self, dst, n_sessions: int = 0) -> None:
+        """Testing hook: later launches record every phase's input and output
+        for sessions 0..n_sessions-1 into dst ([frames][layers][n][R] fp32 on
+        the device, R = act_record_floats); None disables."""
+        rc = lib().wave_debug_dump_acts(self.h, _ptr(dst), n_sessions if dst is not None else 0)
+        if rc != WAVE_OK:
+            raise WaveError(rc, "wave_debug_dump_acts")
+
+    @property
+    def act_record_floats(self) -> int:
+        return lib().wave_debug_act_record_floats(self.h)
 
     def debug_phase_times(self, dst) -> None:
         """Profiling hook: later steps write globaltimer stamps (int64) at

@@ -81,11 +81,16 @@ struct StepParams {
   int4* pieces;          // [2 * max pieces] (sh, c_lo | c_hi << 16, pieces of sh, first slot), (pos, 0, 0, 0)
   int* n_pieces;         // [1]
   const float2* rope;    // [T_max][D/2] (cos, sin)
-  unsigned* bar;         // grid barrier counter (zeroed before each launch)
+  unsigned* bar;         // [0] grid barrier counter, [1] CTAs finished (both zeroed before each launch)
   int* err;              // error bits (sticky until wave_status)
   long long timeout_ns;
   int skip_cta, skip_bar;
   float* kv_dump;        // testing hook: [L][2][S_max][H][D] pre-quantisation K/V, or null
+  float* act_dump;       // testing hook: [frames][L][act_dump_n][act_rec] phase inputs/outputs, or null
+  int act_dump_n;        // sessions 0..act_dump_n-1 are recorded
+  int act_n1, act_n2;    // record sections: input-projection output, mixer output (floats)
+  long long act_rec;     // floats per record
+  int* err_out;          // if set: the last CTA to finish copies *err here (a mapped host word)
   long long* phase_ts;   // profiling hook: globaltimer at start, after each barrier, at end
   long long* arrive_ts;  // profiling hook: [barrier][cta] globaltimer at barrier arrival
 };

@@ -20,7 +20,7 @@
 // Around the layers: a prologue (work list, residual from x, first norm);
 // several frames per launch (beats) with positions + f; chained frames (the
 // depth loop) with x_f = bf16(W_p y_{f-1}) between them.  The hybrid model
-// (step_kernel<true>) replaces the MLP half by nothing and, in all but every
+// (step_kernel<true, ...>) replaces the MLP half by nothing and, in all but every
 // attn_every-th layer, attention by a selective-state block: in-projection,
 // state update, out-projection + residual.
 //
@@ -217,27 +217,44 @@ __device__ __forceinline__ int owner_of(long long U, int G, long long u) {
 }
 
 
-// Prefetch into L2 the weight rows this CTA will stream in GEMM `kind` of
-// `layer` (its stream-K span), so that the phase reads them from L2.  Issued
-// by one thread while an earlier phase streams other data from HBM.
-__device__ void prefetch_gemm_weights(const StepParams& p, int kind, int layer) {
+// Issue L2 prefetches of the weight boxes this CTA streams in GEMM `kind` of
+// `layer` (its stream-K span), from the unit `skip` units into the span, at
+// most `units` units; one tensor-map box per instruction, the producer's
+// boxes and coordinates.
+__device__ __noinline__ void prefetch_gemm_span(const StepParams& p, int kind, int layer, int skip, int units) {
   const int KB = p.kblocks[kind], T = p.tiles[kind];
   const long long U = (long long)T * KB;
+  if (U == 0 || units <= 0) return;
   const int G = stream_k_ctas(gridDim.x, U, T, gemm_seg_cap(kind)), cta = blockIdx.x;
   if (cta >= G) return;
   const Span sp = cta_span(U, G, cta);
-  const int K = (kind == kO) ? p.HD : p.F;   // O and down only
-  const int N = p.d;
-  const uint16_t* W = p.weights + (size_t)layer * p.layer_elems +
-                      (kind == kO ? p.off_wo : p.off_wdown);
-  for (long long u = sp.u0; u < sp.u1;) {
-    const int t = (int)(u / KB);
-    const long long e = min(sp.u1, (long long)(t + 1) * KB);
-    const int k0 = (int)(u - (long long)t * KB) * kKUnit, k1 = min(K, (int)(e - (long long)t * KB) * kKUnit);
-    for (int r = t * kTileM; r < min(N, (t + 1) * kTileM); ++r)
-      bulk_prefetch_l2(W + (size_t)r * K + k0, (uint32_t)(k1 - k0) * 2u);
-    u = e;
+  const CUtensorMap* wm = &p.tm_w[kind];
+  const long long u_end = min(sp.u1, sp.u0 + skip + units);
+  for (long long u = sp.u0 + skip; u < u_end; ++u) {
+    const int t = (int)(u / KB), kb = (int)(u - (long long)t * KB);
+#pragma unroll
+    for (int bx = 0; bx < kKStage; ++bx) {
+      const int k = (kb * kKStage + bx) * kKBlk;
+      if (kind == kGU) {
+        tma_prefetch_4d(wm, k, t * 64, 0, layer);
+        tma_prefetch_4d(wm, k, t * 64, 1, layer);
+      } else if (kind == kIn || kind == kOut) {
+        tma_prefetch_4d(wm, k, t * kTileM, layer % p.attn_every, layer / p.attn_every);
+      } else {
+        tma_prefetch_3d(wm, k, t * kTileM, layer);
+      }
+    }
   }
+}
+// Units of this CTA's span in GEMM `kind` (0 if it takes no part).
+__device__ __forceinline__ int span_units(const StepParams& p, int kind) {
+  const int KB = p.kblocks[kind], T = p.tiles[kind];
+  const long long U = (long long)T * KB;
+  if (U == 0) return 0;
+  const int G = stream_k_ctas(gridDim.x, U, T, gemm_seg_cap(kind));
+  if ((int)blockIdx.x >= G) return 0;
+  const Span sp = cta_span(U, G, blockIdx.x);
+  return (int)(sp.u1 - sp.u0);
 }
 
 __device__ __forceinline__ float4 ld4cg(const float* q) { return __ldcg((const float4*)q); }
@@ -632,7 +649,7 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   const uint64_t kv_policy = policy_evict_first();
   // the output projection's weights are read next: bring them into L2 now
-  if (warp == kWarps - 1 && lane == 0) prefetch_gemm_weights(p, kO, layer);
+  if (warp == kWarps - 1 && lane == 0) prefetch_gemm_span(p, kO, layer, 0, span_units(p, kO));
   __syncwarp();
 
   // Dynamic assignment over the longest-first list: warp gw starts with entry
@@ -1272,10 +1289,47 @@ __device__ void build_pieces(const StepParams& p, Ctx& c) {
   __syncthreads();
 }
 
+// ------------------------------------------------------------ testing hook
+// Activation dump: copies rows 0..act_dump_n-1 of a workspace buffer (fp32
+// or bf16, row stride ld, n values per row) into section `off` of the
+// record of (frame, layer, session).  Runs on all CTAs right after the grid
+// barrier that ends the buffer's producing phase; the buffer is only read
+// until the next barrier, so the copy sees its final values.
+enum ActSection : int { kActIn = 0, kActXn1, kActProj, kActMix, kActMid, kActXn2, kActU, kActOut };
+__device__ __forceinline__ long long act_off(const StepParams& p, int sec) {
+  const long long d = p.d, n1 = p.act_n1, n2 = p.act_n2;
+  switch (sec) {
+    case kActIn: return 0;
+    case kActXn1: return d;
+    case kActProj: return 2 * d;
+    case kActMix: return 2 * d + n1;
+    case kActMid: return 2 * d + n1 + n2;
+    case kActXn2: return 3 * d + n1 + n2;
+    case kActU: return 4 * d + n1 + n2;
+    default: return 4 * d + n1 + n2 + p.F;
+  }
+}
+template <typename T>
+__device__ __noinline__ void act_dump_rows(const StepParams& p, int frame, int layer, int sec, const T* src,
+                                           int ld, int n) {
+  const int ns = p.act_dump_n;
+  const long long off = act_off(p, sec);
+  const int total = ns * n;
+  for (int i = blockIdx.x * kThreads + threadIdx.x; i < total; i += gridDim.x * kThreads) {
+    const int s = i / n, e = i - s * n;
+    float v;
+    if constexpr (sizeof(T) == 2) v = bf16_to_f32(__ldcg((const unsigned short*)src + (size_t)s * ld + e));
+    else v = __ldcg((const float*)src + (size_t)s * ld + e);
+    p.act_dump[(((long long)frame * p.L + layer) * ns + s) * p.act_rec + off + e] = v;
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 // kHybrid selects the hybrid model's layer loop at compile time, so that each
-// model's kernel is register-allocated for its own phases only.
-template <bool kHybrid>
+// model's kernel is register-allocated for its own phases only.  kDump adds
+// the activation-dump testing hook; launches without it run the kernel that
+// has no trace of it (same phases, same arithmetic).
+template <bool kHybrid, bool kDump>
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepParams p) {
   extern __shared__ uint8_t smem_raw[];
   Ctx c;
@@ -1359,9 +1413,17 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         const bool nok = norm_phase(p, c, wl + p.off_g_attn, false);
         if (!(ok = grid_sync(p, c) && nok)) break;
       }
+      if (kDump) {  // the layer's input residual and its normed input
+        act_dump_rows(p, c.frame, l, kActIn, p.resid, p.d, p.d);
+        act_dump_rows(p, c.frame, l, kActXn1, p.xn, p.d, p.d);
+      }
       // the block's input projection: QKV, or the selective-state in-projection
       gemm_phase(p, c, attn_layer ? kQKV : kIn, li, false);
       if (!(ok = grid_sync(p, c))) break;
+      if (kDump) {
+        if (attn_layer) act_dump_rows(p, c.frame, l, kActProj, p.qkv, 3 * p.HD, 3 * p.HD);
+        else act_dump_rows(p, c.frame, l, kActProj, p.zx, p.in_rows, p.in_rows);
+      }
       if (attn_layer) {
         if (p.D == 128) attention_phase<128>(p, c, li); else attention_phase<64>(p, c, li);
         if (!(ok = grid_sync(p, c))) break;
@@ -1369,21 +1431,30 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
           if (p.D == 128) merge_phase<128>(p, c); else merge_phase<64>(p, c);
           if (!(ok = grid_sync(p, c))) break;
         }
+        if (kDump) act_dump_rows(p, c.frame, l, kActMix, p.attn, p.HD, p.HD);
       } else if constexpr (kHybrid) {
         const bool sok = ssm_phase(p, c, l - l / e, l);
         if (!(ok = grid_sync(p, c) && sok)) break;
+        if (kDump) act_dump_rows(p, c.frame, l, kActMix, p.ssm_out, p.d_inner, p.d_inner);
       }
       // and its output projection + residual: O, or the selective-state out-projection
-      gemm_phase(p, c, attn_layer ? kO : kOut, li, hyb && last);
-      if constexpr (!kHybrid) {
+      if constexpr (kHybrid) {
+        gemm_phase(p, c, attn_layer ? kO : kOut, li, last);
+      } else {
+        gemm_phase(p, c, kO, li, false);
         if (!(ok = grid_sync(p, c))) break;
+        if (kDump) act_dump_rows(p, c.frame, l, kActMid, p.resid, p.d, p.d);
         const bool nok2 = norm_phase(p, c, wl + p.off_g_mlp, false);
         if (!(ok = grid_sync(p, c) && nok2)) break;
+        if (kDump) act_dump_rows(p, c.frame, l, kActXn2, p.xn, p.d, p.d);
         gemm_phase(p, c, kGU, l, false);
         if (!(ok = grid_sync(p, c))) break;
+        if (kDump) act_dump_rows(p, c.frame, l, kActU, p.u, p.F, p.F);
         gemm_phase(p, c, kDown, l, last);
       }
       if (!last && !(ok = grid_sync(p, c))) break;
+      // the block's output residual (the last layer's is y, rounded)
+      if (kDump && !last) act_dump_rows(p, c.frame, l, kHybrid ? kActMid : kActOut, p.resid, p.d, p.d);
     }
   }
   // rolling positions: every frame has read them; advance once all are done
@@ -1415,19 +1486,34 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   __syncthreads();
   if (p.phase_ts && blockIdx.x == 0 && threadIdx.x == 0) p.phase_ts[1 + c.bar_index] = globaltimer();
   if (warp == 1) tmem_dealloc(c.tmem, kTmemCols);
+  // the last CTA to finish copies the error word to the caller-visible host
+  // word, so that reading the status needs no copy or synchronisation
+  if (p.err_out && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.bar + 1, 1u) == gridDim.x - 1) {
+      const int e = atomicOr(p.err, 0);
+      *(volatile int*)p.err_out = e;
+      __threadfence_system();
+    }
+  }
 }
 
+// The four instantiations: decoder / hybrid, without / with the dump hook.
+static const void* const kKernels[4] = {(const void*)step_kernel<false, false>, (const void*)step_kernel<true, false>,
+                                        (const void*)step_kernel<false, true>, (const void*)step_kernel<true, true>};
+
 cudaError_t configure_step_kernel() {
-  cudaError_t e = cudaFuncSetAttribute(step_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem_layout().total);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(step_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              smem_layout().total);
+  for (const void* fn : kKernels) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_layout().total);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_step(const StepParams& p, int grid, cudaStream_t stream) {
   void* args[] = {(void*)&p};
-  const void* fn = p.hybrid ? (const void*)step_kernel<true> : (const void*)step_kernel<false>;
+  const void* fn = kKernels[(p.hybrid ? 1 : 0) + (p.act_dump ? 2 : 0)];
   return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), args, (size_t)smem_layout().total,
                                      stream);
 }
@@ -1447,14 +1533,16 @@ int barriers_per_launch(int L, int T_max, int frames, bool advance, bool depth) 
 }
 
 cudaError_t occupancy_per_sm(int* blocks) {
-  int a = 0, b = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, step_kernel<false>, kThreads,
-                                                                (size_t)smem_layout().total);
-  if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, step_kernel<true>, kThreads,
-                                                    (size_t)smem_layout().total);
-  *blocks = a < b ? a : b;
-  return e;
+  int lo = 1 << 30;
+  for (const void* fn : kKernels) {
+    int a = 0;
+    const cudaError_t e =
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, fn, kThreads, (size_t)smem_layout().total);
+    if (e != cudaSuccess) return e;
+    if (a < lo) lo = a;
+  }
+  *blocks = lo;
+  return cudaSuccess;
 }
 
 }  // namespace wave

@@ -57,24 +57,33 @@ typedef struct wave_ctx wave_t; /* opaque; owns only its device workspace */
 
 /*
  * Create a step context for at most S_max sessions (1..128) and a history of
- * T_max slots per session (a multiple of 4).  This is the pages' "profile per
- * model, session capacity and context length" (dotwave.ai "04 / Under the
- * hood").  Allocates the device workspace on the current device (activations,
- * partial sums, the RoPE cos/sin table, barrier words); about
- * 0.5 MB + S_max * (2.1 * d_model + ...) bytes, e.g. ~60 MB for the 7B-class
- * shape at S_max = 128.  Returns WAVE_EINVAL for a bad shape, WAVE_EDEVICE off
- * sm_103, WAVE_ENOMEM/WAVE_ECUDA on failure; *out is set only on success.
+ * T_max slots per session (a multiple of 4): the dotwave.ai case study ("04 /
+ * Under the hood") builds one engine profile per model, session capacity and
+ * context length, and a handle is that profile here.  Allocates the device
+ * workspace on the current device (activations, partial sums, the RoPE
+ * cos/sin table, barrier words; about 0.5 MB + S_max * (2.1 * d_model + ...)
+ * bytes, e.g. ~60 MB for the 7B-class shape at S_max = 128) and one pinned,
+ * device-mapped host word for the error status.  Returns WAVE_EINVAL for a
+ * bad shape, WAVE_EDEVICE off sm_103, WAVE_ENOMEM/WAVE_ECUDA on failure;
+ * *out is set only on success.
  */
 int wave_create(const wave_config* cfg, int S_max, int T_max, wave_t** out);
 
-/* Free the workspace.  Waits for the handle's work to finish.  NULL is a no-op. */
+/* Free the workspace (the end of the per-session state's residence that
+ * the dotwave.ai case study, "02 / The solution", keeps between beats; the
+ * caller's history buffers are untouched).  Waits for the device to finish
+ * the handle's work first.  NULL is a no-op. */
 void wave_destroy(wave_t* h);
 
-/* Bytes of the bf16 weight blob for cfg (see wave_weight_offset). */
+/* Bytes of the bf16 weight blob for cfg (see wave_weight_offset): the bf16
+ * weights of the narilabs blog, "Compressing the Temporal KV cache", laid
+ * out as below.  0 for an invalid shape. */
 size_t wave_weights_bytes(const wave_config* cfg);
 
 /*
- * Byte offset inside the weight blob of one tensor of one layer.  which:
+ * Byte offset inside the weight blob of one tensor of one layer (the pages
+ * fix no layout; this is the library's, in nn.Linear [out][in] order so
+ * that every row streams contiguously).  which:
  *   0 g_attn  [d]            RMSNorm gain before attention
  *   1 Wqkv    [3*H*D][d]     rows: q (H*D), then k (H*D), then v (H*D)
  *   2 Wo      [d][H*D]
@@ -88,8 +97,9 @@ size_t wave_weight_offset(const wave_config* cfg, int layer, int which);
 
 /*
  * One frame for sessions 0..S-1 (1 <= S <= S_max).  Asynchronous: enqueues
- * two operations on `stream` (a 4-byte memset of the barrier word and one
- * cooperative kernel launch) and returns; nothing is synchronised.
+ * two operations on `stream` (an 8-byte memset of the barrier and exit
+ * counters and one cooperative kernel launch) and returns; nothing is
+ * synchronised.
  *
  *   weights    bf16 blob, layout of wave_weight_offset, 16-byte aligned, read only.
  *   kv_fp8     uint8 [L][2][S_max][H][T_max][D] E4M3 codes (index 0 = K, 1 = V),
@@ -160,7 +170,8 @@ int wave_depth(wave_t* h, int S, int steps, const void* weights, const void* w_p
                float* kv_scales, const void* x0, void* xs, void* y, void* stream);
 
 /*
- * The hybrid recurrent step (BASELINE-style config: the NemotronH-style
+ * The hybrid recurrent step (e.g. 48 layers of width 4096, an attention
+ * block every sixth layer, 64 state heads of 64 x 128: the NemotronH-style
  * thinker of the vllm-omni recipe page, "Summary", whose recurrent state is
  * FP32 per the dotwave.ai profile.json): n_layers pre-norm residual blocks
  * without MLPs; layer l is an attention block (RMSNorm, QKV, RoPE, FP8 K/V
@@ -205,14 +216,24 @@ int wave_hybrid_step(wave_t* h, int S, const void* weights, uint8_t* kv_fp8, flo
                      float* ssm_state, const int32_t* positions, const void* x, void* y, void* stream);
 
 /*
- * Synchronise the stream of the last launch on this handle, then return
- * and clear the device error word: WAVE_OK, WAVE_ETIMEOUT (a device wait gave
- * up; the step's outputs are undefined, the GPU context stays usable) or
- * WAVE_EPOS.  Returns WAVE_ECUDA if the synchronisation itself failed.
+ * The error status of the handle's launches, read without synchronising
+ * anything: every launch's last CTA copies the device error word into a
+ * pinned host word as the kernel ends, and wave_status reads that word.  So
+ * call it after the caller has synchronised with the launches it asks
+ * about (stream or event synchronisation); before that it reports only the
+ * launches already finished.  The bits are sticky across launches until
+ * read: a non-OK result clears them (host word now, device word by an
+ * asynchronous memset enqueued on the handle's last stream).  Returns
+ * WAVE_OK, WAVE_ETIMEOUT (a device wait gave up; that step's outputs are
+ * undefined, the GPU context stays usable) or WAVE_EPOS; WAVE_ECUDA if the
+ * clearing memset could not be enqueued.  This is the step's own failure
+ * report: the pages describe none (their only recovery, the vllm-omni recipe
+ * page's eager fallback in "Notes", is a second code path this library does
+ * not have), so errors become status codes and no device wait is unbounded.
  */
 int wave_status(wave_t* h);
 
-/* Static description of a return code. */
+/* Static description of a return code (see wave_status). */
 const char* wave_strerror(int code);
 
 /*
@@ -265,6 +286,27 @@ int wave_debug_skip_barrier(wave_t* h, int cta, int barrier);
  * [L][2][S_max][H][D] floats, so that tests can check the append bit for bit
  * against a reference quantiser.  dst = NULL disables. */
 int wave_debug_dump_kv(wave_t* h, float* dst);
+/* Activation dump: make later launches (any number of frames) record, for
+ * sessions 0..n_sessions-1, every phase's input and output as fp32 values
+ * into dst (device, 16-byte aligned): [frames][layers][n_sessions][R] floats,
+ * R = wave_debug_act_record_floats(h), layers = the model's layer count.
+ * Record of a layer, in this order (d model width, F the MLP width; N1 =
+ * max(3 H D, the hybrid in-projection rows), N2 = max(H D, the hybrid
+ * d_inner)):
+ *   [0, d)          the layer's input residual (fp32)
+ *   [d, 2d)         its RMS-normed input xn (bf16 values)
+ *   [2d, 2d+N1)     the input projection's output: q, k, v before RoPE, or the
+ *                   selective-state block's z, x, B, C, dt (fp32)
+ *   [.., +N2)       the attention output (bf16) or the gated mixer output (bf16)
+ *   [.., +d)        decoder: residual after O; hybrid: the block's output residual
+ *   [.., +d)        decoder: the MLP's normed input (bf16)
+ *   [.., +F)        decoder: the SwiGLU output u (bf16)
+ *   [.., +d)        decoder: the layer's output residual (fp32)
+ * The last layer's output residual is not recorded (y holds it, rounded).
+ * The dump runs a second instantiation of the step kernel that differs from
+ * the usual one only by these copies.  dst = NULL disables. */
+int wave_debug_dump_acts(wave_t* h, float* dst, int n_sessions);
+long long wave_debug_act_record_floats(wave_t* h);
 /* Profiling hook: make later steps record %globaltimer (ns) into dst, a device
  * buffer of wave_barriers_per_step(h) + 2 int64: [0] at kernel entry, [1+b]
  * when grid barrier b released CTA 0, and the last entry at kernel exit.

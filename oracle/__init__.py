@@ -69,6 +69,8 @@ def lib():
         L.oracle_hybrid_step.restype = i32
         L.oracle_ssm_mixer.argtypes = [ctypes.POINTER(OracleHybridCfg), vp, vp, vp, vp, vp, vp, vp]
         L.oracle_ssm_mixer.restype = None
+        L.oracle_ssm_update.argtypes = [ctypes.POINTER(OracleHybridCfg), vp, vp, vp, vp, vp, vp]
+        L.oracle_ssm_update.restype = None
         L.oracle_hybrid_layer_offset.argtypes = [ctypes.POINTER(OracleHybridCfg), i32]
         L.oracle_hybrid_layer_offset.restype = i64
         L.oracle_proj.argtypes = [vp, i32, i32, vp, vp]
@@ -287,4 +289,19 @@ def ssm_mixer(w, w_in: np.ndarray, a_log: np.ndarray, dt_bias: np.ndarray, d_ski
     lib().oracle_ssm_mixer(ctypes.byref(c), _p(np.ascontiguousarray(w_in)), _p(np.ascontiguousarray(a_log)),
                            _p(np.ascontiguousarray(dt_bias)), _p(np.ascontiguousarray(d_skip)), _p(xn),
                            _p(state), _p(out))
+    return out
+
+
+def ssm_update(w, zx: np.ndarray, a_log: np.ndarray, dt_bias: np.ndarray, d_skip: np.ndarray,
+               state: np.ndarray) -> np.ndarray:
+    """The state update and gated output of one Mamba2-style block for one
+    session from its in-projection output zx (fp64 [in_rows]): state fp32
+    [Hs][P][N] updated in place; returns the gated output (unrounded) [d_i]."""
+    c = hybrid_cfg_of(w)
+    out = np.empty(w.d_inner, dtype=np.float64)
+    zx = np.ascontiguousarray(zx, dtype=np.float64)
+    assert state.flags["C_CONTIGUOUS"] and state.dtype == np.float32
+    lib().oracle_ssm_update(ctypes.byref(c), _p(zx), _p(np.ascontiguousarray(a_log)),
+                            _p(np.ascontiguousarray(dt_bias)), _p(np.ascontiguousarray(d_skip)), _p(state),
+                            _p(out))
     return out

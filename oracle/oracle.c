@@ -317,10 +317,12 @@ void oracle_proj(const uint16_t* wp, int d, int n, const uint16_t* y, uint16_t* 
 }
 
 /* ------------------------------------------------------------------ hybrid
- * The hybrid recurrent step (BASELINE config 5, the NemotronH-style thinker
- * of the vllm-omni recipe page, "Summary"; "recurrent_state": "FP32" in the
- * dotwave.ai profile.json).  The pages give no layer definition; readings:
- * every layer is a pre-norm residual block without an MLP.  Layer l is an
+ * The hybrid recurrent step (48 layers of width 4096 at full size, an
+ * attention block every sixth layer, 64 state heads of 64 x 128: the
+ * NemotronH-style thinker of the vllm-omni recipe page, "Summary";
+ * "recurrent_state": "FP32" in the dotwave.ai profile.json).  The pages give
+ * no layer definition; readings: every layer is a pre-norm residual block
+ * without an MLP.  Layer l is an
  * attention block (the decoder's attention half: RMSNorm, QKV, RoPE, FP8
  * append, attention, O) when l % attn_every == attn_every - 1, else a
  * Mamba2-style selective-state block:
@@ -358,15 +360,16 @@ int64_t oracle_hybrid_layer_offset(const oracle_hybrid_cfg* c, int l) {
 
 static double oracle_softplus(double v) { return v > 0 ? v + log1p(exp(-v)) : log1p(exp(v)); }
 
-/* One Mamba2-style block's mixer for one session: xn (bf16-rounded) in, the
- * gated output out[d_i] (bf16-rounded) and the state [Hs][P][N] updated. */
-void oracle_ssm_mixer(const oracle_hybrid_cfg* c, const uint16_t* w_in, const uint16_t* a_log,
-                      const uint16_t* dt_bias, const uint16_t* dskip, const double* xn,
-                      float* state, double* out) {
-  const int d = c->d_model, Hs = c->ssm_heads, P = c->ssm_head_dim, N = c->ssm_state;
-  const int di = Hs * P, rows = 2 * di + 2 * N + Hs;
-  double* zx = (double*)malloc(sizeof(double) * rows);
-  oracle_matvec(w_in, rows, d, xn, zx);
+/* The state update and gated output of one Mamba2-style block for one
+ * session, from its in-projection output zx = [z d_i | x d_i | B N | C N |
+ * dt Hs]: per head dt = softplus(dt + dt_bias), a = exp(dt * -exp(A_log)); per
+ * head dim p and state n the state becomes a h + dt B[n] x[p], stored in fp32
+ * (the state is fp32), y[p] = sum_n C[n] h[p][n] + D x[p] over the stored
+ * values, out[p] = y[p] silu(z[p]) (unrounded).  state is [Hs][P][N]. */
+void oracle_ssm_update(const oracle_hybrid_cfg* c, const double* zx, const uint16_t* a_log,
+                       const uint16_t* dt_bias, const uint16_t* dskip, float* state, double* out) {
+  const int Hs = c->ssm_heads, P = c->ssm_head_dim, N = c->ssm_state;
+  const int di = Hs * P;
   const double* z = zx;
   const double* xs = zx + di;
   const double* B = zx + 2 * di;
@@ -390,6 +393,18 @@ void oracle_ssm_mixer(const oracle_hybrid_cfg* c, const uint16_t* w_in, const ui
       out[hh * P + p] = y * oracle_silu(z[hh * P + p]);
     }
   }
+}
+
+/* One Mamba2-style block's mixer for one session: xn (bf16-rounded) in,
+ * zx = W_in xn, then the state update and gated output above. */
+void oracle_ssm_mixer(const oracle_hybrid_cfg* c, const uint16_t* w_in, const uint16_t* a_log,
+                      const uint16_t* dt_bias, const uint16_t* dskip, const double* xn,
+                      float* state, double* out) {
+  const int d = c->d_model, di = c->ssm_heads * c->ssm_head_dim;
+  const int rows = 2 * di + 2 * c->ssm_state + c->ssm_heads;
+  double* zx = (double*)malloc(sizeof(double) * rows);
+  oracle_matvec(w_in, rows, d, xn, zx);
+  oracle_ssm_update(c, zx, a_log, dt_bias, dskip, state, out);
   free(zx);
 }
 
