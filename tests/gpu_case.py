@@ -179,3 +179,19 @@ def codes_vs_oracle(gpu_codes, gpu_pre, ora_codes, ora_scales, ora_pre):
     assert np.all((signed(lo) <= gs) & (gs <= signed(hi))), \
         "a code differs by more than the two paths' difference can explain"
     return n
+
+
+def dump_acts(wave, n, frames, run):
+    """Run `run()` (one launch on `wave`) with the activation dump on for
+    sessions 0..n-1 and return its records [frames][layers][n][R] (host
+    fp32).  The launch's other outputs are the caller's to read."""
+    layers = wave.cfg.n_layers
+    buf = torch.full((frames, layers, n, wave.act_record_floats), float("nan"), dtype=torch.float32,
+                     device="cuda")
+    wave.debug_dump_acts(buf, n)
+    try:
+        run()
+        assert wave.status() == fsd.WAVE_OK
+    finally:
+        wave.debug_dump_acts(None)
+    return buf.cpu().numpy()

@@ -12,7 +12,11 @@ shapes of test_gpu_step.py, is replaced here by: (a) every appended FP8 code
 and scale bit-exact against the oracle's quantiser on the GPU's own
 pre-quantisation rows, (b) layer-0 K/V rows (before any cascade) within
 1e-4 of the oracle's, and (c) y within three times the oracle's own
-one-ulp sensitivity, normwise, and never above 5e-2.
+one-ulp sensitivity, normwise, and never above 5e-2.  And (d) every phase of
+every one of the 32 layers, for the first sessions, against the oracle's
+functions applied to the GPU's own inputs to that phase: no cascade reaches a
+phase checked on its own inputs, so each is held to the stated element-wise
+bound and to a tight bound that a 1% error anywhere fails.
 """
 import numpy as np
 import pytest
@@ -21,7 +25,8 @@ import torch
 import frame_step_decode_gb300 as fsd
 import oracle
 import synth
-from gpu_case import DeviceCase, codes_vs_oracle, y_close
+import phase_check
+from gpu_case import DeviceCase, codes_vs_oracle, dump_acts, y_close
 
 pytestmark = pytest.mark.gpu
 
@@ -40,19 +45,24 @@ def big():
     torch.cuda.empty_cache()
 
 
+@pytest.fixture(scope="module")
+def W7():
+    return synth.weights_host(synth.SEVEN_B)
+
+
 def _sample(pos):
     order = np.argsort(pos)
     return sorted({int(order[0]), int(order[-1]), int(order[len(order) // 2]), 17})
 
 
-def test_device_generator_matches_host_generator(big):
+def test_device_generator_matches_host_generator(big, W7):
     case, _ = big
-    W = synth.weights_host(case.w)
+    W = W7
     assert torch.equal(case.weights.view(torch.int16),
                        torch.from_numpy(W.view(np.int16)).to("cuda"))
 
 
-def test_full_size_step_matches_oracle_on_sampled_sessions(big):
+def test_full_size_step_matches_oracle_on_sampled_sessions(big, W7):
     case, wave = big
     w = case.w
     sess = _sample(case.pos_h)
@@ -73,7 +83,7 @@ def test_full_size_step_matches_oracle_on_sampled_sessions(big):
     finally:
         wave.debug_dump_kv(None)
     y = case.y_bits()
-    W = synth.weights_host(w)
+    W = W7
     kv_in, sc_in = kv_o.copy(), sc_o.copy()
     _, y_exact, kv_new = oracle.step(w, W, kv_o, sc_o, case.pos_h[sess], case.x_h[sess], want_kv_new=True)
     # the oracle's own sensitivity: one element of x moved by one bf16 ulp
@@ -102,3 +112,23 @@ def test_full_size_step_matches_oracle_on_sampled_sessions(big):
         assert np.all(err <= 5e-2 * ref + 1e-6)
     print(f"{n_diff} of {len(sess) * L * 2 * H * D} appended codes differ from the oracle's own "
           "(each within the two paths' measured difference of the oracle's value)")
+
+
+def test_full_size_every_phase_of_every_layer_matches_oracle(big, W7):
+    case, wave = big
+    w = case.w
+    n = 4
+    case.step(wave)
+    assert wave.status() == fsd.WAVE_OK
+    y_plain = case.y_bits()
+    recs = dump_acts(wave, n, 1, lambda: case.step(wave))
+    y = case.y_bits()
+    assert np.array_equal(y, y_plain), "the dump's kernel must give the usual kernel's bits"
+    worst = {}
+    for s in range(n):
+        P = int(case.pos_h[s])
+        kv = case.kv[:, :, s, :, :P + 1].cpu().numpy()
+        sc = case.sc[:, :, s, :, :P + 1].cpu().numpy()
+        phase_check.check_decoder_frame(w, W7, recs[0, :, s], P, kv, sc, case.x_h[s], y[s], worst)
+    print("positions", case.pos_h[:n], {k: round(v, 3) for k, v in worst.items()})
+    assert all(v <= 1.0 for v in worst.values()), worst

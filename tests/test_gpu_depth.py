@@ -9,7 +9,10 @@ x0 is nudged by one bf16 ulp, so the element-wise 1e-3 + 2e-2|y| bound is
 replaced, for every step, by: y within three times the oracle's own
 one-ulp response, normwise, and never above 5e-2.  Later steps also feed
 one step's bf16 output into the next through W_p.  Every depth-cache slot
-the loop writes is checked to be written, and a rerun to give the same bits."""
+the loop writes is checked to be written, and a rerun to give the same bits.
+And every phase of every layer of all 8 steps (with the projection between
+steps) is held to the stated element-wise bound and a tight one against the
+oracle's functions applied to the GPU's own inputs to that phase."""
 import numpy as np
 import pytest
 import torch
@@ -17,13 +20,15 @@ import torch
 import frame_step_decode_gb300 as fsd
 import oracle
 import synth
-from gpu_case import bf16_to_f64
+import phase_check
+from gpu_case import bf16_to_f64, dump_acts
 
 pytestmark = pytest.mark.gpu
 
 W = synth.DEPTH
 STEPS = W.extra["depth_steps"]
 SAMPLE = [0, 17, 40, 79]
+PHASE_SESSIONS = range(6)   # the activation dump records sessions 0..5
 
 
 @pytest.fixture(scope="module")
@@ -51,9 +56,14 @@ def run():
         wave.depth(S, STEPS, weights, wp, kv, sc, x0, xs, y2)
         assert wave.status() == fsd.WAVE_OK
         same = torch.equal(y.view(torch.int16), y2.view(torch.int16))
+        # once more with the activation dump on (its kernel gives the same bits)
+        y3 = torch.zeros_like(y)
+        recs = dump_acts(wave, len(PHASE_SESSIONS), STEPS,
+                         lambda: wave.depth(S, STEPS, weights, wp, kv, sc, x0, xs, y3))
+        same = same and torch.equal(y.view(torch.int16), y3.view(torch.int16))
     finally:
         wave.close()
-    out = dict(Wh=Wh, wp=wp_h, x0=x0_h, same=same,
+    out = dict(Wh=Wh, wp=wp_h, x0=x0_h, same=same, recs=recs,
                y=y.view(torch.int16).cpu().numpy().view(np.uint16),
                xs=xs.view(torch.int16).cpu().numpy().view(np.uint16),
                kv=kv.cpu().numpy(), sc=sc.cpu().numpy())
@@ -107,3 +117,20 @@ def test_depth_loop_on_a_ragged_prefix_batch():
             wave.close()
         outs.append(y)
     assert torch.equal(outs[0].view(torch.int16), outs[1][:, :S].view(torch.int16))
+
+
+def test_every_phase_of_every_step_matches_oracle(run):
+    w = W
+    worst = {}
+    for s in PHASE_SESSIONS:
+        kv = np.ascontiguousarray(run["kv"][:, :, s])
+        sc = np.ascontiguousarray(run["sc"][:, :, s])
+        for k in range(STEPS):
+            if k > 0:   # x_k = bf16(W_p y_{k-1}) on the GPU's own y_{k-1}
+                yk = synth.bf16_bits_to_f32(run["y"][k - 1, s]).astype(np.float64)
+                phase_check.note(worst, "proj", synth.bf16_bits_to_f32(run["xs"][k, s]),
+                                 oracle.matvec(run["wp"], yk), True)
+            phase_check.check_decoder_frame(w, run["Wh"], run["recs"][k, :, s], k, kv, sc, run["xs"][k, s],
+                                            run["y"][k, s], worst)
+    print({k: round(v, 3) for k, v in worst.items()})
+    assert all(v <= 1.0 for v in worst.values()), worst

@@ -10,7 +10,8 @@ import torch
 
 import frame_step_decode_gb300 as fsd
 import synth
-from gpu_case import DeviceCase, codes_vs_oracle, oracle_reference, y_close
+import phase_check
+from gpu_case import DeviceCase, codes_vs_oracle, dump_acts, oracle_reference, y_close
 
 pytestmark = pytest.mark.gpu
 
@@ -144,8 +145,10 @@ def test_ragged_batch_sizes(S):
 
 def test_edge_positions():
     w = synth.MID
-    # chunk (48 tokens) and piece (240 tokens) boundaries, and the extremes
-    pos = np.array([0, 1, 47, 48, 49, 95, 96, 239, 240, 241, 255, 256, w.T_max - 1, 63, 64, 287, 288],
+    # 32-token chunk boundaries and the extremes (T_max = 320 is below one
+    # 512-token piece, so every history here is a single piece; the split
+    # into pieces and their merge are tested on the long shapes below)
+    pos = np.array([0, 1, 31, 32, 33, 63, 64, 95, 96, 127, 128, 255, 256, w.T_max - 1, 287, 288, 160],
                    dtype=np.int32)
     case = DeviceCase(w, S=pos.size, pos=pos)
     wave = fsd.Wave(case.cfg, case.S_max, w.T_max)
@@ -396,5 +399,110 @@ def test_timeout_at_each_barrier_of_a_wide_layer(barrier, wide_weights):
         kv_o, sc_o = oracle.prefill_history(WIDE1, sess, fresh.pos_h, poison=True)
         _y_within_sensitivity(WIDE1, wide_weights, fresh.pos_h, np.ascontiguousarray(fresh.x_h), fresh.y_bits(),
                               kv_o, sc_o)
+    finally:
+        wave.close()
+
+
+# ----------------------------------------------------------------- phases
+def _check_phases(case, wave, n=None):
+    """Every phase of every layer of sessions 0..n-1 against the oracle's
+    functions on the GPU's own inputs to that phase (tests/phase_check.py),
+    under the stated bound and the tight one; and the dump's kernel gives
+    the same y bits as the usual kernel."""
+    w = case.w
+    n = case.S if n is None else n
+    kv0, sc0 = case.kv.clone(), case.sc.clone()
+    case.step(wave)
+    assert wave.status() == fsd.WAVE_OK
+    y_plain = case.y_bits()
+    case.kv.copy_(kv0)
+    case.sc.copy_(sc0)
+    recs = dump_acts(wave, n, 1, lambda: case.step(wave))
+    y = case.y_bits()
+    assert np.array_equal(y, y_plain), "the dump's kernel must give the usual kernel's bits"
+    W = getattr(case, "W_h", None)
+    W = synth.weights_host(w) if W is None else W
+    worst = {}
+    for s in range(n):
+        P = int(case.pos_h[s])
+        kv = case.kv[:, :, s, :, :P + 1].cpu().numpy()
+        sc = case.sc[:, :, s, :, :P + 1].cpu().numpy()
+        phase_check.check_decoder_frame(w, W, recs[0, :, s], P, kv, sc, case.x_h[s], y[s], worst)
+    print(w.name, {k: round(v, 3) for k, v in worst.items()})
+    assert all(v <= 1.0 for v in worst.values()), worst
+
+
+def test_every_phase_matches_oracle_tiny(tiny):
+    case, wave = tiny
+    _check_phases(case, wave)
+
+
+def test_every_phase_matches_oracle_mid(mid):
+    case, wave = mid
+    _check_phases(case, wave)
+
+
+def test_every_phase_matches_oracle_wide_layer(wide_weights):
+    case = DeviceCase(WIDE1, device_gen=True)
+    case.W_h = wide_weights
+    wave = fsd.Wave(case.cfg, case.S_max, WIDE1.T_max)
+    try:
+        _check_phases(case, wave)
+    finally:
+        wave.close()
+
+
+# ------------------------------------------------ split histories and their merge
+# Histories longer than one 512-token piece are cut into several pieces
+# whose partial results the merge phase combines: positions at the chunk
+# (32) and piece (512) boundaries and both head dims.
+MERGE_POS = np.array([0, 31, 32, 511, 512, 513, 1023, 1024, 1535, 1536, 1663, 777], dtype=np.int32)
+MERGE128 = synth.Workload("merge-2L-d512-h4x128-f1376", 2, 512, 4, 128, 1376, S=12, T_max=1664, pos_lo=0,
+                          pos_hi=1664)
+MERGE64 = synth.Workload("merge-2L-d512-h8x64-f1376", 2, 512, 8, 64, 1376, S=12, T_max=1664, pos_lo=0,
+                         pos_hi=1664)
+
+
+@pytest.mark.parametrize("w", [MERGE128, MERGE64], ids=["D128", "D64"])
+def test_split_histories_merge_to_the_oracle(w):
+    case = DeviceCase(w, pos=MERGE_POS)
+    wave = fsd.Wave(case.cfg, case.S_max, w.T_max)
+    try:
+        _check_case(case, wave)
+        _check_phases(case, wave)
+    finally:
+        wave.close()
+
+
+# ----------------------------------------------------------------- status
+def test_status_reads_without_synchronising():
+    # wave_status synchronises nothing: called while the step still waits
+    # behind ~100 ms of other work on its stream it returns at once and
+    # reports no finished launch; after the caller synchronises it reports
+    # the step's error, then nothing (cleared, on the host and the device)
+    import time
+    w = synth.TINY
+    case = DeviceCase(w)
+    wave = fsd.Wave(case.cfg, case.S_max, w.T_max)
+    stream = torch.cuda.Stream()
+    try:
+        bad = case.pos.clone()
+        bad[1] = w.T_max
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(200_000_000)
+            wave.step(case.S, case.weights, case.kv, case.sc, bad, case.x, case.y, stream=stream)
+            t0 = time.perf_counter()
+            rc = fsd.lib().wave_status(wave.h)
+            dt = time.perf_counter() - t0
+            running = not stream.query()
+        assert running and dt < 0.05, (running, dt)
+        assert rc == fsd.WAVE_OK
+        stream.synchronize()
+        assert fsd.lib().wave_status(wave.h) == fsd.WAVE_EPOS
+        assert fsd.lib().wave_status(wave.h) == fsd.WAVE_OK
+        wave.step(case.S, case.weights, case.kv, case.sc, case.pos, case.x, case.y, stream=stream)
+        stream.synchronize()
+        assert fsd.lib().wave_status(wave.h) == fsd.WAVE_OK
     finally:
         wave.close()
