@@ -445,11 +445,78 @@ def run_phases(args, w):
     wave.close()
 
 
+# -------------------------------------------------- the other workloads
+def timed_runs(launch, steps, runs, stream, gpu_index):
+    """`runs` runs of `steps` launches each, every launch timed by its own
+    CUDA event pair on `stream`, with nvidia-smi clocks sampled across all
+    of them.  Returns ([per-launch ms of each run], clocks)."""
+    import torch
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    time.sleep(0.3)
+    per_run = []
+    for _ in range(runs):
+        ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for i in range(steps):
+            ev0[i].record(stream)
+            launch()
+            ev1[i].record(stream)
+        torch.cuda.synchronize()
+        per_run.append([a.elapsed_time(b) for a, b in zip(ev0, ev1)])
+    return per_run, clocks.stop()
+
+
+def run_stats(per_run, deadline_ms=None):
+    """Mean, p50 and p99 over every timed launch, the same per run, and the
+    launches over the deadline."""
+    allv = [t for r in per_run for t in r]
+    out = {"ms_mean": statistics.mean(allv), "p50_ms": statistics.median(allv),
+           "p99_ms": float(np.percentile(allv, 99)),
+           "runs": [{"ms_mean": statistics.mean(r), "p50_ms": statistics.median(r),
+                     "p99_ms": float(np.percentile(r, 99))} for r in per_run]}
+    if deadline_ms is not None:
+        out["over_deadline"] = int(sum(1 for t in allv if t > deadline_ms))
+        out["deadline_ms"] = deadline_ms
+    return out
+
+
+def roofline_of(bytes_per_launch, ms):
+    """The HBM roofline object of a launch moving bytes_per_launch in ms."""
+    peak, peak_kind = measured_peaks()
+    achieved = bytes_per_launch / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "peak_kind": peak_kind, "frac_of_8000": achieved / 8000.0,
+            "algorithmic_bytes_per_launch": bytes_per_launch, "traffic": None}
+
+
+def cpu_baseline_of(seconds, units, sample):
+    """The oracle's rate on one sampled unit of the same workload."""
+    return {"value": units / seconds, "unit": METRIC, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": sample}
+
+
+def _oracle_frames_seconds(w, s, pos, frames):
+    """Seconds of the oracle for `frames` successive frames of session s of
+    the decoder workload w (inputs prepared outside the timing)."""
+    import oracle
+    W = synth.weights_host(w)
+    x = synth.x_bf16(w)[[s]]
+    p = np.asarray([pos[s]], dtype=np.int32)
+    kv, sc = oracle.prefill_history(w, [s], p, poison=False)
+    t0 = time.perf_counter()
+    for f in range(frames):
+        oracle.step(w, W, kv, sc, p + f, x)
+    return time.perf_counter() - t0
+
+
 def run_sweep(args, w):
     """Session sweep on one GPU: one history of S_max = max(S) sessions, and
     for each S the first S of them (positions are the first S of one draw,
     so the sweeps nest).  One JSON line per S: session-frames/s, p50/p99
-    step ms, algorithmic GB/s and its fraction of the HBM peak."""
+    step ms over --runs runs of --steps steps, the HBM roofline fraction of
+    the step, clocks, and the oracle on one session as the CPU baseline."""
     import torch
     import frame_step_decode_gb300 as fsd
     device = torch.device("cuda", 0)
@@ -458,40 +525,40 @@ def run_sweep(args, w):
     weights, kv, sc, pos, pos_h, x, y = build_inputs(w, S_max, device)
     wave = fsd.Wave(fsd.WaveConfig.of(w), S_max, w.T_max)
     stream = torch.cuda.current_stream()
-    peak, peak_kind = measured_peaks()
+    cpu = None
+    if not args.no_cpu_baseline:
+        sec = _oracle_frames_seconds(w, 0, pos_h, 1)
+        cpu = cpu_baseline_of(sec, 1, f"session 0 (pos {int(pos_h[0])}) of {w.name}, one frame; "
+                                       "sessions are independent, so the rate holds at any S")
     for S in sizes:
+        launch = lambda: wave.step(S, weights, kv, sc, pos, x, y, stream=stream)
         for _ in range(max(3, args.warmup)):
-            wave.step(S, weights, kv, sc, pos, x, y, stream=stream)
+            launch()
         if wave.status() != fsd.WAVE_OK:
             raise RuntimeError(f"warm-up failed at S={S}")
-        ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        torch.cuda.synchronize()
-        for i in range(args.steps):
-            ev0[i].record(stream)
-            wave.step(S, weights, kv, sc, pos, x, y, stream=stream)
-            ev1[i].record(stream)
-        torch.cuda.synchronize()
+        per_run, clk = timed_runs(launch, args.steps, args.runs, stream, 0)
         if wave.status() != fsd.WAVE_OK:
             raise RuntimeError(f"timed step failed at S={S}")
-        per = [ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)]
-        ms = statistics.mean(per)
+        st = run_stats(per_run, 80.0)
         b = algorithmic_bytes(w, pos_h[:S])
-        gbs = b / (ms * 1e-3) / 1e9
-        print(json.dumps({"sweep": True, "workload": w.name, "S": S, "metric": METRIC,
-                          "value": S / (ms * 1e-3), "ms_per_step": ms,
-                          "p50_ms": statistics.median(per), "p99_ms": float(np.percentile(per, 99)),
-                          "algorithmic_bytes": b, "achieved_gbs": gbs, "peak_gbs": peak,
-                          "peak_kind": peak_kind, "frac": gbs / peak, "frac_of_8000": gbs / 8000.0,
-                          "steps": args.steps}), flush=True)
+        print(json.dumps({"mode": "sweep", "metric": METRIC, "value": S / (st["ms_mean"] * 1e-3), "unit": METRIC,
+                          "higher_is_better": True, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": st["ms_mean"], "stats": st, "dtype": "bf16",
+                          "data": "synthetic (seeded)",
+                          "config": {"workload": w.name, "S": S, "T_max": w.T_max,
+                                     "positions": f"first {S} of one uniform [{w.pos_lo}, {w.pos_hi}) draw",
+                                     "l2": "inputs larger than L2 (no flush needed)"},
+                          "roofline": roofline_of(b, st["ms_mean"]), "clocks": clk, "cpu_baseline": cpu}),
+              flush=True)
     wave.close()
 
 
 def run_beat(args, w):
     """Beats of `--beat` frames per launch (the pages' beat is two 80 ms
-    frames with a 160 ms deadline): per-beat CUDA-event times, p50/p99, and
-    late beats.  Positions are held fixed between beats (advance off) so that
-    every timed beat moves the same bytes."""
+    frames with a 160 ms deadline): per-beat CUDA-event times over --runs
+    runs, p50/p99, beats over the deadline, roofline, clocks and the oracle
+    on one session's beat.  Positions are held fixed between beats (advance
+    off) so that every timed beat moves the same bytes."""
     import torch
     import frame_step_decode_gb300 as fsd
     device = torch.device("cuda", 0)
@@ -503,40 +570,40 @@ def run_beat(args, w):
     ys = torch.empty_like(xs)
     wave = fsd.Wave(fsd.WaveConfig.of(w), S, w.T_max)
     stream = torch.cuda.current_stream()
+    launch = lambda: wave.beat(S, F, weights, kv, sc, pos, xs, ys, advance=False, stream=stream)
     for _ in range(max(3, args.warmup)):
-        wave.beat(S, F, weights, kv, sc, pos, xs, ys, advance=False, stream=stream)
+        launch()
     if wave.status() != fsd.WAVE_OK:
         raise RuntimeError("warm-up beat failed")
-    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        ev0[i].record(stream)
-        wave.beat(S, F, weights, kv, sc, pos, xs, ys, advance=False, stream=stream)
-        ev1[i].record(stream)
-    torch.cuda.synchronize()
+    per_run, clk = timed_runs(launch, args.steps, args.runs, stream, 0)
     if wave.status() != fsd.WAVE_OK:
         raise RuntimeError("timed beat failed")
-    per = [ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)]
-    ms = statistics.mean(per)
+    st = run_stats(per_run, 80.0 * F)
     b = sum(algorithmic_bytes(w, pos_h + f) for f in range(F))
-    gbs = b / (ms * 1e-3) / 1e9
-    peak, peak_kind = measured_peaks()
-    print(json.dumps({"beat": True, "frames_per_launch": F, "workload": w.name, "S": S, "metric": METRIC,
-                      "value": F * S / (ms * 1e-3), "ms_per_beat": ms, "p50_ms": statistics.median(per),
-                      "p99_ms": float(np.percentile(per, 99)),
-                      "late_beats_over_deadline": int(sum(1 for t in per if t > 80.0 * F)),
-                      "deadline_ms": 80.0 * F, "achieved_gbs": gbs, "peak_gbs": peak,
-                      "peak_kind": peak_kind, "frac": gbs / peak, "steps": args.steps}), flush=True)
+    line = {"mode": "beat", "metric": METRIC, "value": F * S / (st["ms_mean"] * 1e-3), "unit": METRIC,
+            "higher_is_better": True, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "frames_per_launch": F, "ms_per_beat": st["ms_mean"], "stats": st, "dtype": "bf16",
+            "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "S": S, "T_max": w.T_max, "frames": F,
+                       "positions": f"uniform [{w.pos_lo}, {w.pos_hi}), at most T_max - {F}",
+                       "l2": "inputs larger than L2 (no flush needed)"},
+            "roofline": roofline_of(b, st["ms_mean"]), "clocks": clk, "cpu_baseline": None}
+    if not args.no_cpu_baseline:
+        sec = _oracle_frames_seconds(w, 0, pos_h, F)
+        line["cpu_baseline"] = cpu_baseline_of(sec, F, f"session 0 (pos {int(pos_h[0])}) of {w.name}, "
+                                                       f"one beat of {F} frames")
+    print(json.dumps(line), flush=True)
     wave.close()
 
 
 def run_depth(args):
     """The inner depth loop: 8 dependent steps per frame of the 6-layer
     d=1024 model, S = 80, one launch per frame (wave_depth).  Per-frame CUDA
-    events; reports frames/s, session-steps/s, p50/p99 frame ms, and the
+    events over --runs runs; reports session-frames/s (a session's frame is
+    its 8 dependent steps), session-steps/s, p50/p99 frame ms, the
     algorithmic bytes per frame (weights once per step + W_p once per chained
-    step + the depth cache read and written) against the HBM peak."""
+    step + the depth cache read and written) against the HBM peak, clocks,
+    and the oracle's depth loop for one session."""
     import torch
     import frame_step_decode_gb300 as fsd
     w = synth.DEPTH
@@ -556,32 +623,33 @@ def run_depth(args):
     xs = torch.empty((steps, S, d), dtype=torch.bfloat16, device=device)
     y = torch.empty((steps, S, d), dtype=torch.bfloat16, device=device)
     wave = fsd.Wave(fsd.WaveConfig.of(w), S, T)
+    launch = lambda: wave.depth(S, steps, weights, wp, kv, sc, x0, xs, y, stream=stream)
     for _ in range(max(3, args.warmup)):
-        wave.depth(S, steps, weights, wp, kv, sc, x0, xs, y, stream=stream)
+        launch()
     if wave.status() != fsd.WAVE_OK:
         raise RuntimeError("warm-up depth loop failed")
-    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        ev0[i].record(stream)
-        wave.depth(S, steps, weights, wp, kv, sc, x0, xs, y, stream=stream)
-        ev1[i].record(stream)
-    torch.cuda.synchronize()
+    per_run, clk = timed_runs(launch, args.steps, args.runs, stream, 0)
     if wave.status() != fsd.WAVE_OK:
         raise RuntimeError("timed depth loop failed")
-    per = [ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)]
-    ms = statistics.mean(per)
+    st = run_stats(per_run, 80.0)
+    ms = st["ms_mean"]
     b = sum(algorithmic_bytes(w, np.full(S, k)) for k in range(steps)) + (steps - 1) * 2 * d * d
-    gbs = b / (ms * 1e-3) / 1e9
-    peak, peak_kind = measured_peaks()
-    print(json.dumps({"depth_loop": True, "workload": w.name, "S": S, "steps_per_frame": steps,
-                      "metric": "frames/s", "value": 1000.0 / ms, "session_steps_per_s": S * steps / (ms * 1e-3),
-                      "ms_per_frame": ms, "p50_ms": statistics.median(per), "p99_ms": float(np.percentile(per, 99)),
-                      "us_per_step": 1000.0 * ms / steps, "algorithmic_bytes": b, "achieved_gbs": gbs,
-                      "peak_gbs": peak, "peak_kind": peak_kind, "frac": gbs / peak,
-                      "barriers_per_frame": steps * (7 * L - 1) + 2 * (steps - 1), "steps": args.steps}),
-          flush=True)
+    line = {"mode": "depth", "metric": METRIC, "value": S / (ms * 1e-3), "unit": METRIC,
+            "higher_is_better": True, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "session_steps_per_s": S * steps / (ms * 1e-3), "ms_per_frame": ms, "us_per_step": 1000.0 * ms / steps,
+            "stats": st, "dtype": "bf16", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "S": S, "steps_per_frame": steps, "T_max": T,
+                       "l2": "weights re-read every dependent step (154 MB, larger than L2)"},
+            "roofline": roofline_of(b, ms), "clocks": clk, "cpu_baseline": None,
+            "barriers_per_frame": steps * (7 * L - 1) + 2 * (steps - 1)}
+    if not args.no_cpu_baseline:
+        import oracle
+        Wh, wp_h, x_h = synth.weights_host(w), synth.proj_host(w), synth.x_bf16(w, 1)
+        t0 = time.perf_counter()
+        oracle.depth_loop(w, Wh, wp_h, x_h, steps)
+        line["cpu_baseline"] = cpu_baseline_of(time.perf_counter() - t0, 1,
+                                               f"session 0 of {w.name}: one frame of {steps} dependent steps")
+    print(json.dumps(line), flush=True)
     wave.close()
 
 
@@ -599,8 +667,9 @@ def hybrid_bytes(w, pos) -> int:
 
 def run_hybrid(args):
     """The hybrid recurrent step (48 layers: selective-state blocks with an
-    attention block every sixth layer), S = 56: per-step CUDA events, p50/p99,
-    session-frames/s and the HBM fraction of its algorithmic bytes."""
+    attention block every sixth layer), S = 56: per-step CUDA events over
+    --runs runs, p50/p99, session-frames/s, the HBM fraction of its
+    algorithmic bytes, clocks, and the oracle on one session."""
     import torch
     import frame_step_decode_gb300 as fsd
     w = synth.HYBRID
@@ -662,26 +731,31 @@ def run_hybrid(args):
                   f"({100 * np.sum(v) / t.sum():5.1f}%){extra}")
         wave.close()
         return
-    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        ev0[i].record(stream)
-        wave.hybrid_step(S, weights, kv, sc, state, pos, x, y, stream=stream)
-        ev1[i].record(stream)
-    torch.cuda.synchronize()
+    launch = lambda: wave.hybrid_step(S, weights, kv, sc, state, pos, x, y, stream=stream)
+    per_run, clk = timed_runs(launch, args.steps, args.runs, stream, 0)
     if wave.status() != fsd.WAVE_OK:
         raise RuntimeError("timed hybrid step failed")
-    per = [ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)]
-    ms = statistics.mean(per)
+    st = run_stats(per_run, 80.0)
     b = hybrid_bytes(w, pos_h)
-    gbs = b / (ms * 1e-3) / 1e9
-    peak, peak_kind = measured_peaks()
-    print(json.dumps({"hybrid": True, "workload": w.name, "S": S, "metric": METRIC, "value": S / (ms * 1e-3),
-                      "ms_per_step": ms, "p50_ms": statistics.median(per), "p99_ms": float(np.percentile(per, 99)),
-                      "algorithmic_bytes": b, "achieved_gbs": gbs, "peak_gbs": peak, "peak_kind": peak_kind,
-                      "frac": gbs / peak, "frac_of_8000": gbs / 8000.0, "steps": args.steps}), flush=True)
+    line = {"mode": "hybrid", "metric": METRIC, "value": S / (st["ms_mean"] * 1e-3), "unit": METRIC,
+            "higher_is_better": True, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": st["ms_mean"], "stats": st, "dtype": "bf16 (fp32 state)", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "S": S, "T_max": T,
+                       "positions": f"uniform [{aw.pos_lo}, {aw.pos_hi})",
+                       "l2": "inputs larger than L2 (no flush needed)"},
+            "roofline": roofline_of(b, st["ms_mean"]), "clocks": clk, "cpu_baseline": None}
     wave.close()
+    if not args.no_cpu_baseline:
+        import oracle
+        W = synth.hybrid_weights_host(w)
+        p1 = pos_h[:1]
+        kv1, sc1, st1 = oracle.hybrid_prefill(w, [0], p1, poison=False)
+        x1 = synth.x_bf16(aw, 1)
+        t0 = time.perf_counter()
+        oracle.hybrid_step(w, W, kv1, sc1, st1, p1, x1)
+        line["cpu_baseline"] = cpu_baseline_of(time.perf_counter() - t0, 1,
+                                               f"session 0 (pos {int(p1[0])}) of {w.name}, one frame")
+    print(json.dumps(line), flush=True)
 
 
 def main():
@@ -704,7 +778,22 @@ def main():
                     help="comma-separated session counts: one JSON line per S (one GPU)")
     ap.add_argument("--phases", action="store_true",
                     help="print the per-phase time table of one step instead of the JSON line")
+    ap.add_argument("--runs", type=int, default=3,
+                    help="runs of --steps launches per point in the --sweep/--beat/--depth/--hybrid modes")
     args = ap.parse_args()
+    # --gpus N: one process per GPU.  Launched by torchrun, WORLD_SIZE must
+    # say the same; launched plainly with N > 1, start the N ranks here.
+    world = os.environ.get("WORLD_SIZE")
+    if world is None and args.gpus > 1:
+        import socket
+        with socket.socket() as so:
+            so.bind(("127.0.0.1", 0))
+            port = so.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__), *sys.argv[1:]]
+        sys.exit(subprocess.call(cmd))
+    if world is not None and int(world) != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch one rank per GPU")
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
     w = synth.SEVEN_B
