@@ -425,9 +425,9 @@ def run_phases(args, w):
     for l in range(w.n_layers):
         if l > 0:
             names.append("norm1")
-        names += ["qkv", "attn"] + (["merge"] if -(-w.T_max // 32) > 16 else []) + ["o", "norm2", "gu", "down"]
+        names += ["qkv", "attn"] + (["merge"] if -(-w.T_max // 32) > 16 else []) + ["o", "norm2", "gu+down"]
     d, HD, F = w.d_model, w.HD, w.ffn
-    wbytes = {"qkv": 3 * HD * d * 2, "o": d * HD * 2, "gu": 2 * F * d * 2, "down": d * F * 2}
+    wbytes = {"qkv": 3 * HD * d * 2, "o": d * HD * 2, "gu+down": 3 * F * d * 2}
     kvb = sum(2 * w.n_heads * (int(q) + 1) * (w.head_dim + 4) for q in pos_h)
     print(f"{w.name} S={S}: step {t.sum():.1f} us (phase = work + the grid barrier after it)")
     agg = {}
@@ -641,7 +641,7 @@ def run_depth(args):
             "config": {"workload": w.name, "S": S, "steps_per_frame": steps, "T_max": T,
                        "l2": "weights re-read every dependent step (154 MB, larger than L2)"},
             "roofline": roofline_of(b, ms), "clocks": clk, "cpu_baseline": None,
-            "barriers_per_frame": steps * (7 * L - 1) + 2 * (steps - 1)}
+            "barriers_per_frame": steps * (6 * L - 1) + 2 * (steps - 1)}
     if not args.no_cpu_baseline:
         import oracle
         Wh, wp_h, x_h = synth.weights_host(w), synth.proj_host(w), synth.x_bf16(w, 1)

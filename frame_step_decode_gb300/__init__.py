@@ -49,7 +49,7 @@ class WaveError(RuntimeError):
 _lib = None
 EXPORTS = ("wave_create", "wave_destroy", "wave_weights_bytes", "wave_weight_offset", "wave_step", "wave_beat", "wave_depth",
            "wave_status", "wave_strerror", "wave_kv_quantize", "wave_fp8_encode", "wave_step_static",
-           "wave_set_timeout_ns", "wave_debug_skip_barrier", "wave_debug_dump_kv", "wave_debug_dump_acts",
+           "wave_set_timeout_ns", "wave_debug_skip_barrier", "wave_debug_skip_signal", "wave_debug_dump_kv", "wave_debug_dump_acts",
            "wave_debug_act_record_floats", "wave_debug_phase_times", "wave_debug_arrival_times",
            "wave_grid_size", "wave_barriers_per_step", "wave_hybrid_create", "wave_hybrid_step",
            "wave_hybrid_weights_bytes", "wave_hybrid_layer_offset")
@@ -99,6 +99,8 @@ def lib() -> ctypes.CDLL:
         L.wave_set_timeout_ns.restype = i32
         L.wave_debug_skip_barrier.argtypes = [vp, i32, i32]
         L.wave_debug_skip_barrier.restype = i32
+        L.wave_debug_skip_signal.argtypes = [vp, i32, i32]
+        L.wave_debug_skip_signal.restype = i32
         L.wave_debug_dump_kv.argtypes = [vp, vp]
         L.wave_debug_dump_kv.restype = i32
         L.wave_debug_dump_acts.argtypes = [vp, vp, i32]
@@ -201,6 +203,11 @@ class Wave:
 
     def debug_skip_barrier(self, cta: int, barrier: int) -> None:
         lib().wave_debug_skip_barrier(self.h, cta, barrier)
+
+    def debug_skip_signal(self, cta: int, which: int = 0) -> None:
+        """Testing hook: CTA `cta` never publishes its finished QKV (which=0)
+        or gate/up (which=1) tiles in later steps; cta < 0 disables."""
+        lib().wave_debug_skip_signal(self.h, cta, which)
 
     def debug_dump_kv(self, dst) -> None:
         """Testing hook: later steps write their pre-quantisation K/V rows

@@ -31,7 +31,7 @@ struct wave_ctx {
   int maps_S = -1;
   cudaStream_t last_stream = nullptr;
   long long timeout_ns = 2000000000LL;
-  int skip_cta = -1, skip_bar = -1;
+  int skip_cta = -1, skip_bar = -1, skip_sig = -1, skip_sig_kind = -1;
   float* kv_dump = nullptr;
   float* act_dump = nullptr;
   int act_dump_n = 0;
@@ -190,6 +190,8 @@ static int launch_frames(wave_t* h, int S, int frames, const void* weights, uint
   p.timeout_ns = h->timeout_ns;
   p.skip_cta = h->skip_cta;
   p.skip_bar = h->skip_bar;
+  p.skip_sig = h->skip_sig;
+  p.skip_sig_kind = h->skip_sig_kind;
   p.act_dump = h->act_dump;
   p.act_dump_n = h->act_dump ? (S < h->act_dump_n ? S : h->act_dump_n) : 0;
   if (frames == 1) {  // the profiling and testing hooks below are sized for one frame
@@ -266,6 +268,13 @@ extern "C" int wave_debug_skip_barrier(wave_t* h, int cta, int barrier) {
   if (!h) return WAVE_EINVAL;
   h->skip_cta = cta;
   h->skip_bar = barrier;
+  return WAVE_OK;
+}
+
+extern "C" int wave_debug_skip_signal(wave_t* h, int cta, int which) {
+  if (!h || (cta >= 0 && which != 0 && which != 1)) return WAVE_EINVAL;
+  h->skip_sig = cta;
+  h->skip_sig_kind = which == 0 ? kQKV : kGU;
   return WAVE_OK;
 }
 

@@ -73,9 +73,12 @@ struct StepParams {
   float* qkv;            // [S_max][3*H*D] fp32
   uint16_t* attn;        // [S_pad_max][H*D] bf16 attention output
   uint16_t* u;           // [S_pad_max][F] bf16 SwiGLU output
-  float* gemm_part;      // [G][max_tiles_per_cta][S_pad][128] split-K partials
-  int* tile_cnt;         // [2][1024] per tile: segments arrived, final reducers done
-  int* att_ctr;          // [L] attention work counters (tile_cnt + 2048)
+  float* gemm_part;      // [2 banks][G][max_tiles_per_cta][S_pad][128] split-K partials
+  long long part_bank;   // floats per bank of gemm_part
+  int* tile_cnt;         // [2 banks][2][1024] per tile: segments arrived, final reducers done
+  int* done_cnt;         // [kind] tiles of that projection finished (and published) in this frame
+  int* qkv_done;         // [1024] per QKV tile: history layer + 1 once its q, k, v rows are written
+  int* att_ctr;          // [L] attention work counters
   float* att_part;       // [max pieces][D + 4] (acc, m, l) per attention piece
   int2* sh_info;         // [S_max*H] (first partial slot, pieces) per (session, head)
   int4* pieces;          // [2 * max pieces] (sh, c_lo | c_hi << 16, pieces of sh, first slot), (pos, 0, 0, 0)
@@ -85,6 +88,8 @@ struct StepParams {
   int* err;              // error bits (sticky until wave_status)
   long long timeout_ns;
   int skip_cta, skip_bar;
+  int skip_sig;          // testing hook: this CTA never publishes its finished tiles of ...
+  int skip_sig_kind;     // ... this projection (kQKV or kGU); skip_sig -1: off
   float* kv_dump;        // testing hook: [L][2][S_max][H][D] pre-quantisation K/V, or null
   float* act_dump;       // testing hook: [frames][L][act_dump_n][act_rec] phase inputs/outputs, or null
   int act_dump_n;        // sessions 0..act_dump_n-1 are recorded
@@ -97,9 +102,17 @@ struct StepParams {
 
 // CTAs taking part in a stream-K GEMM phase of `tiles` tiles and U units:
 // every participating span is non-empty and a tile has at most 64 segments.
-// Counter words of the workspace: two per GEMM tile (1024 tiles at most),
-// then one attention work counter per layer (1024 layers at most).
-constexpr int kCounterWords = 2048 + 1024;
+// Counter words of the workspace (zeroed at each frame's start): two banks of
+// two words per GEMM tile (1024 tiles at most; consecutive projections with
+// no grid barrier between them use different banks), the gate/up tiles'
+// done flags, then one attention work counter per layer (1024 layers at most).
+constexpr int kTileCntWords = 2048;
+constexpr int kDoneCntOff = 2 * kTileCntWords;   // per projection kind: tiles finished so far this frame
+constexpr int kQkvDoneOff = kDoneCntOff + 32;
+constexpr int kAttCtrOff = kQkvDoneOff + 1024;
+constexpr int kCounterWords = kAttCtrOff + 1024;
+// The bank of a projection's counters and partial slots.
+__host__ __device__ inline int gemm_bank(int kind) { return (kind == kO || kind == kDown || kind == kOut) ? 1 : 0; }
 // Frames one launch may run back to back (wave_beat).
 constexpr int kMaxFrames = 64;
 
@@ -126,7 +139,7 @@ cudaError_t occupancy_per_sm(int* blocks);
 // Whether a history of T_max slots can be cut into several attention pieces
 // (and so needs the merge phase).
 inline bool needs_merge(int T_max) { return (T_max + kChunk - 1) / kChunk > kPieceChunks; }
-int barriers_per_step(int L, int T_max);
+int barriers_per_step(int L, int T_max);  // of the decoder kernel without the dump hook
 int barriers_per_launch(int L, int T_max, int frames, bool advance, bool depth);
 int hybrid_barriers_per_step(int L, int attn_every, int T_max);
 // Dynamic shared memory layout shared by host checks and the kernel.

@@ -218,7 +218,7 @@ size_t carve_workspace(const Plan& pl, char* base, Workspace* ws) {
       {(void**)&w.qkv, (size_t)(SP * 3 * HD * 4)},
       {(void**)&w.attn, (size_t)(SP * HD * 2)},
       {(void**)&w.u, (size_t)(SP * F * 2)},
-      {(void**)&w.gemm_part, (size_t)pl.grid * pl.max_tiles_per_cta * SP * kTileM * 4},
+      {(void**)&w.gemm_part, 2 * (size_t)pl.grid * pl.max_tiles_per_cta * SP * kTileM * 4},
       {(void**)&w.tile_cnt, kCounterWords * 4},
       {(void**)&w.att_part, (size_t)(max_pieces * (D + 4) * 4)},
       {(void**)&w.sh_info, (size_t)(pl.S_max * H * 8)},
@@ -470,8 +470,11 @@ void fill_params(StepParams* p, const Plan& pl, const Workspace& ws, const Maps&
   p->attn = ws.attn;
   p->u = ws.u;
   p->gemm_part = ws.gemm_part;
+  p->part_bank = (long long)pl.grid * pl.max_tiles_per_cta * pl.S_pad_max * kTileM;
   p->tile_cnt = ws.tile_cnt;
-  p->att_ctr = ws.tile_cnt + 2048;
+  p->done_cnt = ws.tile_cnt + kDoneCntOff;
+  p->qkv_done = ws.tile_cnt + kQkvDoneOff;
+  p->att_ctr = ws.tile_cnt + kAttCtrOff;
   p->att_part = ws.att_part;
   p->sh_info = ws.sh_info;
   p->pieces = ws.pieces;
@@ -482,6 +485,8 @@ void fill_params(StepParams* p, const Plan& pl, const Workspace& ws, const Maps&
   p->timeout_ns = 2000000000LL;
   p->skip_cta = -1;
   p->skip_bar = -1;
+  p->skip_sig = -1;
+  p->skip_sig_kind = -1;
   act_sections(pl, &p->act_n1, &p->act_n2);
   p->act_rec = act_record_floats(pl);
 }

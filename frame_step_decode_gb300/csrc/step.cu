@@ -88,9 +88,51 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   return v;
 }
 __device__ __forceinline__ void set_err(const StepParams& p, int bits) { atomicOr(p.err, bits); }
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Wait (bounded) until *f >= v, the flag written with st_release by another
+// CTA; false if the wait gave up (timeout here or elsewhere).
+__device__ bool wait_flag_ge(const StepParams& p, const int* f, int v) {
+  if ((int)ld_acquire((const unsigned*)f) >= v) return true;
+  const long long t0 = globaltimer();
+  for (uint32_t it = 0;; ++it) {
+    if ((int)ld_acquire((const unsigned*)f) >= v) return true;
+    if ((it & 15) == 15) {
+      if (*(volatile int*)p.err & kErrTimeout) return false;
+      if (globaltimer() - t0 > p.timeout_ns) {
+        set_err(p, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// The same wait with a smaller footprint, for call sites under register
+// pressure: bounded by a spin count that approximates the timeout.
+__device__ __forceinline__ bool wait_flag_ge_light(const StepParams& p, const int* f, int v) {
+  const uint32_t max_it = (uint32_t)min(p.timeout_ns / 128, 0x7fffffffLL) + 1u;
+  for (uint32_t it = 0; it < max_it; ++it) {
+    if ((int)ld_acquire((const unsigned*)f) >= v) return true;
+    __nanosleep(128);
+    if ((it & 63) == 63 && (*(volatile int*)p.err & kErrTimeout)) return false;
+  }
+  set_err(p, kErrTimeout);
+  return false;
+}
+
+// Projections whose next phase starts without a grid barrier publish every
+// finished tile: the QKV tiles one flag each (attention waits for its
+// head's tiles), both a count of finished tiles (gate/up: the down
+// projection waits for the count to cover every tile).
+__device__ __forceinline__ bool publishes(int kind) { return kind == kQKV || kind == kGU; }
+__device__ __forceinline__ void publish_tile(const StepParams& p, int kind, int t, int layer) {
+  if (kind == kQKV) st_release(p.qkv_done + t, layer + 1);
+  atomicAdd(p.done_cnt + kind, 1);  // after the release (or the fence before it)
 }
 
 // ------------------------------------------------------------- grid barrier
@@ -335,7 +377,7 @@ __device__ __forceinline__ void resid_store(const StepParams& p, int s, int n, f
 // et + step, ...
 template <bool kOne>
 __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t, const float* first,
-                                         const long long* seg, int nseg, int et, int step,
+                                         const float* part, const long long* seg, int nseg, int et, int step,
                                          bool last_layer, int frame) {
   if (kind == kGU) {
     // item (s, r4): gate rows 4r4..4r4+3 and the up rows 64 below them
@@ -347,7 +389,7 @@ __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t
       const size_t o0 = (size_t)(i0 >> 4) * kTileM + 4 * (i0 & 15);
       const size_t o1 = two ? (size_t)(i1 >> 4) * kTileM + 4 * (i1 & 15) : o0;
       float4 g0, g1, u0, u1;
-      seg_sum4<kOne>(first, p.gemm_part, seg, nseg, o0, o1, o0 + 64, o1 + 64, g0, g1, u0, u1);
+      seg_sum4<kOne>(first, part, seg, nseg, o0, o1, o0 + 64, o1 + 64, g0, g1, u0, u1);
       swiglu_store(p.u + (size_t)(i0 >> 4) * F, t * 64 + 4 * (i0 & 15), F, g0, u0);
       if (two) swiglu_store(p.u + (size_t)(i1 >> 4) * F, t * 64 + 4 * (i1 & 15), F, g1, u1);
     }
@@ -364,7 +406,7 @@ __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t
         ov[k] = (size_t)(iv[k] >> 5) * kTileM + 4 * (iv[k] & 31);
       }
       float4 a[4];
-      seg_sum4<kOne>(first, p.gemm_part, seg, nseg, ov[0], ov[1], ov[2], ov[3], a[0], a[1], a[2], a[3]);
+      seg_sum4<kOne>(first, part, seg, nseg, ov[0], ov[1], ov[2], ov[3], a[0], a[1], a[2], a[3]);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int n = t * kTileM + 4 * (iv[k] & 31);
@@ -390,7 +432,7 @@ __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t
         ov[k] = (size_t)(iv[k] >> 5) * kTileM + 4 * (iv[k] & 31);
       }
       float4 a[4];
-      seg_sum4<kOne>(first, p.gemm_part, seg, nseg, ov[0], ov[1], ov[2], ov[3], a[0], a[1], a[2], a[3]);
+      seg_sum4<kOne>(first, part, seg, nseg, ov[0], ov[1], ov[2], ov[3], a[0], a[1], a[2], a[3]);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int n = t * kTileM + 4 * (iv[k] & 31);
@@ -410,7 +452,7 @@ __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t
       const float4 old0 = (n0 < d) ? __ldcg((const float4*)(p.resid + (size_t)s0 * d + n0)) : z;
       const float4 old1 = (n1 < d) ? __ldcg((const float4*)(p.resid + (size_t)s1 * d + n1)) : z;
       float4 a0, a1;
-      seg_sum2<kOne>(first, p.gemm_part, seg, nseg, (size_t)s0 * kTileM + (n0 - t * kTileM),
+      seg_sum2<kOne>(first, part, seg, nseg, (size_t)s0 * kTileM + (n0 - t * kTileM),
                (size_t)s1 * kTileM + (n1 - t * kTileM), a0, a1);
       if (n0 < d) resid_store(p, s0, n0, old0, a0, last_layer, frame);
       if (two && n1 < d) resid_store(p, s1, n1, old1, a1, last_layer, frame);
@@ -434,6 +476,14 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
   const uint32_t stride = (uint32_t)gemm_stage_bytes(S_pad);
   const uint32_t ring = c.sbase + c.lay.ring_off;
 
+  // The stream-K span as units (t, kb); weights have no input dependency,
+  // the activations of the down projection are the gate/up projection's
+  // SwiGLU output, which other CTAs may still be finishing (no grid barrier
+  // between the two projections).
+  const bool wait_inputs = (kind == kDown);
+  int* const cnt = p.tile_cnt + gemm_bank(kind) * kTileCntWords;
+  float* const part = p.gemm_part + (size_t)gemm_bank(kind) * (size_t)p.part_bank;
+
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
@@ -441,38 +491,71 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
       const CUtensorMap* xm = &p.tm_x[kind];
       // the projection between chained frames reads the previous frame's y rows
       const int xrow0 = (kind == kProj) ? (c.frame - 1) * p.S : 0;
-      bool fail = false;
-      for (long long u = sp.u0; !fail && u < sp.u1;) {
-        const int t = (int)(u / KB);
-        const long long e = min(sp.u1, (long long)(t + 1) * KB);
-        for (int kb = (int)(u - (long long)t * KB); kb < (int)(e - (long long)t * KB); ++kb) {
-          const uint32_t slot = c.ring_it % nst, ph = (c.ring_it / nst) & 1u;
-          if (!mbar_wait(bar_empty(c, slot), ph ^ 1u, p.timeout_ns, p.err)) {
-            set_err(p, kErrTimeout);
-            fail = true;
-            break;
-          }
-          const uint32_t fb = bar_full(c, slot);
-          mbar_arrive_expect_tx(fb, (uint32_t)kKStage * (16384u + b_bytes));
-          const uint32_t a = ring + slot * stride;
+      auto load_w = [&](uint32_t a, uint32_t fb, int t, int kb) {
 #pragma unroll
-          for (int bx = 0; bx < kKStage; ++bx) {
-            // K beyond the matrix (a ragged last unit) reads as zeros
-            const int k = (kb * kKStage + bx) * kKBlk;
-            const uint32_t wa = a + (uint32_t)bx * 16384u;
-            if (kind == kGU) {
-              tma_load_4d(wa, wm, k, t * 64, 0, layer, fb, pol);
-              tma_load_4d(wa + 8192, wm, k, t * 64, 1, layer, fb, pol);
-            } else if (kind == kIn || kind == kOut) {  // hybrid Mamba blocks: (place in group, group)
-              tma_load_4d(wa, wm, k, t * kTileM, layer % p.attn_every, layer / p.attn_every, fb, pol);
-            } else {
-              tma_load_3d(wa, wm, k, t * kTileM, layer, fb, pol);
-            }
-            tma_load_2d(a + (uint32_t)kKStage * 16384u + (uint32_t)bx * b_stride, xm, k, xrow0, fb);
+        for (int bx = 0; bx < kKStage; ++bx) {
+          // K beyond the matrix (a ragged last unit) reads as zeros
+          const int k = (kb * kKStage + bx) * kKBlk;
+          const uint32_t wa = a + (uint32_t)bx * 16384u;
+          if (kind == kGU) {
+            tma_load_4d(wa, wm, k, t * 64, 0, layer, fb, pol);
+            tma_load_4d(wa + 8192, wm, k, t * 64, 1, layer, fb, pol);
+          } else if (kind == kIn || kind == kOut) {  // hybrid Mamba blocks: (place in group, group)
+            tma_load_4d(wa, wm, k, t * kTileM, layer % p.attn_every, layer / p.attn_every, fb, pol);
+          } else {
+            tma_load_3d(wa, wm, k, t * kTileM, layer, fb, pol);
           }
-          c.ring_it++;
         }
-        u = e;
+      };
+      auto load_x = [&](uint32_t a, uint32_t fb, int kb) {
+#pragma unroll
+        for (int bx = 0; bx < kKStage; ++bx)
+          tma_load_2d(a + (uint32_t)kKStage * 16384u + (uint32_t)bx * b_stride, xm, (kb * kKStage + bx) * kKBlk,
+                      xrow0, fb);
+      };
+      bool fail = false;
+      // with inputs to wait for, the first ring's worth of weights is issued
+      // before the first wait, so that it streams while other CTAs finish
+      const long long n_pre = wait_inputs ? min((long long)nst, sp.u1 - sp.u0) : 0;
+      const uint32_t it0 = c.ring_it;
+      long long n_w = 0;  // units of the first ring whose weights are issued
+      for (; n_w < n_pre; ++n_w) {
+        const long long u = sp.u0 + n_w;
+        const uint32_t it = it0 + (uint32_t)n_w, slot = it % nst;
+        if (!mbar_wait(bar_empty(c, slot), ((it / nst) & 1u) ^ 1u, p.timeout_ns, p.err)) {
+          set_err(p, kErrTimeout);
+          fail = true;
+          break;
+        }
+        mbar_arrive_expect_tx(bar_full(c, slot), (uint32_t)kKStage * (16384u + b_bytes));
+        load_w(ring + slot * stride, bar_full(c, slot), (int)(u / KB), (int)(u % KB));
+      }
+      // every gate/up tile of this layer is done (one count; they finish
+      // together), then the activation boxes of the first ring
+      if (!fail && wait_inputs) {
+        fail = !wait_flag_ge(p, p.done_cnt + kGU, (layer + 1) * p.tiles[kGU]);
+        fence_proxy_async_global();  // the TMA reads below come after those tiles' writes
+      }
+      for (long long i = 0; !fail && i < n_pre; ++i) {
+        const long long u = sp.u0 + i;
+        const uint32_t slot = (it0 + (uint32_t)i) % nst;
+        load_x(ring + slot * stride, bar_full(c, slot), (int)(u % KB));
+      }
+      c.ring_it = it0 + (uint32_t)n_w;
+      for (long long u = sp.u0 + n_pre; !fail && u < sp.u1; ++u) {
+        const int t = (int)(u / KB), kb = (int)(u % KB);
+        const uint32_t slot = c.ring_it % nst, ph = (c.ring_it / nst) & 1u;
+        if (!mbar_wait(bar_empty(c, slot), ph ^ 1u, p.timeout_ns, p.err)) {
+          set_err(p, kErrTimeout);
+          fail = true;
+          break;
+        }
+        const uint32_t fb = bar_full(c, slot);
+        mbar_arrive_expect_tx(fb, (uint32_t)kKStage * (16384u + b_bytes));
+        const uint32_t a = ring + slot * stride;
+        load_w(a, fb, t, kb);
+        load_x(a, fb, kb);
+        c.ring_it++;
       }
     }
     __syncwarp();
@@ -540,7 +623,7 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
       tc_fence_after();
       const uint32_t tb_addr = c.tmem + ((uint32_t)(q * 32) << 16) + b * 128u;
       // Store this segment's sums as a partial slot ([column][128 rows] fp32).
-      float* slot = p.gemm_part + ((size_t)cta * MT + (t - first_tile)) * (size_t)S_pad * kTileM;
+      float* slot = part + ((size_t)cta * MT + (t - first_tile)) * (size_t)S_pad * kTileM;
       for (int col = 0; col < S_pad; col += 16) {
         float v[16];
         tmem_ld16(tb_addr + col, v);
@@ -553,14 +636,22 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
       if (nseg == 1) {
         // whole tile here: the four epilogue warps finish it from the slot
         named_bar(1, 128);
-        finish_tile<true>(p, kind, t, slot, nullptr, 1, threadIdx.x - 64, 128, last_layer, c.frame);
+        finish_tile<true>(p, kind, t, slot, part, nullptr, 1, threadIdx.x - 64, 128, last_layer, c.frame);
+        if (publishes(kind)) {  // publish the tile to the next phase
+          fence_proxy_async_global();
+          named_bar(1, 128);
+          if (threadIdx.x == 64 && !(p.skip_sig == cta && p.skip_sig_kind == kind)) {
+            __threadfence();
+            publish_tile(p, kind, t, layer);
+          }
+        }
       } else {
         // split tile: count this segment in (one thread releases the four
         // warps' stores, which the named barrier orders before it)
         named_bar(1, 128);
         if (threadIdx.x == 64) {
           __threadfence();
-          atomicAdd(p.tile_cnt + t, 1);
+          atomicAdd(cnt + t, 1);
         }
       }
       c.acc_it++;
@@ -582,7 +673,7 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
   const int m = (c_last - c_first) + (cta_span(U, G, c_last).u1 == te ? 1 : 0);
   const int idx = cta - c_first;
   const int MT = p.max_tiles_per_cta;
-  long long* seg = (long long*)(c.smem + c.lay.red_off);  // partial-slot offsets, segment order
+  long long* seg = (long long*)(c.smem + c.lay.red_off);  // partial-slot offsets (from part), segment order
   for (int j = threadIdx.x; j < nseg; j += kThreads) {
     const int cj = c_first + j;
     const int ftj = (int)(cta_span(U, G, cj).u0 / KB);
@@ -592,7 +683,7 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
     int ok = (*(volatile int*)p.err & kErrTimeout) ? 0 : 1;
     const long long t0 = globaltimer();
     for (uint32_t it = 0; ok; ++it) {
-      if ((int)ld_acquire((const unsigned*)(p.tile_cnt + t)) >= nseg) break;
+      if ((int)ld_acquire((const unsigned*)(cnt + t)) >= nseg) break;
       if ((it & 15) == 15) {
         if (*(volatile int*)p.err & kErrTimeout) { ok = 0; break; }
         if (globaltimer() - t0 > p.timeout_ns) {
@@ -606,13 +697,21 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
   }
   __syncthreads();
   if (!*misc_word(c, 3)) return;
-  finish_tile<false>(p, kind, t, p.gemm_part + seg[0], seg, nseg, idx * kThreads + threadIdx.x, m * kThreads,
+  finish_tile<false>(p, kind, t, part + seg[0], part, seg, nseg, idx * kThreads + threadIdx.x, m * kThreads,
               last_layer, c.frame);
+  const bool pub = publishes(kind);
+  if (pub) fence_proxy_async_global();  // the next phase may read these rows by TMA
   __syncthreads();
-  // the last final contributor to finish re-arms the tile's counters
-  if (threadIdx.x == 0 && atomicAdd(p.tile_cnt + 1024 + t, 1) == m - 1) {
-    p.tile_cnt[t] = 0;
-    p.tile_cnt[1024 + t] = 0;
+  // the last final contributor to finish re-arms the tile's counters (and
+  // publishes the tile where the next phase waits for it: every
+  // contributor's writes came before its count, so they come before that)
+  if (threadIdx.x == 0) {
+    if (pub) __threadfence();
+    if (atomicAdd(cnt + 1024 + t, 1) == m - 1) {
+      cnt[t] = 0;
+      cnt[1024 + t] = 0;
+      if (pub && !(p.skip_sig == cta && p.skip_sig_kind == kind)) publish_tile(p, kind, t, layer);
+    }
   }
 }
 
@@ -685,6 +784,17 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
       for (int k = 0; k < min(n, kAttStages); ++k) issue(c_lo + k, (c.att_it + k) % kAttStages);
     }
     __syncwarp();
+    // q (and for the tail piece k and v) come from QKV tiles that other CTAs
+    // may still be finishing (no grid barrier between the two phases): wait
+    // for their readiness flags, lanes 0..2 one tile each in parallel, while
+    // the chunk copies above are in flight
+    bool aborted;
+    {
+      bool ready = true;
+      if (lane < (tail ? 3 : 1)) ready = wait_flag_ge_light(p, p.qkv_done + (lane * HD + h * D) / kTileM, layer + 1);
+      // the flags' acquire orders the q, k, v reads below for the whole warp
+      aborted = __any_sync(0xffffffffu, !ready);
+    }
 
     // RoPE of q (and k) in fp32: lane i holds dims [i*DPL, (i+1)*DPL); its
     // rotate-half partner dims are in lane i^16.
@@ -703,7 +813,7 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
     }
     uint32_t kcodes = 0, vcodes = 0;
     float ks_new = 0.f, vs_new = 0.f;
-    if (tail) {
+    if (tail && !aborted) {
       float x[DPL], y[DPL];
 #pragma unroll
       for (int e = 0; e < DPL; ++e) x[e] = __ldcg(qrow + HD + lane * DPL + e);
@@ -770,9 +880,8 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
 #pragma unroll
     for (int j = 0; j < MTV; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
     float m_run = -INFINITY, l_run = 0.f, R = 0.f;
-    bool aborted = false;
 
-    for (int k = 0; k < n; ++k) {
+    for (int k = 0; !aborted && k < n; ++k) {
       const int ci = c_lo + k;
       const uint32_t it = c.att_it + k;
       const int st = it % kAttStages;
@@ -1419,7 +1528,14 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       }
       // the block's input projection: QKV, or the selective-state in-projection
       gemm_phase(p, c, attn_layer ? kQKV : kIn, li, false);
-      if (!(ok = grid_sync(p, c))) break;
+      // attention starts without a grid barrier: each piece waits for the QKV
+      // tiles it reads (the selective-state phase still takes one; the dump
+      // kernel takes one to read the projection's output whole)
+      if (kDump || !attn_layer) {
+        if (!(ok = grid_sync(p, c))) break;
+      } else {
+        __syncthreads();
+      }
       if (kDump) {
         if (attn_layer) act_dump_rows(p, c.frame, l, kActProj, p.qkv, 3 * p.HD, 3 * p.HD);
         else act_dump_rows(p, c.frame, l, kActProj, p.zx, p.in_rows, p.in_rows);
@@ -1448,8 +1564,12 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         if (!(ok = grid_sync(p, c) && nok2)) break;
         if (kDump) act_dump_rows(p, c.frame, l, kActXn2, p.xn, p.d, p.d);
         gemm_phase(p, c, kGU, l, false);
-        if (!(ok = grid_sync(p, c))) break;
-        if (kDump) act_dump_rows(p, c.frame, l, kActU, p.u, p.F, p.F);
+        if constexpr (kDump) {  // the dump reads u whole: a barrier here in this kernel only
+          if (!(ok = grid_sync(p, c))) break;
+          act_dump_rows(p, c.frame, l, kActU, p.u, p.F, p.F);
+        }
+        // no grid barrier: the down projection's producer waits, per unit,
+        // for the gate/up tiles that unit reads, its weights already streaming
         gemm_phase(p, c, kDown, l, last);
       }
       if (!last && !(ok = grid_sync(p, c))) break;
@@ -1518,12 +1638,12 @@ cudaError_t launch_step(const StepParams& p, int grid, cudaStream_t stream) {
                                      stream);
 }
 
-int barriers_per_step(int L, int T_max) { return (needs_merge(T_max) ? 8 : 7) * L - 1; }
+int barriers_per_step(int L, int T_max) { return (needs_merge(T_max) ? 6 : 5) * L - 1; }
 int hybrid_barriers_per_step(int L, int attn_every, int T_max) {
   int n = 1;  // prologue
   for (int l = 0; l < L; ++l) {
     n += (l > 0) ? 1 : 0;                                                       // norm
-    n += (l % attn_every == attn_every - 1) ? (needs_merge(T_max) ? 3 : 2) : 2;  // phases before the last
+    n += (l % attn_every == attn_every - 1) ? (needs_merge(T_max) ? 2 : 1) : 2;  // phases before the last
     n += (l < L - 1) ? 1 : 0;                                                   // after the last
   }
   return n;

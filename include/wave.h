@@ -281,6 +281,12 @@ int wave_set_timeout_ns(wave_t* h, long long ns);
 /* Make CTA `cta` skip its arrival at grid barrier number `barrier` (0-based)
  * in later steps, so that the others' waits run out; cta < 0 disables. */
 int wave_debug_skip_barrier(wave_t* h, int cta, int barrier);
+/* Make CTA `cta` never publish the readiness of the tiles it finishes in
+ * later steps, of the QKV projection (which = 0: attention's waits for q, k,
+ * v run out) or of the gate/up projection (which = 1: the down projection's
+ * waits run out) -- the two phase hand-overs without a grid barrier; cta < 0
+ * disables. */
+int wave_debug_skip_signal(wave_t* h, int cta, int which);
 /* Make later steps also write, for every session with a valid position, the
  * fp32 K (after RoPE) and V rows they quantise into dst, a device buffer of
  * [L][2][S_max][H][D] floats, so that tests can check the append bit for bit

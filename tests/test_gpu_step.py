@@ -376,20 +376,27 @@ def test_wide_layer_matches_oracle(wide_weights):
         wave.close()
 
 
-@pytest.mark.parametrize("barrier", [0, 1, 2, 3, 4, 5])
-def test_timeout_at_each_barrier_of_a_wide_layer(barrier, wide_weights):
-    # barriers of one layer with no merge phase: 0 before QKV, 1 before
-    # attention, 2 before O, 3 before the second norm, 4 before gate/up, 5
-    # before down; a CTA that never arrives makes every CTA give up there,
-    # drain its copies and return WAVE_ETIMEOUT, and the next step is exact
+@pytest.mark.parametrize("barrier", [0, 1, 2, 3, "qkv", "gate/up"])
+def test_timeout_at_each_wait_of_a_wide_layer(barrier, wide_weights):
+    # the grid barriers of one layer with no merge phase: 0 before QKV, 1
+    # before O, 2 before the second norm, 3 before gate/up; and the two
+    # hand-overs without a barrier, where a CTA never publishes its finished
+    # QKV tiles (attention waits) or gate/up tiles (the down projection
+    # waits).  Every CTA gives up there, drains its copies and returns
+    # WAVE_ETIMEOUT, and the next step is exact
     case = DeviceCase(WIDE1, device_gen=True)
     wave = fsd.Wave(case.cfg, case.S_max, WIDE1.T_max)
     try:
+        assert wave.barriers_per_step == 4
         wave.set_timeout_ns(20_000_000)  # 20 ms
-        wave.debug_skip_barrier(7, barrier)
+        if barrier in ("qkv", "gate/up"):
+            wave.debug_skip_signal(7, 0 if barrier == "qkv" else 1)
+        else:
+            wave.debug_skip_barrier(7, barrier)
         case.step(wave)
         assert wave.status() == fsd.WAVE_ETIMEOUT
         wave.debug_skip_barrier(-1, -1)
+        wave.debug_skip_signal(-1)
         wave.set_timeout_ns(2_000_000_000)
         fresh = DeviceCase(WIDE1, device_gen=True)
         fresh.step(wave)
