@@ -251,8 +251,10 @@ def build_inputs(w, S, device):
     import frame_step_decode_gb300 as fsd
     stream = torch.cuda.current_stream().cuda_stream
     L, H, T, D = w.n_layers, w.n_heads, w.T_max, w.head_dim
-    weights = torch.empty(synth.weight_elems(w), dtype=torch.bfloat16, device=device)
-    synth.weights_device(w, weights, stream)
+    rm = torch.empty(synth.weight_elems(w), dtype=torch.bfloat16, device=device)
+    synth.weights_device(w, rm, stream)
+    weights = fsd.pack_weights(fsd.WaveConfig.of(w), rm)   # the packed blob the step reads
+    del rm
     kv = torch.empty((L, 2, S, H, T, D), dtype=torch.uint8, device=device)
     sc = torch.empty((L, 2, S, H, T), dtype=torch.float32, device=device)
     raw = torch.empty((S, H, T, D), dtype=torch.float32, device=device)
@@ -401,8 +403,11 @@ def run_gpu(args, w):
 
 
 def run_phases(args, w):
-    """Per-phase time of one step from the kernel's phase timestamps
-    (profiling hook): mean per layer of each phase, barrier included."""
+    """Per-phase times of one step from the kernel's phase-end marks
+    (profiling hook): for every phase, when the last CTA finished it minus
+    when the last CTA finished the phase before (the critical path; no grid
+    barrier separates the phases), averaged over the layers, with the spread
+    of the CTAs' finishing times; three steps averaged."""
     import torch
     import frame_step_decode_gb300 as fsd
     device = torch.device("cuda", 0)
@@ -411,37 +416,40 @@ def run_phases(args, w):
     wave = fsd.Wave(fsd.WaveConfig.of(w), S, w.T_max)
     for _ in range(max(3, args.warmup)):
         wave.step(S, weights, kv, sc, pos, x, y)
-    ts = torch.zeros(wave.barriers_per_step + 2, dtype=torch.int64, device=device)
-    wave.debug_phase_times(ts)
-    runs = []
+    n, grid = wave.phases_per_step, wave.grid
+    ts = torch.zeros((n, grid), dtype=torch.int64, device=device)
+    wave.debug_arrival_times(ts)
+    ends, spreads = [], []
     for _ in range(3):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record()
         wave.step(S, weights, kv, sc, pos, x, y)
+        ev1.record()
         if wave.status() != fsd.WAVE_OK:
             raise RuntimeError("step failed")
-        runs.append(np.diff(ts.cpu().numpy().astype(np.float64)) / 1000.0)
-    wave.debug_phase_times(None)
-    t = np.mean(runs, axis=0)
+        t = ts.cpu().numpy().astype(np.float64) / 1000.0
+        last = t.max(axis=1)
+        ends.append(np.diff(np.concatenate([[t.min()], last])))
+        spreads.append(last - t.min(axis=1))
+    wave.debug_arrival_times(None)
+    dur, spr = np.mean(ends, axis=0), np.mean(spreads, axis=0)
     names = ["prologue"]
     for l in range(w.n_layers):
-        if l > 0:
-            names.append("norm1")
-        names += ["qkv", "attn"] + (["merge"] if -(-w.T_max // 32) > 16 else []) + ["o", "norm2", "gu+down"]
+        names += (["norm1"] if l > 0 else []) + ["qkv", "attn", "o", "norm2", "gu", "down"]
     d, HD, F = w.d_model, w.HD, w.ffn
-    wbytes = {"qkv": 3 * HD * d * 2, "o": d * HD * 2, "gu+down": 3 * F * d * 2}
     kvb = sum(2 * w.n_heads * (int(q) + 1) * (w.head_dim + 4) for q in pos_h)
-    print(f"{w.name} S={S}: step {t.sum():.1f} us (phase = work + the grid barrier after it)")
+    nbytes = {"qkv": 3 * HD * d * 2, "o": d * HD * 2, "gu": 2 * F * d * 2, "down": d * F * 2, "attn": kvb}
+    print(f"{w.name} S={S}: {dur.sum():.1f} us from the first mark (phase = the last CTA's finish minus "
+          "the last CTA's finish of the phase before; spread = last minus first CTA)")
     agg = {}
-    for n, v in zip(names, t):
-        agg.setdefault(n, []).append(v)
-    for n, v in agg.items():
-        m = float(np.mean(v))
-        extra = ""
-        if n in wbytes:
-            extra = f"  {wbytes[n] / m / 1e3:6.0f} GB/s of weights"
-        if n == "attn":
-            extra = f"  {kvb / m / 1e3:6.0f} GB/s of FP8 K/V"
-        print(f"  {n:8s} x{len(v):3d}  mean {m:8.1f} us  total {np.sum(v):9.1f} us "
-              f"({100 * np.sum(v) / t.sum():5.1f}%){extra}")
+    for nm, v, sp in zip(names, dur, spr):
+        agg.setdefault(nm, []).append((v, sp))
+    for nm, vs in agg.items():
+        m = float(np.mean([v for v, _ in vs]))
+        sp = float(np.mean([q for _, q in vs]))
+        extra = f"  {nbytes[nm] / m / 1e3:6.0f} GB/s" if nm in nbytes else ""
+        print(f"  {nm:8s} x{len(vs):3d}  mean {m:7.1f} us  spread {sp:6.1f} us  total {m * len(vs):9.1f} us "
+              f"({100 * m * len(vs) / dur.sum():5.1f}%){extra}")
     wave.close()
 
 
@@ -612,8 +620,10 @@ def run_depth(args):
     L, H, T, D = w.n_layers, w.n_heads, w.T_max, w.head_dim
     device = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
-    weights = torch.empty(synth.weight_elems(w), dtype=torch.bfloat16, device=device)
-    synth.weights_device(w, weights, stream.cuda_stream)
+    rm = torch.empty(synth.weight_elems(w), dtype=torch.bfloat16, device=device)
+    synth.weights_device(w, rm, stream.cuda_stream)
+    weights = fsd.pack_weights(fsd.WaveConfig.of(w), rm)
+    del rm
     wp = torch.empty((d, d), dtype=torch.bfloat16, device=device)
     synth.proj_device(w, wp.data_ptr(), stream.cuda_stream)
     x0 = torch.empty((S, d), dtype=torch.bfloat16, device=device)
@@ -678,8 +688,10 @@ def run_hybrid(args):
     device = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
     La, H, T, D = w.n_attn, w.n_heads, w.T_max, w.head_dim
-    weights = torch.empty(synth.hybrid_weight_elems(w), dtype=torch.bfloat16, device=device)
-    synth.hybrid_weights_device(w, weights, stream.cuda_stream)
+    rm = torch.empty(synth.hybrid_weight_elems(w), dtype=torch.bfloat16, device=device)
+    synth.hybrid_weights_device(w, rm, stream.cuda_stream)
+    weights = fsd.hybrid_pack_weights(fsd.WaveHybridConfig.of(w), rm)
+    del rm
     kv = torch.empty((La, 2, S, H, T, D), dtype=torch.uint8, device=device)
     sc = torch.empty((La, 2, S, H, T), dtype=torch.float32, device=device)
     raw = torch.empty((S, H, T, D), dtype=torch.float32, device=device)

@@ -47,11 +47,13 @@ class WaveError(RuntimeError):
 
 
 _lib = None
-EXPORTS = ("wave_create", "wave_destroy", "wave_weights_bytes", "wave_weight_offset", "wave_step", "wave_beat", "wave_depth",
+EXPORTS = ("wave_create", "wave_destroy", "wave_weights_bytes", "wave_weight_offset", "wave_packed_weights_bytes",
+           "wave_pack_weights", "wave_hybrid_packed_weights_bytes", "wave_hybrid_pack_weights",
+           "wave_step", "wave_beat", "wave_depth",
            "wave_status", "wave_strerror", "wave_kv_quantize", "wave_fp8_encode", "wave_step_static",
            "wave_set_timeout_ns", "wave_debug_skip_barrier", "wave_debug_skip_signal", "wave_debug_dump_kv", "wave_debug_dump_acts",
            "wave_debug_act_record_floats", "wave_debug_phase_times", "wave_debug_arrival_times",
-           "wave_grid_size", "wave_barriers_per_step", "wave_hybrid_create", "wave_hybrid_step",
+           "wave_grid_size", "wave_barriers_per_step", "wave_phases_per_step", "wave_hybrid_create", "wave_hybrid_step",
            "wave_hybrid_weights_bytes", "wave_hybrid_layer_offset")
 
 
@@ -71,6 +73,14 @@ def lib() -> ctypes.CDLL:
         L.wave_weights_bytes.restype = sz
         L.wave_weight_offset.argtypes = [cfgp, i32, i32]
         L.wave_weight_offset.restype = sz
+        L.wave_packed_weights_bytes.argtypes = [cfgp]
+        L.wave_packed_weights_bytes.restype = sz
+        L.wave_pack_weights.argtypes = [cfgp, vp, vp, vp]
+        L.wave_pack_weights.restype = i32
+        L.wave_hybrid_packed_weights_bytes.argtypes = [ctypes.POINTER(WaveHybridConfig)]
+        L.wave_hybrid_packed_weights_bytes.restype = sz
+        L.wave_hybrid_pack_weights.argtypes = [ctypes.POINTER(WaveHybridConfig), vp, vp, vp]
+        L.wave_hybrid_pack_weights.restype = i32
         L.wave_step.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
         L.wave_step.restype = i32
         L.wave_beat.argtypes = [vp, i32, i32, vp, vp, vp, vp, i32, vp, vp, vp]
@@ -115,6 +125,8 @@ def lib() -> ctypes.CDLL:
         L.wave_grid_size.restype = i32
         L.wave_barriers_per_step.argtypes = [vp]
         L.wave_barriers_per_step.restype = i32
+        L.wave_phases_per_step.argtypes = [vp]
+        L.wave_phases_per_step.restype = i32
         _lib = L
     return _lib
 
@@ -146,6 +158,38 @@ def weights_bytes(cfg: WaveConfig) -> int:
 
 def weight_offset(cfg: WaveConfig, layer: int, which: int) -> int:
     return lib().wave_weight_offset(ctypes.byref(cfg), layer, which)
+
+
+def packed_weights_bytes(cfg: WaveConfig) -> int:
+    return lib().wave_packed_weights_bytes(ctypes.byref(cfg))
+
+
+def pack_weights(cfg: WaveConfig, src, dst=None, stream=None):
+    """wave_pack_weights: the packed blob the step reads, from the row-major
+    blob src (a device tensor).  Returns dst (a new bf16 device tensor when
+    not given)."""
+    import torch
+    if dst is None:
+        dst = torch.empty(packed_weights_bytes(cfg) // 2, dtype=torch.bfloat16, device=src.device)
+    rc = lib().wave_pack_weights(ctypes.byref(cfg), _ptr(src), _ptr(dst), _stream(stream))
+    if rc != WAVE_OK:
+        raise WaveError(rc, "wave_pack_weights")
+    return dst
+
+
+def hybrid_packed_weights_bytes(cfg: "WaveHybridConfig") -> int:
+    return lib().wave_hybrid_packed_weights_bytes(ctypes.byref(cfg))
+
+
+def hybrid_pack_weights(cfg: "WaveHybridConfig", src, dst=None, stream=None):
+    """wave_hybrid_pack_weights (as pack_weights, for the hybrid blob)."""
+    import torch
+    if dst is None:
+        dst = torch.empty(hybrid_packed_weights_bytes(cfg) // 2, dtype=torch.bfloat16, device=src.device)
+    rc = lib().wave_hybrid_pack_weights(ctypes.byref(cfg), _ptr(src), _ptr(dst), _stream(stream))
+    if rc != WAVE_OK:
+        raise WaveError(rc, "wave_hybrid_pack_weights")
+    return dst
 
 
 class Wave:
@@ -204,10 +248,13 @@ class Wave:
     def debug_skip_barrier(self, cta: int, barrier: int) -> None:
         lib().wave_debug_skip_barrier(self.h, cta, barrier)
 
-    def debug_skip_signal(self, cta: int, which: int = 0) -> None:
-        """Testing hook: CTA `cta` never publishes its finished QKV (which=0)
-        or gate/up (which=1) tiles in later steps; cta < 0 disables."""
-        lib().wave_debug_skip_signal(self.h, cta, which)
+    def debug_skip_signal(self, which: int, index: int) -> None:
+        """Testing hook: later steps never publish item `index` of kind
+        `which` (0 QKV tile, 1 gate/up tile, 2 a head's attention rows, 3 O
+        tile, 4 down tile, 5 norm row); index < 0 disables."""
+        rc = lib().wave_debug_skip_signal(self.h, which, index)
+        if rc != WAVE_OK:
+            raise WaveError(rc, "wave_debug_skip_signal")
 
     def debug_dump_kv(self, dst) -> None:
         """Testing hook: later steps write their pre-quantisation K/V rows
@@ -232,8 +279,8 @@ class Wave:
         lib().wave_debug_phase_times(self.h, _ptr(dst))
 
     def debug_arrival_times(self, dst) -> None:
-        """Profiling hook: later steps write each CTA's globaltimer stamp at
-        each grid barrier arrival into dst ([barriers][grid] int64); None
+        """Profiling hook: later steps write the globaltimer stamp at which
+        each CTA finished each phase into dst ([phases][grid] int64); None
         disables."""
         lib().wave_debug_arrival_times(self.h, _ptr(dst))
 
@@ -244,6 +291,10 @@ class Wave:
     @property
     def barriers_per_step(self) -> int:
         return lib().wave_barriers_per_step(self.h)
+
+    @property
+    def phases_per_step(self) -> int:
+        return lib().wave_phases_per_step(self.h)
 
     def close(self) -> None:
         if getattr(self, "h", None):

@@ -54,6 +54,34 @@ extern "C" size_t wave_weight_offset(const wave_config* cfg, int layer, int whic
   return (size_t)((le * layer + off[which]) * 2);
 }
 
+extern "C" size_t wave_packed_weights_bytes(const wave_config* cfg) {
+  Plan pl;
+  if (plan_decoder(&pl, cfg, 1, 4, 1) != WAVE_OK) return 0;
+  return (size_t)pl.pk_total * 2;
+}
+
+extern "C" int wave_pack_weights(const wave_config* cfg, const void* src, void* dst, void* stream) {
+  Plan pl;
+  if (!src || !dst || src == dst || ((uintptr_t)src & 15) || ((uintptr_t)dst & 15) ||
+      plan_decoder(&pl, cfg, 1, 4, 1) != WAVE_OK)
+    return WAVE_EINVAL;
+  return pack_weights(pl, src, dst, (cudaStream_t)stream);
+}
+
+extern "C" size_t wave_hybrid_packed_weights_bytes(const wave_hybrid_config* cfg) {
+  Plan pl;
+  if (plan_hybrid(&pl, cfg, 1, 4, 1) != WAVE_OK) return 0;
+  return (size_t)pl.pk_total * 2;
+}
+
+extern "C" int wave_hybrid_pack_weights(const wave_hybrid_config* cfg, const void* src, void* dst, void* stream) {
+  Plan pl;
+  if (!src || !dst || src == dst || ((uintptr_t)src & 15) || ((uintptr_t)dst & 15) ||
+      plan_hybrid(&pl, cfg, 1, 4, 1) != WAVE_OK)
+    return WAVE_EINVAL;
+  return pack_weights(pl, src, dst, (cudaStream_t)stream);
+}
+
 extern "C" const char* wave_strerror(int code) {
   switch (code) {
     case WAVE_OK: return "ok";
@@ -271,10 +299,10 @@ extern "C" int wave_debug_skip_barrier(wave_t* h, int cta, int barrier) {
   return WAVE_OK;
 }
 
-extern "C" int wave_debug_skip_signal(wave_t* h, int cta, int which) {
-  if (!h || (cta >= 0 && which != 0 && which != 1)) return WAVE_EINVAL;
-  h->skip_sig = cta;
-  h->skip_sig_kind = which == 0 ? kQKV : kGU;
+extern "C" int wave_debug_skip_signal(wave_t* h, int which, int index) {
+  if (!h || (index >= 0 && (which < 0 || which > 5))) return WAVE_EINVAL;
+  h->skip_sig = index;
+  h->skip_sig_kind = which;
   return WAVE_OK;
 }
 
@@ -309,6 +337,12 @@ extern "C" int wave_debug_arrival_times(wave_t* h, long long* dst) {
 }
 
 extern "C" int wave_grid_size(wave_t* h) { return h ? h->pl.grid : WAVE_EINVAL; }
+
+extern "C" int wave_phases_per_step(wave_t* h) {
+  if (!h) return WAVE_EINVAL;
+  return h->pl.hybrid ? phases_per_step(h->pl.hcfg.n_layers, true, h->pl.hcfg.attn_every)
+                      : phases_per_step(h->pl.cfg.n_layers, false, 1);
+}
 
 extern "C" int wave_barriers_per_step(wave_t* h) {
   if (!h) return WAVE_EINVAL;

@@ -15,7 +15,10 @@ constexpr int kKStage = 2;        // boxes per ring stage: a stream-K unit is kK
 constexpr int kKUnit = kKBlk * kKStage;
 constexpr int kChunk = 32;        // attention tokens per async-copy chunk (2 x 16)
 constexpr int kAttStages = 3;     // stages per attention warp (two in flight while one is read)
-constexpr int kPieceChunks = 16;  // chunks per attention work piece (512 tokens)
+#ifndef WAVE_PIECE_CHUNKS
+#define WAVE_PIECE_CHUNKS 16
+#endif
+constexpr int kPieceChunks = WAVE_PIECE_CHUNKS;  // chunks per attention work piece
 constexpr int kMaxStages = 8;     // GEMM ring depth cap
 constexpr int kTmemCols = 256;    // two fp32 accumulators of up to 128 columns
 
@@ -47,7 +50,7 @@ struct StepParams {
   int nstage;            // GEMM ring depth for this S
   int tiles[kGemmKinds], kblocks[kGemmKinds];
   int max_tiles_per_cta; // partial-sum slots per CTA
-  long long layer_elems, off_g_attn, off_g_mlp, off_wo, off_wdown;
+  long long layer_elems, off_g_attn, off_g_mlp;  // the packed blob: layer stride, RMSNorm gains
   // caller buffers
   const uint16_t* weights;
   uint8_t* kv;
@@ -58,12 +61,11 @@ struct StepParams {
   int n_frames;          // frames run back to back in this launch (positions + f in frame f)
   int32_t* pos_advance;  // if set: positions += n_frames at the end (empty slots stay empty)
   int depth;             // frames chained: x[f] = bf16(W_p y[f-1]) (the kProj GEMM) before frame f
-  int merge;             // 0 when no (session, head) can need more than one piece (T_max small)
   uint16_t* x_chain;     // where those inputs go (the buffer x points at)
   // hybrid model (selective-state blocks with an attention block every attn_every layers)
   int hybrid, attn_every, ssm_heads, d_inner, in_rows;
-  long long hyb_M, hyb_G;      // elements of one Mamba block and of one group of attn_every layers
-  long long hyb_off_w_in, hyb_off_a_log;  // inside a Mamba block
+  long long hyb_M, hyb_G;      // packed elements of one Mamba block and of one group of attn_every layers
+  long long hyb_off_a_log;     // inside a packed Mamba block: A_log, dt_bias, D
   float* zx;             // [S_pad][in_rows] fp32 in-projection output (z | x | B | C | dt)
   uint16_t* ssm_out;     // [S_pad][d_inner] bf16 gated mixer output
   float* ssm_state;      // caller's [Lm][S_max][Hs][P][N] fp32 state
@@ -78,18 +80,20 @@ struct StepParams {
   int* tile_cnt;         // [2 banks][2][1024] per tile: segments arrived, final reducers done
   int* done_cnt;         // [kind] tiles of that projection finished (and published) in this frame
   int* qkv_done;         // [1024] per QKV tile: history layer + 1 once its q, k, v rows are written
+  int* head_cnt;         // [H] (session, head) attention rows written in this frame
+  int* sh_cnt;           // [S_max*H] pieces of a (session, head) finished in this frame
   int* att_ctr;          // [L] attention work counters
   float* att_part;       // [max pieces][D + 4] (acc, m, l) per attention piece
   int2* sh_info;         // [S_max*H] (first partial slot, pieces) per (session, head)
   int4* pieces;          // [2 * max pieces] (sh, c_lo | c_hi << 16, pieces of sh, first slot), (pos, 0, 0, 0)
-  int* n_pieces;         // [1]
+  int* n_pieces;         // [0] work-list entries, [1] sessions with a valid position
   const float2* rope;    // [T_max][D/2] (cos, sin)
   unsigned* bar;         // [0] grid barrier counter, [1] CTAs finished (both zeroed before each launch)
   int* err;              // error bits (sticky until wave_status)
   long long timeout_ns;
   int skip_cta, skip_bar;
-  int skip_sig;          // testing hook: this CTA never publishes its finished tiles of ...
-  int skip_sig_kind;     // ... this projection (kQKV or kGU); skip_sig -1: off
+  int skip_sig;          // testing hook: item (tile, head or norm row) never published, of ...
+  int skip_sig_kind;     // ... this kind (wave_debug_skip_signal's `which`); skip_sig -1: off
   float* kv_dump;        // testing hook: [L][2][S_max][H][D] pre-quantisation K/V, or null
   float* act_dump;       // testing hook: [frames][L][act_dump_n][act_rec] phase inputs/outputs, or null
   int act_dump_n;        // sessions 0..act_dump_n-1 are recorded
@@ -97,7 +101,7 @@ struct StepParams {
   long long act_rec;     // floats per record
   int* err_out;          // if set: the last CTA to finish copies *err here (a mapped host word)
   long long* phase_ts;   // profiling hook: globaltimer at start, after each barrier, at end
-  long long* arrive_ts;  // profiling hook: [barrier][cta] globaltimer at barrier arrival
+  long long* arrive_ts;  // profiling hook: [phase][cta] globaltimer when each CTA finished each phase
 };
 
 // CTAs taking part in a stream-K GEMM phase of `tiles` tiles and U units:
@@ -108,8 +112,11 @@ struct StepParams {
 // done flags, then one attention work counter per layer (1024 layers at most).
 constexpr int kTileCntWords = 2048;
 constexpr int kDoneCntOff = 2 * kTileCntWords;   // per projection kind: tiles finished so far this frame
+constexpr int kHeadsDone = 8;                    // done_cnt[8]: heads whose attention rows are all written
+constexpr int kNormRows = 9;                     // done_cnt[9]: RMSNorm rows written this frame
 constexpr int kQkvDoneOff = kDoneCntOff + 32;
-constexpr int kAttCtrOff = kQkvDoneOff + 1024;
+constexpr int kHeadCntOff = kQkvDoneOff + 1024;  // per head: (session, head) rows written this frame
+constexpr int kAttCtrOff = kHeadCntOff + 1024;
 constexpr int kCounterWords = kAttCtrOff + 1024;
 // The bank of a projection's counters and partial slots.
 __host__ __device__ inline int gemm_bank(int kind) { return (kind == kO || kind == kDown || kind == kOut) ? 1 : 0; }
@@ -136,10 +143,8 @@ __host__ __device__ inline long long hyb_layer_offset(long long M, long long G, 
 cudaError_t launch_step(const StepParams& p, int grid, cudaStream_t stream);
 cudaError_t configure_step_kernel();
 cudaError_t occupancy_per_sm(int* blocks);
-// Whether a history of T_max slots can be cut into several attention pieces
-// (and so needs the merge phase).
-inline bool needs_merge(int T_max) { return (T_max + kChunk - 1) / kChunk > kPieceChunks; }
 int barriers_per_step(int L, int T_max);  // of the decoder kernel without the dump hook
+int phases_per_step(int L, bool hybrid, int attn_every);
 int barriers_per_launch(int L, int T_max, int frames, bool advance, bool depth);
 int hybrid_barriers_per_step(int L, int attn_every, int T_max);
 // Dynamic shared memory layout shared by host checks and the kernel.

@@ -157,6 +157,36 @@ static int plan_gemms(Plan* pl) {
   return WAVE_OK;
 }
 
+// The packed layout: per decoder layer [g_attn][Wqkv][Wo][g_mlp][Wgu][Wdown],
+// per hybrid group (attn_every - 1) selective-state blocks [g][W_in][W_out]
+// [A_log, dt_bias, D padded to 8] then one attention block [g][Wqkv][Wo];
+// every matrix as packed_matrix_elems of its projection's tiles and units.
+static void plan_packed(Plan* pl) {
+  const long long d = pl->cfg.d_model;
+  auto mat = [&](int kind) { return packed_matrix_elems(pl->tiles[kind], pl->kblocks[kind]); };
+  if (!pl->hybrid) {
+    const long long n[6] = {d, mat(kQKV), mat(kO), d, mat(kGU), mat(kDown)};
+    long long o = 0;
+    for (int i = 0; i < 6; ++i) {
+      pl->pk_off[i] = o;
+      o += n[i];
+    }
+    pl->pk_layer = o;
+    pl->pk_total = o * pl->cfg.n_layers;
+  } else {
+    const wave_hybrid_config& hc = pl->hcfg;
+    pl->pk_w_in = d;
+    pl->pk_w_out = d + mat(kIn);
+    pl->pk_a_log = pl->pk_w_out + (pl->d_inner ? mat(kOut) : 0);
+    pl->pk_M = pl->pk_a_log + (3LL * hc.ssm_heads + 7) / 8 * 8;
+    pl->pk_wqkv = d;
+    pl->pk_wo = d + mat(kQKV);
+    pl->pk_A = pl->pk_wo + mat(kO);
+    pl->pk_layer = (hc.attn_every - 1) * pl->pk_M + pl->pk_A;
+    pl->pk_total = pl->pk_layer * (hc.n_layers / hc.attn_every);
+  }
+}
+
 int plan_decoder(Plan* pl, const wave_config* cfg, int S_max, int T_max, int grid) {
   if (!decoder_shape_ok(cfg)) return WAVE_EINVAL;
   const long long rows = (long long)cfg->n_layers * 2 * S_max * cfg->n_heads * T_max;
@@ -168,7 +198,9 @@ int plan_decoder(Plan* pl, const wave_config* cfg, int S_max, int T_max, int gri
   pl->T_max = T_max;
   pl->grid = grid;
   decoder_layout(cfg, pl->off, &pl->layer_elems);
-  return plan_gemms(pl);
+  const int rc = plan_gemms(pl);
+  plan_packed(pl);
+  return rc;
 }
 
 int plan_hybrid(Plan* pl, const wave_hybrid_config* hc, int S_max, int T_max, int grid) {
@@ -198,7 +230,9 @@ int plan_hybrid(Plan* pl, const wave_hybrid_config* hc, int S_max, int T_max, in
   pl->layer_elems = pl->hyb_G;
   pl->d_inner = hc->ssm_heads * hc->ssm_head_dim;
   pl->in_rows = 2 * pl->d_inner + 2 * hc->ssm_state + hc->ssm_heads;
-  return plan_gemms(pl);
+  const int rc = plan_gemms(pl);
+  plan_packed(pl);
+  return rc;
 }
 
 size_t carve_workspace(const Plan& pl, char* base, Workspace* ws) {
@@ -224,6 +258,7 @@ size_t carve_workspace(const Plan& pl, char* base, Workspace* ws) {
       {(void**)&w.sh_info, (size_t)(pl.S_max * H * 8)},
       {(void**)&w.pieces, (size_t)(max_pieces * 32)},
       {(void**)&w.n_pieces, 16},
+      {(void**)&w.sh_cnt, (size_t)pl.S_max * H * 4},
       {(void**)&w.rope, (size_t)pl.T_max * (D / 2) * 8},
       {(void**)&w.bar, 16},
       {(void**)&w.err, 16},
@@ -251,70 +286,53 @@ void rope_table(const Plan& pl, std::vector<float2>* tab) {
     }
 }
 
+// A packed projection matrix as a tensor of 128-byte rows (64 bf16): a
+// 128-row box is one contiguous 16 KB block, unit (t, kb) the two blocks at
+// rows ((t * kunits + kb) * 2 + bx) * 128.  Outer dims: layers (decoder) or
+// place-in-group and group (hybrid).
+static bool enc_packed(CUtensorMap* m, const char* base, int tiles, int kunits, int rank, const cuuint64_t* outer,
+                       const cuuint64_t* outer_stride_bytes) {
+  cuuint64_t dims[4] = {64, (cuuint64_t)tiles * kunits * 2 * 128, 1, 1}, str[3] = {128, 0, 0};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  for (int i = 0; i < rank - 2; ++i) {
+    dims[2 + i] = outer[i];
+    str[1 + i] = outer_stride_bytes[i];
+  }
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, (void*)base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 static int encode_hybrid_weight_maps(const Plan& pl, const void* weights, Maps* m) {
   const wave_hybrid_config& c = pl.hcfg;
-  const cuuint64_t d = c.d_model, HD = (cuuint64_t)c.n_heads * c.head_dim;
-  const cuuint64_t di = (cuuint64_t)c.ssm_heads * c.ssm_head_dim;
-  const cuuint64_t rows = 2 * di + 2 * c.ssm_state + c.ssm_heads;
   const cuuint64_t e = c.attn_every, groups = c.n_layers / c.attn_every;
-  const cuuint64_t M2 = (cuuint64_t)pl.hyb_M * 2, G2 = (cuuint64_t)pl.hyb_G * 2;
-  char* base = (char*)weights;
-  char* attn0 = base + (e - 1) * M2;  // the first attention block
-  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
-  {  // attention Wqkv [La][3HD][d], one attention block per group
-    cuuint64_t dims[3] = {d, 3 * HD, groups}, str[2] = {d * 2, G2};
-    cuuint32_t box[3] = {kKBlk, kTileM, 1};
-    if (!enc(&m->tm_w[kQKV], BF, 3, attn0 + pl.hyb_off_wqkv * 2, dims, str, box, SW)) return WAVE_ECUDA;
+  const cuuint64_t M2 = (cuuint64_t)pl.pk_M * 2, G2 = (cuuint64_t)pl.pk_layer * 2;
+  const char* base = (const char*)weights;
+  const char* attn0 = base + (e - 1) * M2;  // the first attention block
+  {  // attention Wqkv and Wo, one attention block per group
+    const cuuint64_t outer[1] = {groups}, ostr[1] = {G2};
+    if (!enc_packed(&m->tm_w[kQKV], attn0 + pl.pk_wqkv * 2, pl.tiles[kQKV], pl.kblocks[kQKV], 3, outer, ostr))
+      return WAVE_ECUDA;
+    if (!enc_packed(&m->tm_w[kO], attn0 + pl.pk_wo * 2, pl.tiles[kO], pl.kblocks[kO], 3, outer, ostr))
+      return WAVE_ECUDA;
   }
-  {  // attention Wo [La][d][HD]
-    cuuint64_t dims[3] = {HD, d, groups}, str[2] = {HD * 2, G2};
-    cuuint32_t box[3] = {kKBlk, kTileM, 1};
-    if (!enc(&m->tm_w[kO], BF, 3, attn0 + pl.hyb_off_wo * 2, dims, str, box, SW)) return WAVE_ECUDA;
-  }
-  if (e > 1) {
-    {  // W_in [group][place][rows][d]
-      cuuint64_t dims[4] = {d, rows, e - 1, groups}, str[3] = {d * 2, M2, G2};
-      cuuint32_t box[4] = {kKBlk, kTileM, 1, 1};
-      if (!enc(&m->tm_w[kIn], BF, 4, base + pl.hyb_off_w_in * 2, dims, str, box, SW)) return WAVE_ECUDA;
-    }
-    {  // W_out [group][place][d][d_inner]
-      cuuint64_t dims[4] = {di, d, e - 1, groups}, str[3] = {di * 2, M2, G2};
-      cuuint32_t box[4] = {kKBlk, kTileM, 1, 1};
-      if (!enc(&m->tm_w[kOut], BF, 4, base + pl.hyb_off_w_out * 2, dims, str, box, SW)) return WAVE_ECUDA;
-    }
+  if (e > 1) {  // W_in and W_out [group][place]
+    const cuuint64_t outer[2] = {e - 1, groups}, ostr[2] = {M2, G2};
+    if (!enc_packed(&m->tm_w[kIn], base + pl.pk_w_in * 2, pl.tiles[kIn], pl.kblocks[kIn], 4, outer, ostr))
+      return WAVE_ECUDA;
+    if (!enc_packed(&m->tm_w[kOut], base + pl.pk_w_out * 2, pl.tiles[kOut], pl.kblocks[kOut], 4, outer, ostr))
+      return WAVE_ECUDA;
   }
   return WAVE_OK;
 }
 
 int encode_weight_maps(const Plan& pl, const void* weights, Maps* m) {
   if (pl.hybrid) return encode_hybrid_weight_maps(pl, weights, m);
-  const wave_config& c = pl.cfg;
-  const cuuint64_t d = c.d_model, HD = (cuuint64_t)c.n_heads * c.head_dim, F = c.ffn, L = c.n_layers;
-  const cuuint64_t ls = (cuuint64_t)pl.layer_elems * 2;  // layer stride in bytes
-  char* base = (char*)weights;
-  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
-  {  // Wqkv [L][3HD][d]
-    cuuint64_t dims[3] = {d, 3 * HD, L}, str[2] = {d * 2, ls};
-    cuuint32_t box[3] = {kKBlk, kTileM, 1};
-    if (!enc(&m->tm_w[kQKV], BF, 3, base + pl.off[1] * 2, dims, str, box, SW)) return WAVE_ECUDA;
-  }
-  {  // Wo [L][d][HD]
-    cuuint64_t dims[3] = {HD, d, L}, str[2] = {HD * 2, ls};
-    cuuint32_t box[3] = {kKBlk, kTileM, 1};
-    if (!enc(&m->tm_w[kO], BF, 3, base + pl.off[2] * 2, dims, str, box, SW)) return WAVE_ECUDA;
-  }
-  {  // Wgu [L][2][F][d]
-    cuuint64_t dims[4] = {d, F, 2, L}, str[3] = {d * 2, F * d * 2, ls};
-    cuuint32_t box[4] = {kKBlk, 64, 1, 1};
-    if (!enc(&m->tm_w[kGU], BF, 4, base + pl.off[4] * 2, dims, str, box, SW)) return WAVE_ECUDA;
-  }
-  {  // Wdown [L][d][F]
-    cuuint64_t dims[3] = {F, d, L}, str[2] = {F * 2, ls};
-    cuuint32_t box[3] = {kKBlk, kTileM, 1};
-    if (!enc(&m->tm_w[kDown], BF, 3, base + pl.off[5] * 2, dims, str, box, SW)) return WAVE_ECUDA;
-  }
+  const char* base = (const char*)weights;
+  const cuuint64_t outer[1] = {(cuuint64_t)pl.cfg.n_layers}, ostr[1] = {(cuuint64_t)pl.pk_layer * 2};
+  const int kinds[4] = {kQKV, kO, kGU, kDown}, which[4] = {1, 2, 4, 5};
+  for (int i = 0; i < 4; ++i)
+    if (!enc_packed(&m->tm_w[kinds[i]], base + pl.pk_off[which[i]] * 2, pl.tiles[kinds[i]], pl.kblocks[kinds[i]],
+                    3, outer, ostr))
+      return WAVE_ECUDA;
   return WAVE_OK;
 }
 
@@ -433,11 +451,9 @@ void fill_params(StepParams* p, const Plan& pl, const Workspace& ws, const Maps&
   const int nst = smem_layout().gemm_ring_bytes / gemm_stage_bytes(S_pad);
   p->nstage = nst > kMaxStages ? kMaxStages : nst;
   p->max_tiles_per_cta = pl.max_tiles_per_cta;
-  p->layer_elems = pl.layer_elems;
-  p->off_g_attn = pl.off[0];
-  p->off_g_mlp = pl.off[3];
-  p->off_wo = pl.off[2];
-  p->off_wdown = pl.off[5];
+  p->layer_elems = pl.pk_layer;
+  p->off_g_attn = pl.pk_off[0];
+  p->off_g_mlp = pl.pk_off[3];
   p->weights = (const uint16_t*)weights;
   p->kv = kv;
   p->kv_scales = kv_scales;
@@ -445,7 +461,6 @@ void fill_params(StepParams* p, const Plan& pl, const Workspace& ws, const Maps&
   p->x = (const uint16_t*)x;
   p->y = (uint16_t*)y;
   p->n_frames = frames;
-  p->merge = needs_merge(pl.T_max) ? 1 : 0;
   if (pl.hybrid) {
     const wave_hybrid_config& hc = pl.hcfg;
     p->hybrid = 1;
@@ -454,14 +469,12 @@ void fill_params(StepParams* p, const Plan& pl, const Workspace& ws, const Maps&
     p->ssm_heads = hc.ssm_heads;
     p->d_inner = pl.d_inner;
     p->in_rows = pl.in_rows;
-    p->hyb_M = pl.hyb_M;
-    p->hyb_G = pl.hyb_G;
-    p->hyb_off_w_in = pl.hyb_off_w_in;
-    p->hyb_off_a_log = pl.hyb_off_a_log;
+    p->hyb_M = pl.pk_M;
+    p->hyb_G = pl.pk_layer;
+    p->hyb_off_a_log = pl.pk_a_log;
     p->zx = ws.zx;
     p->ssm_out = ws.ssm_out;
-    p->layer_elems = pl.hyb_G;
-    p->off_wo = (hc.attn_every - 1) * pl.hyb_M + pl.hyb_off_wo;
+    p->layer_elems = pl.pk_layer;
     p->off_g_attn = 0;
   }
   p->resid = ws.resid;
@@ -474,6 +487,8 @@ void fill_params(StepParams* p, const Plan& pl, const Workspace& ws, const Maps&
   p->tile_cnt = ws.tile_cnt;
   p->done_cnt = ws.tile_cnt + kDoneCntOff;
   p->qkv_done = ws.tile_cnt + kQkvDoneOff;
+  p->head_cnt = ws.tile_cnt + kHeadCntOff;
+  p->sh_cnt = ws.sh_cnt;
   p->att_ctr = ws.tile_cnt + kAttCtrOff;
   p->att_part = ws.att_part;
   p->sh_info = ws.sh_info;

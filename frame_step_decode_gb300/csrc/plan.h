@@ -31,7 +31,18 @@ struct Plan {
   int in_rows = 0, d_inner = 0;
   int tiles[kGemmKinds] = {0}, kblocks[kGemmKinds] = {0};
   int max_tiles_per_cta = 1;
+  // The packed blob the step reads (see wave_pack_weights): the same tensors
+  // in the same order, every projection matrix as tile blocks.
+  long long pk_off[6] = {0, 0, 0, 0, 0, 0};  // decoder: offsets inside a packed layer
+  long long pk_layer = 0;                     // decoder: one packed layer; hybrid: one packed group
+  long long pk_M = 0, pk_A = 0;               // hybrid: packed selective-state / attention block
+  long long pk_w_in = 0, pk_w_out = 0, pk_a_log = 0, pk_wqkv = 0, pk_wo = 0;  // inside those blocks
+  long long pk_total = 0;                     // elements of the packed blob
 };
+
+// Elements of one packed projection matrix: `tiles` row tiles x `kunits`
+// 128-column units, each unit two 128-row x 64-column blocks of 8192 elements.
+inline long long packed_matrix_elems(int tiles, int kunits) { return (long long)tiles * kunits * 2 * 8192; }
 
 // The library-owned device buffers of a step, carved out of one block.
 struct Workspace {
@@ -46,6 +57,7 @@ struct Workspace {
   int2* sh_info = nullptr;
   int4* pieces = nullptr;
   int* n_pieces = nullptr;
+  int* sh_cnt = nullptr;
   float2* rope = nullptr;
   unsigned* bar = nullptr;   // [0] grid barrier counter, [1] exit counter (zeroed before each launch)
   int* err = nullptr;
@@ -97,6 +109,9 @@ int encode_proj_maps(const Plan& pl, const void* w_proj, void* y, int S, int ste
 // Floats per record of the activation dump (the testing hook of wave.h):
 // 5 d + max(3 H D, in_rows) + max(H D, d_inner) + F.
 long long act_record_floats(const Plan& pl);
+// Reorder the blob laid out as wave_weight_offset / wave_hybrid_layer_offset
+// describe into the packed blob of the plan (device to device, on stream).
+int pack_weights(const Plan& pl, const void* src, void* dst, cudaStream_t stream);
 // Argument checks of a launch on the host (null pointers, S, frames, alignment).
 bool launch_args_ok(const Plan& pl, int S, int frames, const void* weights, const void* kv,
                     const void* kv_scales, const void* positions, const void* x, const void* y);

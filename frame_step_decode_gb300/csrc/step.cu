@@ -79,6 +79,15 @@ __device__ __forceinline__ volatile int* misc_word(const Ctx& c, int i) {
   return (volatile int*)(c.smem + c.lay.misc_off + 4 * i);
 }
 
+// Profiling hook: this CTA has finished its next phase (call with the CTA's
+// threads past the phase); the mark count is a shared-memory word.
+__device__ __forceinline__ void mark_phase(const StepParams& p, const Ctx& c) {
+  if (p.arrive_ts && threadIdx.x == 0) {
+    const int m = (*misc_word(c, 8))++;
+    p.arrive_ts[(size_t)m * gridDim.x + blockIdx.x] = globaltimer();
+  }
+}
+
 __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -93,7 +102,7 @@ __device__ __forceinline__ void st_release(int* p, int v) {
 }
 // Wait (bounded) until *f >= v, the flag written with st_release by another
 // CTA; false if the wait gave up (timeout here or elsewhere).
-__device__ bool wait_flag_ge(const StepParams& p, const int* f, int v) {
+__device__ __noinline__ bool wait_flag_ge(const StepParams& p, const int* f, int v) {
   if ((int)ld_acquire((const unsigned*)f) >= v) return true;
   const long long t0 = globaltimer();
   for (uint32_t it = 0;; ++it) {
@@ -125,11 +134,17 @@ __device__ __forceinline__ bool wait_flag_ge_light(const StepParams& p, const in
   return false;
 }
 
+// What a testing hook may withhold (wave_debug_skip_signal's `which`).
+enum SigKind : int { kSigQkv = 0, kSigGu = 1, kSigAttn = 2, kSigO = 3, kSigDown = 4, kSigNorm = 5 };
+__device__ __forceinline__ int sig_of(int kind) {
+  return kind == kQKV ? kSigQkv : kind == kGU ? kSigGu : kind == kO ? kSigO : kind == kDown ? kSigDown : -1;
+}
+
 // Projections whose next phase starts without a grid barrier publish every
 // finished tile: the QKV tiles one flag each (attention waits for its
 // head's tiles), both a count of finished tiles (gate/up: the down
 // projection waits for the count to cover every tile).
-__device__ __forceinline__ bool publishes(int kind) { return kind == kQKV || kind == kGU; }
+__device__ __forceinline__ bool publishes(int kind) { return kind != kProj; }
 __device__ __forceinline__ void publish_tile(const StepParams& p, int kind, int t, int layer) {
   if (kind == kQKV) st_release(p.qkv_done + t, layer + 1);
   atomicAdd(p.done_cnt + kind, 1);  // after the release (or the fence before it)
@@ -150,7 +165,6 @@ __device__ bool grid_sync(const StepParams& p, Ctx& c) {
     c.bar_target += gridDim.x;
     __threadfence();
     bool skip = ((int)blockIdx.x == p.skip_cta && c.bar_index == p.skip_bar);
-    if (p.arrive_ts) p.arrive_ts[(size_t)c.bar_index * gridDim.x + blockIdx.x] = globaltimer();
     if (!skip) atomicAdd(p.bar, 1u);
     int ok = 1;
     long long t0 = globaltimer();
@@ -179,8 +193,23 @@ __device__ bool grid_sync(const StepParams& p, Ctx& c) {
 // whole row arrives in one round trip with no register staging, then the
 // block reduces the sum of squares and writes xn.  Returns false if the copy
 // wait gave up.
-__device__ bool norm_phase(const StepParams& p, Ctx& c, const uint16_t* g, bool from_x) {
+// wait_cnt / wait_target: the residual rows are final once *wait_cnt (the
+// producing projection's finished-tile count) reaches wait_target (null: a
+// grid barrier came before).  With publish, every row written adds one to
+// the norm-rows count the next projection waits for (the frame's first norm
+// runs before a grid barrier and before the counts are zeroed, and does not).
+__device__ bool norm_phase(const StepParams& p, Ctx& c, const uint16_t* g, bool from_x, bool publish,
+                           const int* wait_cnt = nullptr, int wait_target = 0) {
   float* red = (float*)(c.smem + c.lay.red_off);
+  if (wait_cnt && (int)blockIdx.x < p.S) {
+    if (threadIdx.x == 0) {
+      const bool ok0 = wait_flag_ge(p, wait_cnt, wait_target);
+      fence_proxy_async_global();  // the row copies below come after those tiles' writes
+      *misc_word(c, 6) = ok0 ? 1 : 0;
+    }
+    __syncthreads();
+    if (!*misc_word(c, 6)) return false;
+  }
   const int d = p.d, d4 = d / 4, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float* rrow = (float*)(c.smem + c.lay.ring_off);                       // d fp32
   const uint16_t* grow = (const uint16_t*)(c.smem + c.lay.ring_off + 4 * d);  // d bf16
@@ -242,7 +271,12 @@ __device__ bool norm_phase(const StepParams& p, Ctx& c, const uint16_t* g, bool 
       o.y = (uint32_t)f32_to_bf16((v.z * rstd) * g2) | ((uint32_t)f32_to_bf16((v.w * rstd) * g3) << 16);
       *(uint2*)(p.xn + (size_t)s * d + 4 * i4) = o;
     }
+    fence_proxy_async_global();  // the next projection reads xn by TMA
     __syncthreads();
+    if (publish && threadIdx.x == 0 && !(p.skip_sig == s && p.skip_sig_kind == kSigNorm)) {
+      __threadfence();
+      atomicAdd(p.done_cnt + kNormRows, 1);
+    }
   }
   fence_proxy_async_smem();  // the next phase's copies overwrite this area
   return true;
@@ -258,46 +292,6 @@ __device__ __forceinline__ int owner_of(long long U, int G, long long u) {
   return (int)(((u + 1) * G + U - 1) / U - 1);
 }
 
-
-// Issue L2 prefetches of the weight boxes this CTA streams in GEMM `kind` of
-// `layer` (its stream-K span), from the unit `skip` units into the span, at
-// most `units` units; one tensor-map box per instruction, the producer's
-// boxes and coordinates.
-__device__ __noinline__ void prefetch_gemm_span(const StepParams& p, int kind, int layer, int skip, int units) {
-  const int KB = p.kblocks[kind], T = p.tiles[kind];
-  const long long U = (long long)T * KB;
-  if (U == 0 || units <= 0) return;
-  const int G = stream_k_ctas(gridDim.x, U, T, gemm_seg_cap(kind)), cta = blockIdx.x;
-  if (cta >= G) return;
-  const Span sp = cta_span(U, G, cta);
-  const CUtensorMap* wm = &p.tm_w[kind];
-  const long long u_end = min(sp.u1, sp.u0 + skip + units);
-  for (long long u = sp.u0 + skip; u < u_end; ++u) {
-    const int t = (int)(u / KB), kb = (int)(u - (long long)t * KB);
-#pragma unroll
-    for (int bx = 0; bx < kKStage; ++bx) {
-      const int k = (kb * kKStage + bx) * kKBlk;
-      if (kind == kGU) {
-        tma_prefetch_4d(wm, k, t * 64, 0, layer);
-        tma_prefetch_4d(wm, k, t * 64, 1, layer);
-      } else if (kind == kIn || kind == kOut) {
-        tma_prefetch_4d(wm, k, t * kTileM, layer % p.attn_every, layer / p.attn_every);
-      } else {
-        tma_prefetch_3d(wm, k, t * kTileM, layer);
-      }
-    }
-  }
-}
-// Units of this CTA's span in GEMM `kind` (0 if it takes no part).
-__device__ __forceinline__ int span_units(const StepParams& p, int kind) {
-  const int KB = p.kblocks[kind], T = p.tiles[kind];
-  const long long U = (long long)T * KB;
-  if (U == 0) return 0;
-  const int G = stream_k_ctas(gridDim.x, U, T, gemm_seg_cap(kind));
-  if ((int)blockIdx.x >= G) return 0;
-  const Span sp = cta_span(U, G, blockIdx.x);
-  return (int)(sp.u1 - sp.u0);
-}
 
 __device__ __forceinline__ float4 ld4cg(const float* q) { return __ldcg((const float4*)q); }
 __device__ __forceinline__ void add4(float4& a, const float4& b) {
@@ -460,7 +454,12 @@ __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t
   }
 }
 
-__device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, bool last_layer) {
+// wait_cnt / wait_target: the activations this projection reads are final
+// once *wait_cnt reaches wait_target (the norm-rows count, the gate/up tile
+// count, the heads-done count; null: a grid barrier came before).  The
+// producer issues the first ring of weights before it waits.
+__device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, bool last_layer,
+                           const int* wait_cnt = nullptr, int wait_target = 0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KB = p.kblocks[kind];
   const long long U = (long long)p.tiles[kind] * KB;
@@ -477,10 +476,9 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
   const uint32_t ring = c.sbase + c.lay.ring_off;
 
   // The stream-K span as units (t, kb); weights have no input dependency,
-  // the activations of the down projection are the gate/up projection's
-  // SwiGLU output, which other CTAs may still be finishing (no grid barrier
-  // between the two projections).
-  const bool wait_inputs = (kind == kDown);
+  // the activations may still be being written by other CTAs (no grid
+  // barrier between the phases).
+  const bool wait_inputs = wait_cnt != nullptr;
   int* const cnt = p.tile_cnt + gemm_bank(kind) * kTileCntWords;
   float* const part = p.gemm_part + (size_t)gemm_bank(kind) * (size_t)p.part_bank;
 
@@ -491,19 +489,21 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
       const CUtensorMap* xm = &p.tm_x[kind];
       // the projection between chained frames reads the previous frame's y rows
       const int xrow0 = (kind == kProj) ? (c.frame - 1) * p.S : 0;
+      // weights: unit (t, kb) of a packed matrix is two contiguous 16 KB
+      // blocks (128 rows x 64 K each, the ragged edges zero-filled by the
+      // packing); the projection between chained frames reads W_p as a plain
+      // [d][d] matrix instead
       auto load_w = [&](uint32_t a, uint32_t fb, int t, int kb) {
 #pragma unroll
         for (int bx = 0; bx < kKStage; ++bx) {
-          // K beyond the matrix (a ragged last unit) reads as zeros
-          const int k = (kb * kKStage + bx) * kKBlk;
           const uint32_t wa = a + (uint32_t)bx * 16384u;
-          if (kind == kGU) {
-            tma_load_4d(wa, wm, k, t * 64, 0, layer, fb, pol);
-            tma_load_4d(wa + 8192, wm, k, t * 64, 1, layer, fb, pol);
+          const int row = ((t * KB + kb) * kKStage + bx) * kTileM;
+          if (kind == kProj) {
+            tma_load_3d(wa, wm, (kb * kKStage + bx) * kKBlk, t * kTileM, 0, fb, pol);
           } else if (kind == kIn || kind == kOut) {  // hybrid Mamba blocks: (place in group, group)
-            tma_load_4d(wa, wm, k, t * kTileM, layer % p.attn_every, layer / p.attn_every, fb, pol);
+            tma_load_4d(wa, wm, 0, row, layer % p.attn_every, layer / p.attn_every, fb, pol);
           } else {
-            tma_load_3d(wa, wm, k, t * kTileM, layer, fb, pol);
+            tma_load_3d(wa, wm, 0, row, layer, fb, pol);
           }
         }
       };
@@ -533,8 +533,8 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
       // every gate/up tile of this layer is done (one count; they finish
       // together), then the activation boxes of the first ring
       if (!fail && wait_inputs) {
-        fail = !wait_flag_ge(p, p.done_cnt + kGU, (layer + 1) * p.tiles[kGU]);
-        fence_proxy_async_global();  // the TMA reads below come after those tiles' writes
+        fail = !wait_flag_ge(p, wait_cnt, wait_target);
+        fence_proxy_async_global();  // the TMA reads below come after those rows' writes
       }
       for (long long i = 0; !fail && i < n_pre; ++i) {
         const long long u = sp.u0 + i;
@@ -640,7 +640,7 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
         if (publishes(kind)) {  // publish the tile to the next phase
           fence_proxy_async_global();
           named_bar(1, 128);
-          if (threadIdx.x == 64 && !(p.skip_sig == cta && p.skip_sig_kind == kind)) {
+          if (threadIdx.x == 64 && !(p.skip_sig == t && p.skip_sig_kind == sig_of(kind))) {
             __threadfence();
             publish_tile(p, kind, t, layer);
           }
@@ -710,7 +710,73 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
     if (atomicAdd(cnt + 1024 + t, 1) == m - 1) {
       cnt[t] = 0;
       cnt[1024 + t] = 0;
-      if (pub && !(p.skip_sig == cta && p.skip_sig_kind == kind)) publish_tile(p, kind, t, layer);
+      if (pub && !(p.skip_sig == t && p.skip_sig_kind == sig_of(kind))) publish_tile(p, kind, t, layer);
+    }
+  }
+}
+
+// --------------------------------------------------------------- merge
+// Combine the split-T partials of one (session, head) cut into np pieces,
+// in piece order: M = max m_i, L = sum l_i 2^(m_i - M), o = sum acc_i
+// 2^(m_i - M) / L, written as bf16.  One warp, lane i owning dims
+// [i*D/32, (i+1)*D/32); up to kMergeMax pieces' loads in flight at once.
+// Run by the warp that finishes the (session, head)'s last piece.
+constexpr int kMergeMax = 8;
+template <int D>
+__device__ __forceinline__ void merge_item(const StepParams& p, int first, int np, int s, int h, int lane) {
+  constexpr int DPL = D / 32;
+  float M = -INFINITY, Ls = 0.f, o[DPL];
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) o[e] = 0.f;
+  if (np > kMergeMax) {
+    for (int i = 0; i < np; ++i) M = fmaxf(M, __ldcg(p.att_part + (size_t)(first + i) * (D + 4) + D));
+  }
+  for (int i0 = 0; i0 < np; i0 += kMergeMax) {
+    float mv[kMergeMax], lv[kMergeMax], ov[kMergeMax][DPL];
+#pragma unroll
+    for (int i = 0; i < kMergeMax; ++i) {
+      if (i0 + i < np) {
+        const float* pp = p.att_part + (size_t)(first + i0 + i) * (D + 4);
+        const float2 ml = __ldcg((const float2*)(pp + D));
+        mv[i] = ml.x;
+        lv[i] = ml.y;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) ov[i][e] = __ldcg(pp + lane * DPL + e);
+      }
+    }
+    if (np <= kMergeMax) {
+#pragma unroll
+      for (int i = 0; i < kMergeMax; ++i)
+        if (i < np) M = fmaxf(M, mv[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < kMergeMax; ++i) {
+      if (i0 + i < np) {
+        const float wgt = ex2(mv[i] - M);
+        Ls += lv[i] * wgt;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[e] += ov[i][e] * wgt;
+      }
+    }
+  }
+  const float inv = 1.0f / Ls;
+  uint16_t* od = p.attn + (size_t)s * p.HD + h * D + lane * DPL;
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) od[e] = f32_to_bf16(o[e] * inv);
+}
+
+// A (session, head)'s bf16 attention output is written (by this warp): count
+// it for its head; the count that completes a head (every live session)
+// adds one to the heads-done word the output projection waits for.
+__device__ __forceinline__ void attn_row_done(const StepParams& p, int h, int la, int lane) {
+  fence_proxy_async_global();  // the output projection reads these rows by TMA
+  __syncwarp();
+  if (lane == 0 && !(p.skip_sig == h && p.skip_sig_kind == kSigAttn)) {
+    __threadfence();
+    const int n_valid = __ldcg(p.n_pieces + 1);
+    if (atomicAdd(p.head_cnt + h, 1) == (la + 1) * n_valid - 1) {
+      __threadfence();
+      atomicAdd(p.done_cnt + kHeadsDone, 1);
     }
   }
 }
@@ -747,9 +813,6 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
   __half* qs_lo = qs_hi + 128;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   const uint64_t kv_policy = policy_evict_first();
-  // the output projection's weights are read next: bring them into L2 now
-  if (warp == kWarps - 1 && lane == 0) prefetch_gemm_span(p, kO, layer, 0, span_units(p, kO));
-  __syncwarp();
 
   // Dynamic assignment over the longest-first list: warp gw starts with entry
   // gw, then takes the next unclaimed entry from the layer's counter, claimed
@@ -1082,9 +1145,10 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
           o[VB / 2 + j] = f32_to_bf16((acc[j][2] + acc[j][3]) * f);
         }
       }
+      attn_row_done(p, h, layer, lane);
     } else {
-      // split (session, head): store this piece's (acc, m, l); the merge phase
-      // combines them after the next grid barrier
+      // split (session, head): store this piece's (acc, m, l) and count it;
+      // the warp whose piece completes the count merges them
       float* part = p.att_part + (size_t)(first + c_lo / kPieceChunks) * (D + 4);
       if (t4 == 0) {
 #pragma unroll
@@ -1096,6 +1160,17 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
           part[D] = m_run;
           part[D + 1] = l_run;
         }
+      }
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        __threadfence();  // this piece's partial before its count
+        last = atomicAdd(p.sh_cnt + sh, 1) == (layer + 1) * np - 1;
+        if (last) __threadfence();  // every piece's partial before the reads below
+      }
+      if (__shfl_sync(0xffffffffu, last, 0)) {
+        merge_item<D>(p, first, np, s, h, lane);
+        attn_row_done(p, h, layer, lane);
       }
     }
     pi = __shfl_sync(0xffffffffu, nxt, 0);
@@ -1216,73 +1291,6 @@ __device__ __forceinline__ bool ssm_phase(const StepParams& p, Ctx& c, int lm, i
   return true;
 }
 
-// --------------------------------------------------------------- merge
-// Combine the split-T partials of every (session, head) cut into several
-// pieces, in piece order: M = max m_i, L = sum l_i 2^(m_i - M),
-// o = sum acc_i 2^(m_i - M) / L, written as bf16.  One warp per (session,
-// head), lane i owning dims [i*D/32, (i+1)*D/32); the warp's work-list
-// entries are read up front (lane k: its k-th entry) and up to kMergeMax
-// pieces' loads are in flight at once.
-constexpr int kMergeMax = 8;
-template <int D>
-__device__ void merge_phase(const StepParams& p, Ctx& c) {
-  constexpr int DPL = D / 32;
-  const int lane = threadIdx.x & 31;
-  const int NW = gridDim.x * kWarps;
-  const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  const int N = p.S * p.H;
-  for (int base = gw; base < N; base += 32 * NW) {
-    const int mine = base + lane * NW;
-    const int2 info_l = (mine < N) ? __ldcg(p.sh_info + mine) : make_int2(0, 0);
-    const int cnt = min(32, (N - base + NW - 1) / NW);
-    for (int k = 0; k < cnt; ++k) {
-      const int sh = base + k * NW;
-      const int first = __shfl_sync(0xffffffffu, info_l.x, k);
-      const int np = __shfl_sync(0xffffffffu, info_l.y, k);
-      if (np <= 1) continue;
-      float M = -INFINITY, Ls = 0.f, o[DPL];
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) o[e] = 0.f;
-      if (np > kMergeMax) {
-        for (int i = 0; i < np; ++i) M = fmaxf(M, __ldcg(p.att_part + (size_t)(first + i) * (D + 4) + D));
-      }
-      for (int i0 = 0; i0 < np; i0 += kMergeMax) {
-        float mv[kMergeMax], lv[kMergeMax], ov[kMergeMax][DPL];
-#pragma unroll
-        for (int i = 0; i < kMergeMax; ++i) {
-          if (i0 + i < np) {
-            const float* pp = p.att_part + (size_t)(first + i0 + i) * (D + 4);
-            const float2 ml = __ldcg((const float2*)(pp + D));
-            mv[i] = ml.x;
-            lv[i] = ml.y;
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) ov[i][e] = __ldcg(pp + lane * DPL + e);
-          }
-        }
-        if (np <= kMergeMax) {
-#pragma unroll
-          for (int i = 0; i < kMergeMax; ++i)
-            if (i < np) M = fmaxf(M, mv[i]);
-        }
-#pragma unroll
-        for (int i = 0; i < kMergeMax; ++i) {
-          if (i0 + i < np) {
-            const float wgt = ex2(mv[i] - M);
-            Ls += lv[i] * wgt;
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) o[e] += ov[i][e] * wgt;
-          }
-        }
-      }
-      const float inv = 1.0f / Ls;
-      const int s = sh / p.H, h = sh - s * p.H;
-      uint16_t* od = p.attn + (size_t)s * p.HD + h * D + lane * DPL;
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) od[e] = f32_to_bf16(o[e] * inv);
-    }
-  }
-}
-
 // ---------------------------------------------------------------- prologue
 // One CTA turns positions into the attention work list: each (session, head)
 // history of pos+1 slots is cut into pieces of up to kPieceChunks chunks.
@@ -1358,6 +1366,9 @@ __device__ void build_pieces(const StepParams& p, Ctx& c) {
       off += t;
     }
     *p.n_pieces = off;
+    int nv = 0;
+    for (int s = 0; s < p.S; ++s) nv += (spos[s] >= 0) ? 1 : 0;
+    p.n_pieces[1] = nv;  // sessions whose attention rows the output projection waits for
     int run = 0;
     for (int i = 0; i < kThreads; ++i) {
       const int v = red[i];
@@ -1467,6 +1478,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     }
     for (int w = 0; w < kWarps; ++w)
       for (int st = 0; st < kAttStages; ++st) mbar_init(bar_att(c, w, st), 1);
+    *misc_word(c, 8) = 0;  // phase marks of the profiling hook
     mbar_init(bar_drain(c), 1);
     mbar_init(bar_norm(c), 1);
     for (int i = 0; i < kSsmStages; ++i) mbar_init(bar_ssm(c, i), 1);
@@ -1504,10 +1516,20 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     // phase 0: work list, counter reset, residual and first norm
     for (int i = blockIdx.x * kThreads + threadIdx.x; i < kCounterWords; i += gridDim.x * kThreads)
       p.tile_cnt[i] = 0;
+    for (int i = blockIdx.x * kThreads + threadIdx.x; i < p.S * p.H; i += gridDim.x * kThreads) p.sh_cnt[i] = 0;
     if (blockIdx.x == gridDim.x - 1) build_pieces(p, c);
-    const bool n0 = norm_phase(p, c, p.weights + p.off_g_attn, true);
+    const bool n0 = norm_phase(p, c, p.weights + p.off_g_attn, true, false);
     if (!(ok = grid_sync(p, c) && n0)) break;
+    mark_phase(p, c);
 
+    // Within a frame no grid barrier separates the phases: each waits, by
+    // counts and flags in global memory, for exactly the data it reads, its
+    // weights or history already streaming.  Norm rows wait for the finished
+    // tiles of the projection that wrote the residual; a projection waits
+    // for the norm rows, the attention rows or the gate/up tiles it reads;
+    // attention waits per piece for its head's QKV tiles.  Counts grow over
+    // the frame, so a target is the phase's ordinal times its per-phase
+    // count.  (The dump kernel adds a barrier before each dump.)
     for (int l = 0; ok && l < p.L; ++l) {
       // decoder layer: attention half + MLP half; hybrid model: an attention
       // block every attn_every layers, selective-state blocks otherwise, no MLP
@@ -1519,15 +1541,40 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       const uint16_t* wl = hyb ? p.weights + hyb_layer_offset(p.hyb_M, p.hyb_G, e, l)
                                : p.weights + (size_t)l * p.layer_elems;
       if (l > 0) {
-        const bool nok = norm_phase(p, c, wl + p.off_g_attn, false);
-        if (!(ok = grid_sync(p, c) && nok)) break;
+        // the residual is final once the previous block's output projection
+        // has finished every tile
+        int wk, wt;
+        if constexpr (kHybrid) {
+          const int lp = l - 1;
+          const bool pa = (lp % e == e - 1);
+          wk = pa ? kO : kOut;
+          wt = (pa ? lp / e + 1 : lp - lp / e + 1) * p.tiles[wk];
+        } else {
+          wk = kDown;
+          wt = l * p.tiles[kDown];
+        }
+        if constexpr (kDump) {
+          if (!(ok = grid_sync(p, c))) break;
+        }
+        const bool nok = norm_phase(p, c, wl + p.off_g_attn, false, true, kDump ? nullptr : p.done_cnt + wk, wt);
+        if (!(ok = nok)) break;
+        if constexpr (kDump) {
+          if (!(ok = grid_sync(p, c))) break;
+        } else {
+          __syncthreads();
+        }
+        mark_phase(p, c);
       }
       if (kDump) {  // the layer's input residual and its normed input
         act_dump_rows(p, c.frame, l, kActIn, p.resid, p.d, p.d);
         act_dump_rows(p, c.frame, l, kActXn1, p.xn, p.d, p.d);
       }
-      // the block's input projection: QKV, or the selective-state in-projection
-      gemm_phase(p, c, attn_layer ? kQKV : kIn, li, false);
+      // the block's input projection: QKV, or the selective-state in-projection,
+      // once this layer's norm rows are written (counted from the frame's
+      // second norm: two per decoder layer, one per hybrid layer; layer 0's
+      // follows the prologue's grid barrier)
+      const int n_rows = (hyb ? l : 2 * l) * p.S;
+      gemm_phase(p, c, attn_layer ? kQKV : kIn, li, false, l > 0 ? p.done_cnt + kNormRows : nullptr, n_rows);
       // attention starts without a grid barrier: each piece waits for the QKV
       // tiles it reads (the selective-state phase still takes one; the dump
       // kernel takes one to read the projection's output whole)
@@ -1536,45 +1583,74 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       } else {
         __syncthreads();
       }
+      mark_phase(p, c);
       if (kDump) {
         if (attn_layer) act_dump_rows(p, c.frame, l, kActProj, p.qkv, 3 * p.HD, 3 * p.HD);
         else act_dump_rows(p, c.frame, l, kActProj, p.zx, p.in_rows, p.in_rows);
       }
       if (attn_layer) {
+        // split histories are merged by the warp that finishes their last
+        // piece; the output projection waits for every head's rows, its
+        // weights already streaming
         if (p.D == 128) attention_phase<128>(p, c, li); else attention_phase<64>(p, c, li);
-        if (!(ok = grid_sync(p, c))) break;
-        if (p.merge) {  // only when some (session, head) is cut into several pieces
-          if (p.D == 128) merge_phase<128>(p, c); else merge_phase<64>(p, c);
+        if constexpr (kDump) {
           if (!(ok = grid_sync(p, c))) break;
+          act_dump_rows(p, c.frame, l, kActMix, p.attn, p.HD, p.HD);
+        } else {
+          __syncthreads();  // the CTA's warps leave the shared ring before the projection refills it
+          if (*(volatile int*)p.err & kErrTimeout) { ok = false; break; }
         }
-        if (kDump) act_dump_rows(p, c.frame, l, kActMix, p.attn, p.HD, p.HD);
+        mark_phase(p, c);
       } else if constexpr (kHybrid) {
         const bool sok = ssm_phase(p, c, l - l / e, l);
         if (!(ok = grid_sync(p, c) && sok)) break;
+        mark_phase(p, c);
         if (kDump) act_dump_rows(p, c.frame, l, kActMix, p.ssm_out, p.d_inner, p.d_inner);
       }
-      // and its output projection + residual: O, or the selective-state out-projection
+      // and its output projection + residual: O (once every head's rows are
+      // written; with no live session there is none to wait for), or the
+      // selective-state out-projection
       if constexpr (kHybrid) {
-        gemm_phase(p, c, attn_layer ? kO : kOut, li, last);
+        gemm_phase(p, c, attn_layer ? kO : kOut, li, last,
+                   attn_layer && __ldcg(p.n_pieces + 1) > 0 ? p.done_cnt + kHeadsDone : nullptr, (li + 1) * p.H);
       } else {
-        gemm_phase(p, c, kO, li, false);
-        if (!(ok = grid_sync(p, c))) break;
-        if (kDump) act_dump_rows(p, c.frame, l, kActMid, p.resid, p.d, p.d);
-        const bool nok2 = norm_phase(p, c, wl + p.off_g_mlp, false);
-        if (!(ok = grid_sync(p, c) && nok2)) break;
-        if (kDump) act_dump_rows(p, c.frame, l, kActXn2, p.xn, p.d, p.d);
-        gemm_phase(p, c, kGU, l, false);
-        if constexpr (kDump) {  // the dump reads u whole: a barrier here in this kernel only
+        gemm_phase(p, c, kO, li, false, __ldcg(p.n_pieces + 1) > 0 ? p.done_cnt + kHeadsDone : nullptr,
+                   (li + 1) * p.H);
+        if constexpr (kDump) {
+          if (!(ok = grid_sync(p, c))) break;
+          act_dump_rows(p, c.frame, l, kActMid, p.resid, p.d, p.d);
+        } else {
+          __syncthreads();
+        }
+        mark_phase(p, c);
+        const bool nok2 = norm_phase(p, c, wl + p.off_g_mlp, false, true, kDump ? nullptr : p.done_cnt + kO,
+                                     (l + 1) * p.tiles[kO]);
+        if (!(ok = nok2)) break;
+        if constexpr (kDump) {
+          if (!(ok = grid_sync(p, c))) break;
+          act_dump_rows(p, c.frame, l, kActXn2, p.xn, p.d, p.d);
+        } else {
+          __syncthreads();
+        }
+        mark_phase(p, c);
+        gemm_phase(p, c, kGU, l, false, p.done_cnt + kNormRows, (2 * l + 1) * p.S);
+        if constexpr (kDump) {  // the dump reads u whole
           if (!(ok = grid_sync(p, c))) break;
           act_dump_rows(p, c.frame, l, kActU, p.u, p.F, p.F);
+        } else {
+          __syncthreads();
         }
-        // no grid barrier: the down projection's producer waits, per unit,
-        // for the gate/up tiles that unit reads, its weights already streaming
-        gemm_phase(p, c, kDown, l, last);
+        mark_phase(p, c);
+        gemm_phase(p, c, kDown, l, last, p.done_cnt + kGU, (l + 1) * p.tiles[kGU]);
       }
-      if (!last && !(ok = grid_sync(p, c))) break;
-      // the block's output residual (the last layer's is y, rounded)
-      if (kDump && !last) act_dump_rows(p, c.frame, l, kHybrid ? kActMid : kActOut, p.resid, p.d, p.d);
+      if (kDump && !last) {  // the block's output residual (the last layer's is y, rounded)
+        if (!(ok = grid_sync(p, c))) break;
+        act_dump_rows(p, c.frame, l, kHybrid ? kActMid : kActOut, p.resid, p.d, p.d);
+      }
+      // the next phase (a norm, or the next frame's prologue) reuses the ring
+      __syncthreads();
+      mark_phase(p, c);
+      if (*(volatile int*)p.err & kErrTimeout) { ok = false; break; }
     }
   }
   // rolling positions: every frame has read them; advance once all are done
@@ -1638,14 +1714,18 @@ cudaError_t launch_step(const StepParams& p, int grid, cudaStream_t stream) {
                                      stream);
 }
 
-int barriers_per_step(int L, int T_max) { return (needs_merge(T_max) ? 6 : 5) * L - 1; }
+int barriers_per_step(int L, int T_max) { return 1; }  // the prologue's
+// Phase marks of one frame (the profiling hook): the prologue, then per
+// layer its norms and phases, in the layer loop's order.
+int phases_per_step(int L, bool hybrid, int attn_every) {
+  if (!hybrid) return 1 + L * 6 + (L - 1);  // QKV, attention, O, norm2, gate/up, down; norm1 after layer 0
+  int n = 1;
+  for (int l = 0; l < L; ++l) n += (l > 0 ? 1 : 0) + 3;  // norm, in-projection, mixer or attention, out
+  return n;
+}
 int hybrid_barriers_per_step(int L, int attn_every, int T_max) {
   int n = 1;  // prologue
-  for (int l = 0; l < L; ++l) {
-    n += (l > 0) ? 1 : 0;                                                       // norm
-    n += (l % attn_every == attn_every - 1) ? (needs_merge(T_max) ? 2 : 1) : 2;  // phases before the last
-    n += (l < L - 1) ? 1 : 0;                                                   // after the last
-  }
+  for (int l = 0; l < L; ++l) n += (l % attn_every == attn_every - 1) ? 0 : 2;  // in-projection, state phase
   return n;
 }
 int barriers_per_launch(int L, int T_max, int frames, bool advance, bool depth) {

@@ -96,12 +96,35 @@ size_t wave_weights_bytes(const wave_config* cfg);
 size_t wave_weight_offset(const wave_config* cfg, int layer, int which);
 
 /*
+ * The packed weight blob the step reads.  The blob of wave_weight_offset
+ * (row-major [out][in] matrices) is the interchange layout; the step reads
+ * the same tensors in the same order with every projection matrix stored as
+ * blocks of 128 rows x 64 inputs (16 KB, row-major inside a block), ordered
+ * by 128-row tile, then by 64-input block, rows and inputs beyond the matrix
+ * zero (the gate/up matrix's tile t holds gate rows 64t..64t+63, then up rows
+ * 64t..64t+63).  Every 16 KB the projections stream is then one contiguous
+ * block, which HBM serves at its streaming rate; the row-major tiles' 128-byte
+ * rows, kilobytes apart, cost DRAM page switches.  The pages fix no layout
+ * (the weights are bf16: the narilabs blog, "Compressing the Temporal KV
+ * cache").  The RMSNorm gains are copied as they are.
+ *
+ * wave_packed_weights_bytes: bytes of the packed blob (0 for a bad shape);
+ * the same as wave_weights_bytes when d_model, n_heads * head_dim and ffn
+ * are multiples of 128.  wave_pack_weights: reorder src (the blob of
+ * wave_weight_offset) into dst (wave_packed_weights_bytes, distinct from
+ * src); both device pointers, 16-byte aligned; asynchronous on `stream`.
+ * WAVE_EINVAL for bad arguments.
+ */
+size_t wave_packed_weights_bytes(const wave_config* cfg);
+int wave_pack_weights(const wave_config* cfg, const void* src, void* dst, void* stream);
+
+/*
  * One frame for sessions 0..S-1 (1 <= S <= S_max).  Asynchronous: enqueues
  * two operations on `stream` (an 8-byte memset of the barrier and exit
  * counters and one cooperative kernel launch) and returns; nothing is
  * synchronised.
  *
- *   weights    bf16 blob, layout of wave_weight_offset, 16-byte aligned, read only.
+ *   weights    the packed bf16 blob (wave_pack_weights), 16-byte aligned, read only.
  *   kv_fp8     uint8 [L][2][S_max][H][T_max][D] E4M3 codes (index 0 = K, 1 = V),
  *              16-byte aligned.  Slots 0..pos[s]-1 are read; slot pos[s] of every
  *              (layer, K|V, s, head) is written; no other byte is touched.
@@ -201,12 +224,20 @@ typedef struct {
 size_t wave_hybrid_weights_bytes(const wave_hybrid_config* cfg);
 size_t wave_hybrid_layer_offset(const wave_hybrid_config* cfg, int layer);
 
+/* The hybrid step's packed blob: the blob of wave_hybrid_layer_offset with
+ * every projection matrix (W_in, W_out, Wqkv, Wo) packed as for
+ * wave_pack_weights; gains and the A_log / dt_bias / D block copied as they
+ * are.  Sizes and arguments as wave_packed_weights_bytes / wave_pack_weights. */
+size_t wave_hybrid_packed_weights_bytes(const wave_hybrid_config* cfg);
+int wave_hybrid_pack_weights(const wave_hybrid_config* cfg, const void* src, void* dst, void* stream);
+
 /* A handle for the hybrid step (the attention blocks' history as in
  * wave_create, with n_layers / attn_every layers).  Release with
  * wave_destroy.  wave_step / wave_beat / wave_depth refuse a hybrid handle. */
 int wave_hybrid_create(const wave_hybrid_config* cfg, int S_max, int T_max, wave_t** out);
 
-/* One frame of the hybrid model for sessions 0..S-1.  kv_fp8 / kv_scales:
+/* One frame of the hybrid model for sessions 0..S-1.  weights: the hybrid
+ * packed blob (wave_hybrid_pack_weights).  kv_fp8 / kv_scales:
  * the attention blocks' history ([La][2][S_max][H][T_max][D], La = n_layers /
  * attn_every; as wave_step).  ssm_state: fp32 [Lm][S_max][Hs][64][128]
  * (Lm = n_layers - La), 16-byte aligned, read and written in place; an empty
@@ -281,12 +312,15 @@ int wave_set_timeout_ns(wave_t* h, long long ns);
 /* Make CTA `cta` skip its arrival at grid barrier number `barrier` (0-based)
  * in later steps, so that the others' waits run out; cta < 0 disables. */
 int wave_debug_skip_barrier(wave_t* h, int cta, int barrier);
-/* Make CTA `cta` never publish the readiness of the tiles it finishes in
- * later steps, of the QKV projection (which = 0: attention's waits for q, k,
- * v run out) or of the gate/up projection (which = 1: the down projection's
- * waits run out) -- the two phase hand-overs without a grid barrier; cta < 0
- * disables. */
-int wave_debug_skip_signal(wave_t* h, int cta, int which);
+/* Make later steps never publish the readiness of one item, so that the
+ * wait for it runs out at a phase hand-over without a grid barrier: which =
+ * 0 the QKV tile `index` (attention waits), 1 the gate/up tile `index` (the
+ * down projection waits), 2 the attention rows of head `index` (the output
+ * projection waits), 3 the output-projection tile `index` (the second
+ * RMSNorm waits), 4 the down-projection tile `index` (the next layer's first
+ * RMSNorm waits), 5 the RMSNorm row `index` (the next projection waits).
+ * index < 0 disables. */
+int wave_debug_skip_signal(wave_t* h, int which, int index);
 /* Make later steps also write, for every session with a valid position, the
  * fp32 K (after RoPE) and V rows they quantise into dst, a device buffer of
  * [L][2][S_max][H][D] floats, so that tests can check the append bit for bit
@@ -319,13 +353,19 @@ long long wave_debug_act_record_floats(wave_t* h);
  * dst = NULL disables. */
 int wave_debug_phase_times(wave_t* h, long long* dst);
 /* Profiling hook: later steps write, into the device buffer dst of
- * wave_barriers_per_step(h) x wave_grid_size(h) int64, the globaltimer value
- * at which each CTA arrived at each grid barrier ([barrier][cta]), so that
- * the spread of a phase's finishing times can be read.  dst = NULL disables. */
+ * wave_phases_per_step(h) x wave_grid_size(h) int64, the globaltimer value
+ * at which each CTA finished each phase ([phase][cta]; the prologue, then
+ * each layer's phases in order: decoder [first RMSNorm from layer 1 on],
+ * QKV, attention, O, second RMSNorm, gate/up, down; hybrid [RMSNorm from
+ * layer 1 on], in-projection (or QKV), state update (or attention),
+ * out-projection (or O)), so that the spread of a phase's finishing times
+ * and the critical path can be read.  dst = NULL disables. */
 int wave_debug_arrival_times(wave_t* h, long long* dst);
-/* Grid size (CTAs, one per SM) and barriers per step, for tests and tools. */
+/* Grid size (CTAs, one per SM), grid barriers and phases per step, for
+ * tests and tools. */
 int wave_grid_size(wave_t* h);
 int wave_barriers_per_step(wave_t* h);
+int wave_phases_per_step(wave_t* h);
 
 #ifdef __cplusplus
 }

@@ -16,7 +16,7 @@ POISON_CODE = 0x7F
 class DeviceCase:
     """Device buffers of one workload at S sessions (S_max = S unless given)."""
 
-    def __init__(self, w, S=None, S_max=None, poison=True, device_gen=False, pos=None):
+    def __init__(self, w, S=None, S_max=None, poison=True, device_gen=False, pos=None, keep_rowmajor=False):
         self.w = w
         self.S = w.S if S is None else S
         self.S_max = self.S if S_max is None else S_max
@@ -30,11 +30,15 @@ class DeviceCase:
         self.y = torch.zeros_like(self.x)
         n_w = synth.weight_elems(w)
         if device_gen:
-            self.weights = torch.empty(n_w, dtype=torch.bfloat16, device=dev)
-            synth.weights_device(w, self.weights, torch.cuda.current_stream().cuda_stream)
+            rm = torch.empty(n_w, dtype=torch.bfloat16, device=dev)
+            synth.weights_device(w, rm, torch.cuda.current_stream().cuda_stream)
         else:
             self.W_h = synth.weights_host(w)
-            self.weights = torch.from_numpy(self.W_h.view(np.int16)).to(dev).view(torch.bfloat16)
+            rm = torch.from_numpy(self.W_h.view(np.int16)).to(dev).view(torch.bfloat16)
+        # the step reads the packed blob; the row-major one is kept only if asked
+        self.weights = fsd.pack_weights(self.cfg, rm)
+        self.weights_rm = rm if keep_rowmajor else None
+        del rm
         self.kv = torch.zeros((L, 2, self.S_max, H, T, D), dtype=torch.uint8, device=dev)
         self.sc = torch.zeros((L, 2, self.S_max, H, T), dtype=torch.float32, device=dev)
         stream = torch.cuda.current_stream().cuda_stream
@@ -93,7 +97,7 @@ class HybridCase:
     attention blocks' FP8 history (the library's own quantiser, poisoned
     beyond pos), the selective-state blocks' fp32 state, positions, x, y."""
 
-    def __init__(self, w, pos=None, device_gen=False, poison=True, S=None, S_max=None):
+    def __init__(self, w, pos=None, device_gen=False, poison=True, S=None, S_max=None, keep_rowmajor=False):
         self.w = w
         self.S = w.S if S is None else S
         self.S_max = self.S if S_max is None else S_max
@@ -110,11 +114,14 @@ class HybridCase:
         self.y = torch.zeros_like(self.x)
         n_w = synth.hybrid_weight_elems(w)
         if device_gen:
-            self.weights = torch.empty(n_w, dtype=torch.bfloat16, device=dev)
-            synth.hybrid_weights_device(w, self.weights, stream)
+            rm = torch.empty(n_w, dtype=torch.bfloat16, device=dev)
+            synth.hybrid_weights_device(w, rm, stream)
         else:
             self.W_h = synth.hybrid_weights_host(w)
-            self.weights = torch.from_numpy(self.W_h.view(np.int16)).to(dev).view(torch.bfloat16)
+            rm = torch.from_numpy(self.W_h.view(np.int16)).to(dev).view(torch.bfloat16)
+        self.weights = fsd.hybrid_pack_weights(self.cfg, rm)   # the packed blob the step reads
+        self.weights_rm = rm if keep_rowmajor else None
+        del rm
         self.kv = torch.zeros((La, 2, self.S_max, H, T, D), dtype=torch.uint8, device=dev)
         self.sc = torch.zeros((La, 2, self.S_max, H, T), dtype=torch.float32, device=dev)
         raw = torch.empty((self.S, H, T, D), dtype=torch.float32, device=dev)

@@ -60,3 +60,22 @@ def test_hybrid_blob_layout_matches_the_generator(w):
     assert fsd.hybrid_weights_bytes(many) == 0
     many.ssm_heads = 1024
     assert fsd.hybrid_weights_bytes(many) > 0
+
+
+def test_packed_blob_sizes():
+    # every projection matrix padded to 128-row tiles (gate/up: 64-row
+    # halves) and 128-input units, vectors as they are
+    def up(a, b):
+        return -(-a // b) * b
+    for w in (synth.TINY, synth.SEVEN_B, synth.MID, synth.DEPTH):
+        d, HD, F = w.d_model, w.HD, w.ffn
+        per_layer = (2 * d + up(3 * HD, 128) * up(d, 128) + up(d, 128) * up(HD, 128)
+                     + up(F, 64) * 2 * up(d, 128) + up(d, 128) * up(F, 128))
+        assert fsd.packed_weights_bytes(fsd.WaveConfig.of(w)) == 2 * w.n_layers * per_layer
+    assert fsd.packed_weights_bytes(fsd.WaveConfig.of(synth.SEVEN_B)) == fsd.weights_bytes(fsd.WaveConfig.of(synth.SEVEN_B))
+    h = synth.HYBRID
+    d, di, HD, Hs = h.d_model, h.d_inner, h.HD, h.ssm_heads
+    mamba = d + up(h.in_rows, 128) * up(d, 128) + up(d, 128) * up(di, 128) + up(3 * Hs, 8)
+    attn = d + up(3 * HD, 128) * up(d, 128) + up(d, 128) * up(HD, 128)
+    groups = h.n_layers // h.attn_every
+    assert fsd.hybrid_packed_weights_bytes(fsd.WaveHybridConfig.of(h)) == 2 * groups * ((h.attn_every - 1) * mamba + attn)

@@ -40,7 +40,7 @@ def run():
     wp_h = synth.proj_host(w)
     x0_h = synth.x_bf16(w, S)
     dev = "cuda"
-    weights = torch.from_numpy(Wh.view(np.int16)).to(dev).view(torch.bfloat16)
+    weights = fsd.pack_weights(fsd.WaveConfig.of(w), torch.from_numpy(Wh.view(np.int16)).to(dev).view(torch.bfloat16))
     wp = torch.from_numpy(wp_h.view(np.int16)).to(dev).view(torch.bfloat16)
     x0 = torch.from_numpy(x0_h.view(np.int16)).to(dev).view(torch.bfloat16)
     kv = torch.full((L, 2, S, H, T, D), 0x7F, dtype=torch.uint8, device=dev)
@@ -100,7 +100,7 @@ def test_depth_loop_on_a_ragged_prefix_batch():
     L, H, T, D = w.n_layers, w.n_heads, w.T_max, w.head_dim
     Wh = synth.weights_host(w)
     dev = "cuda"
-    weights = torch.from_numpy(Wh.view(np.int16)).to(dev).view(torch.bfloat16)
+    weights = fsd.pack_weights(fsd.WaveConfig.of(w), torch.from_numpy(Wh.view(np.int16)).to(dev).view(torch.bfloat16))
     wp = torch.from_numpy(synth.proj_host(w).view(np.int16)).to(dev).view(torch.bfloat16)
     x0 = torch.from_numpy(synth.x_bf16(w, w.S).view(np.int16)).to(dev).view(torch.bfloat16)
     outs = []

@@ -338,7 +338,7 @@ def test_barrier_timeout_is_reported_and_context_survives():
     wave = fsd.Wave(case.cfg, case.S_max, w.T_max)
     try:
         wave.set_timeout_ns(20_000_000)  # 20 ms
-        wave.debug_skip_barrier(3, 5)
+        wave.debug_skip_barrier(3, 0)
         case.step(wave)
         assert wave.status() == fsd.WAVE_ETIMEOUT
         wave.debug_skip_barrier(-1, -1)
@@ -376,27 +376,31 @@ def test_wide_layer_matches_oracle(wide_weights):
         wave.close()
 
 
-@pytest.mark.parametrize("barrier", [0, 1, 2, 3, "qkv", "gate/up"])
+SIGNALS = {"qkv": 0, "gate/up": 1, "attention": 2, "o": 3, "norm": 5}
+
+
+@pytest.mark.parametrize("barrier", [0, "qkv", "gate/up", "attention", "o", "norm"])
 def test_timeout_at_each_wait_of_a_wide_layer(barrier, wide_weights):
-    # the grid barriers of one layer with no merge phase: 0 before QKV, 1
-    # before O, 2 before the second norm, 3 before gate/up; and the two
-    # hand-overs without a barrier, where a CTA never publishes its finished
-    # QKV tiles (attention waits) or gate/up tiles (the down projection
-    # waits).  Every CTA gives up there, drains its copies and returns
-    # WAVE_ETIMEOUT, and the next step is exact
+    # the one grid barrier of a step (after the prologue) and the hand-overs
+    # between phases, where one item is never published: a QKV tile
+    # (attention waits), a gate/up tile (the down projection waits), a head's
+    # attention rows (the output projection waits), an output-projection tile
+    # (the second norm waits) or a norm row (gate/up waits).  Every CTA gives
+    # up there, drains its copies and returns WAVE_ETIMEOUT, and the next
+    # step is exact
     case = DeviceCase(WIDE1, device_gen=True)
     wave = fsd.Wave(case.cfg, case.S_max, WIDE1.T_max)
     try:
-        assert wave.barriers_per_step == 4
+        assert wave.barriers_per_step == 1
         wave.set_timeout_ns(20_000_000)  # 20 ms
-        if barrier in ("qkv", "gate/up"):
-            wave.debug_skip_signal(7, 0 if barrier == "qkv" else 1)
+        if barrier in SIGNALS:
+            wave.debug_skip_signal(SIGNALS[barrier], 2)
         else:
             wave.debug_skip_barrier(7, barrier)
         case.step(wave)
         assert wave.status() == fsd.WAVE_ETIMEOUT
         wave.debug_skip_barrier(-1, -1)
-        wave.debug_skip_signal(-1)
+        wave.debug_skip_signal(0, -1)
         wave.set_timeout_ns(2_000_000_000)
         fresh = DeviceCase(WIDE1, device_gen=True)
         fresh.step(wave)

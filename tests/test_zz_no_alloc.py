@@ -61,7 +61,7 @@ def test_static_scratch_rejects_a_shape_that_does_not_fit():
     cfg = fsd.WaveConfig(1, 64, 1, 64, 64, 1e-5, 1e4)
     T = 200_000
     dev = "cuda"
-    weights = torch.zeros(fsd.weights_bytes(cfg) // 2, dtype=torch.bfloat16, device=dev)
+    weights = torch.zeros(fsd.packed_weights_bytes(cfg) // 2, dtype=torch.bfloat16, device=dev)
     kv = torch.zeros((1, 2, 1, 1, T, 64), dtype=torch.uint8, device=dev)
     sc = torch.zeros((1, 2, 1, 1, T), dtype=torch.float32, device=dev)
     pos = torch.zeros(1, dtype=torch.int32, device=dev)
