@@ -297,34 +297,10 @@ __device__ __forceinline__ float4 ld4cg(const float* q) { return __ldcg((const f
 __device__ __forceinline__ void add4(float4& a, const float4& b) {
   a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
 }
-// Sum, in segment order, of the float4 at element offsets o0 / o1 of each of
+// Sum, in segment order, of the float4 at element offsets o0..o3 of each of
 // a tile's partial slots (the first at `first`, the others at part +
-// seg[1..nseg)); the first five segments' loads in flight together, four
-// more per later pass.  kOne: the tile has one segment (no partner slots).
-template <bool kOne>
-__device__ __forceinline__ void seg_sum2(const float* first, const float* part, const long long* seg,
-                                         int nseg, size_t o0, size_t o1, float4& a0, float4& a1) {
-  a0 = ld4cg(first + o0);
-  a1 = ld4cg(first + o1);
-  if (kOne) return;
-  for (int j = 1; j < nseg; j += 2) {
-    float4 t0[2], t1[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k)
-      if (j + k < nseg) {
-        t0[k] = ld4cg(part + seg[j + k] + o0);
-        t1[k] = ld4cg(part + seg[j + k] + o1);
-      }
-#pragma unroll
-    for (int k = 0; k < 2; ++k)
-      if (j + k < nseg) {
-        add4(a0, t0[k]);
-        add4(a1, t1[k]);
-      }
-  }
-}
-// The same for four offsets (four items, or gate and up rows of two items),
-// two more segments per later pass.
+// seg[1..nseg)); the four loads of a segment in flight together.  kOne: the
+// tile has one segment (no partner slots).
 template <bool kOne>
 __device__ __forceinline__ void seg_sum4(const float* first, const float* part, const long long* seg,
                                          int nseg, size_t o0, size_t o1, size_t o2, size_t o3,
@@ -374,18 +350,40 @@ __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t
                                          const float* part, const long long* seg, int nseg, int et, int step,
                                          bool last_layer, int frame) {
   if (kind == kGU) {
-    // item (s, r4): gate rows 4r4..4r4+3 and the up rows 64 below them
+    // item (s, r4): gate rows 4r4..4r4+3 and the up rows 64 below them; four
+    // items per pass, their eight loads per segment in flight together
     const int F = p.F, items = p.S * 16;
 #pragma unroll 1
-    for (int i0 = et; i0 < items; i0 += 2 * step) {
-      const int i1 = i0 + step;
-      const bool two = i1 < items;
-      const size_t o0 = (size_t)(i0 >> 4) * kTileM + 4 * (i0 & 15);
-      const size_t o1 = two ? (size_t)(i1 >> 4) * kTileM + 4 * (i1 & 15) : o0;
-      float4 g0, g1, u0, u1;
-      seg_sum4<kOne>(first, part, seg, nseg, o0, o1, o0 + 64, o1 + 64, g0, g1, u0, u1);
-      swiglu_store(p.u + (size_t)(i0 >> 4) * F, t * 64 + 4 * (i0 & 15), F, g0, u0);
-      if (two) swiglu_store(p.u + (size_t)(i1 >> 4) * F, t * 64 + 4 * (i1 & 15), F, g1, u1);
+    for (int i0 = et; i0 < items; i0 += 4 * step) {
+      int iv[4];
+      size_t ov[4];
+      float4 g[4], u[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        iv[k] = (i0 + k * step < items) ? i0 + k * step : i0;
+        ov[k] = (size_t)(iv[k] >> 4) * kTileM + 4 * (iv[k] & 15);
+        g[k] = ld4cg(first + ov[k]);
+        u[k] = ld4cg(first + ov[k] + 64);
+      }
+      if (!kOne) {
+        for (int j = 1; j < nseg; ++j) {
+          const float* bk = part + seg[j];
+          float4 tg[4], tu[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            tg[k] = ld4cg(bk + ov[k]);
+            tu[k] = ld4cg(bk + ov[k] + 64);
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            add4(g[k], tg[k]);
+            add4(u[k], tu[k]);
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (k == 0 || iv[k] != i0) swiglu_store(p.u + (size_t)(iv[k] >> 4) * F, t * 64 + 4 * (iv[k] & 15), F, g[k], u[k]);
     }
   } else if (kind == kProj) {
     // item (s, r4): the next frame's input x[frame][s][n..n+3] in bf16; four items per pass
@@ -434,22 +432,26 @@ __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t
       }
     }
   } else {
-    // item (s, r4): output rows 4r4..4r4+3 of the tile, residual added
+    // item (s, r4): output rows 4r4..4r4+3 of the tile, residual added; four
+    // items per pass, their old values' and partials' loads in flight together
     const int d = p.d, items = p.S * 32;
 #pragma unroll 1
-    for (int i0 = et; i0 < items; i0 += 2 * step) {
-      const int i1 = i0 + step;
-      const bool two = i1 < items;
-      const int s0 = i0 >> 5, s1 = two ? (i1 >> 5) : s0;
-      const int n0 = t * kTileM + 4 * (i0 & 31), n1 = two ? t * kTileM + 4 * (i1 & 31) : n0;
-      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 old0 = (n0 < d) ? __ldcg((const float4*)(p.resid + (size_t)s0 * d + n0)) : z;
-      const float4 old1 = (n1 < d) ? __ldcg((const float4*)(p.resid + (size_t)s1 * d + n1)) : z;
-      float4 a0, a1;
-      seg_sum2<kOne>(first, part, seg, nseg, (size_t)s0 * kTileM + (n0 - t * kTileM),
-               (size_t)s1 * kTileM + (n1 - t * kTileM), a0, a1);
-      if (n0 < d) resid_store(p, s0, n0, old0, a0, last_layer, frame);
-      if (two && n1 < d) resid_store(p, s1, n1, old1, a1, last_layer, frame);
+    for (int i0 = et; i0 < items; i0 += 4 * step) {
+      int iv[4], nv[4];
+      size_t ov[4];
+      float4 old[4], a[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        iv[k] = (i0 + k * step < items) ? i0 + k * step : i0;
+        nv[k] = t * kTileM + 4 * (iv[k] & 31);
+        ov[k] = (size_t)(iv[k] >> 5) * kTileM + 4 * (iv[k] & 31);
+        old[k] = (nv[k] < d) ? __ldcg((const float4*)(p.resid + (size_t)(iv[k] >> 5) * d + nv[k]))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      seg_sum4<kOne>(first, part, seg, nseg, ov[0], ov[1], ov[2], ov[3], a[0], a[1], a[2], a[3]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if ((k == 0 || iv[k] != i0) && nv[k] < d) resid_store(p, iv[k] >> 5, nv[k], old[k], a[k], last_layer, frame);
     }
   }
 }
