@@ -297,10 +297,26 @@ __device__ __forceinline__ float4 ld4cg(const float* q) { return __ldcg((const f
 __device__ __forceinline__ void add4(float4& a, const float4& b) {
   a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
 }
-// Sum, in segment order, of the float4 at element offsets o0..o3 of each of
-// a tile's partial slots (the first at `first`, the others at part +
-// seg[1..nseg)); the four loads of a segment in flight together.  kOne: the
+// Sum, in segment order, of the float4 at element offsets o[0..NI) of each
+// of a tile's partial slots (the first at `first`, the others at part +
+// seg[1..nseg)); the NI loads of a segment in flight together.  kOne: the
 // tile has one segment (no partner slots).
+template <bool kOne, int NI>
+__device__ __forceinline__ void seg_sumn(const float* first, const float* part, const long long* seg, int nseg,
+                                         const size_t* o, float4* a) {
+#pragma unroll
+  for (int k = 0; k < NI; ++k) a[k] = __ldcg((const float4*)(first + o[k]));
+  if (kOne) return;
+  for (int j = 1; j < nseg; ++j) {
+    const float* bk = part + seg[j];
+    float4 tv[NI];
+#pragma unroll
+    for (int k = 0; k < NI; ++k) tv[k] = __ldcg((const float4*)(bk + o[k]));
+#pragma unroll
+    for (int k = 0; k < NI; ++k) add4(a[k], tv[k]);
+  }
+}
+// The same for four offsets passed one by one.
 template <bool kOne>
 __device__ __forceinline__ void seg_sum4(const float* first, const float* part, const long long* seg,
                                          int nseg, size_t o0, size_t o1, size_t o2, size_t o3,
@@ -411,22 +427,24 @@ __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t
       }
     }
   } else if (kind == kQKV || kind == kIn) {
-    // item (s, r4): output rows 4r4..4r4+3 of the tile (fp32); four items per pass
+    // item (s, r4): output rows 4r4..4r4+3 of the tile (fp32); five items per
+    // pass (two passes for a tile finished by one CTA at S = 80)
+    constexpr int QI = 5;
     const int N = (kind == kQKV) ? 3 * p.HD : p.in_rows, items = p.S * 32;
     float* dst = (kind == kQKV) ? p.qkv : p.zx;
 #pragma unroll 1
-    for (int i0 = et; i0 < items; i0 += 4 * step) {
-      int iv[4];
-      size_t ov[4];
+    for (int i0 = et; i0 < items; i0 += QI * step) {
+      int iv[QI];
+      size_t ov[QI];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < QI; ++k) {
         iv[k] = (i0 + k * step < items) ? i0 + k * step : i0;
         ov[k] = (size_t)(iv[k] >> 5) * kTileM + 4 * (iv[k] & 31);
       }
-      float4 a[4];
-      seg_sum4<kOne>(first, part, seg, nseg, ov[0], ov[1], ov[2], ov[3], a[0], a[1], a[2], a[3]);
+      float4 a[QI];
+      seg_sumn<kOne, QI>(first, part, seg, nseg, ov, a);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < QI; ++k) {
         const int n = t * kTileM + 4 * (iv[k] & 31);
         if ((k == 0 || iv[k] != i0) && n < N) *(float4*)(dst + (size_t)(iv[k] >> 5) * N + n) = a[k];
       }
