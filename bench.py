@@ -651,7 +651,7 @@ def run_depth(args):
             "config": {"workload": w.name, "S": S, "steps_per_frame": steps, "T_max": T,
                        "l2": "weights re-read every dependent step (154 MB, larger than L2)"},
             "roofline": roofline_of(b, ms), "clocks": clk, "cpu_baseline": None,
-            "barriers_per_frame": steps * (6 * L - 1) + 2 * (steps - 1)}
+            "grid_barriers_per_frame": steps * wave.barriers_per_step + 2 * (steps - 1)}
     if not args.no_cpu_baseline:
         import oracle
         Wh, wp_h, x_h = synth.weights_host(w), synth.proj_host(w), synth.x_bf16(w, 1)
@@ -715,31 +715,35 @@ def run_hybrid(args):
     if wave.status() != fsd.WAVE_OK:
         raise RuntimeError("warm-up hybrid step failed")
     if args.phases:
-        ts = torch.zeros(wave.barriers_per_step + 2, dtype=torch.int64, device=device)
-        wave.debug_phase_times(ts)
-        runs = []
+        # phase-end marks: each phase's time is the last CTA's finish minus
+        # the last CTA's finish of the phase before (the hand-overs overlap)
+        n, grid = wave.phases_per_step, wave.grid
+        ts = torch.zeros((n, grid), dtype=torch.int64, device=device)
+        wave.debug_arrival_times(ts)
+        ends = []
         for _ in range(3):
             wave.hybrid_step(S, weights, kv, sc, state, pos, x, y, stream=stream)
             if wave.status() != fsd.WAVE_OK:
                 raise RuntimeError("step failed")
-            runs.append(np.diff(ts.cpu().numpy().astype(np.float64)) / 1000.0)
-        wave.debug_phase_times(None)
-        t = np.mean(runs, axis=0)
+            tm = ts.cpu().numpy().astype(np.float64) / 1000.0
+            ends.append(np.diff(np.concatenate([[tm.min()], tm.max(axis=1)])))
+        wave.debug_arrival_times(None)
+        t = np.mean(ends, axis=0)
         names = ["prologue"]
-        merge = -(-T // 32) > 16
         for l in range(w.n_layers):
             if l > 0:
                 names.append("norm")
-            names += (["qkv", "attn"] + (["merge"] if merge else []) + ["o"]) if w.is_attn(l) else ["in", "ssm", "out"]
-        print(f"{w.name} S={S}: step {t.sum():.1f} us (phase = work + the grid barrier after it)")
+            names += ["qkv", "attn", "o"] if w.is_attn(l) else ["in", "ssm", "out"]
+        print(f"{w.name} S={S}: {t.sum():.1f} us from the first mark (phase = the last CTA's finish minus "
+              "the last CTA's finish of the phase before)")
         agg = {}
-        for n, v in zip(names, t):
-            agg.setdefault(n, []).append(v)
+        for n_, v in zip(names, t):
+            agg.setdefault(n_, []).append(v)
         blk = w.ssm_heads * w.ssm_head_dim * w.ssm_state * 4 * 2 * S
-        for n, v in agg.items():
+        for n_, v in agg.items():
             m = float(np.mean(v))
-            extra = f"  {blk / m / 1e3:6.0f} GB/s of state" if n == "ssm" else ""
-            print(f"  {n:8s} x{len(v):3d}  mean {m:8.1f} us  total {np.sum(v):9.1f} us "
+            extra = f"  {blk / m / 1e3:6.0f} GB/s of state" if n_ == "ssm" else ""
+            print(f"  {n_:8s} x{len(v):3d}  mean {m:8.1f} us  total {np.sum(v):9.1f} us "
                   f"({100 * np.sum(v) / t.sum():5.1f}%){extra}")
         wave.close()
         return

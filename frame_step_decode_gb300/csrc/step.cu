@@ -835,12 +835,9 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
   const uint64_t kv_policy = policy_evict_first();
 
   // Dynamic assignment over the longest-first list: warp gw starts with entry
-  // gw, then takes the next unclaimed entry from the layer's counter, claimed
-  // one piece ahead so that the atomic's latency hides behind the current one.
+  // gw, then takes the next unclaimed entry from the layer's counter.
   int* ctr = p.att_ctr + layer;
   for (int pi = gw; pi < n_pieces;) {
-    int nxt = 0;
-    if (lane == 0) nxt = NW + atomicAdd(ctr, 1);
     const int4 pc = __ldcg(p.pieces + 2 * pi);
     const int P = __ldcg(p.pieces + 2 * pi + 1).x;
     const int sh = pc.x, c_lo = pc.y & 0xFFFF, c_hi = pc.y >> 16, np = pc.z, first = pc.w;
@@ -1193,6 +1190,12 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
         attn_row_done(p, h, layer, lane);
       }
     }
+    // the next piece is claimed once this warp is free (a piece claimed
+    // ahead would wait behind the current one while other warps run dry
+    // at the end of the list; the claim's latency hides behind the other
+    // warps' copies)
+    int nxt = 0;
+    if (lane == 0) nxt = NW + atomicAdd(ctr, 1);
     pi = __shfl_sync(0xffffffffu, nxt, 0);
   }
 }
