@@ -366,40 +366,26 @@ __device__ __forceinline__ void finish_tile(const StepParams& p, int kind, int t
                                          const float* part, const long long* seg, int nseg, int et, int step,
                                          bool last_layer, int frame) {
   if (kind == kGU) {
-    // item (s, r4): gate rows 4r4..4r4+3 and the up rows 64 below them; four
-    // items per pass, their eight loads per segment in flight together
+    // item (s, r4): gate rows 4r4..4r4+3 and the up rows 64 below them; five
+    // items per pass, their ten loads per segment in flight together
+    constexpr int GI = 5;
     const int F = p.F, items = p.S * 16;
 #pragma unroll 1
-    for (int i0 = et; i0 < items; i0 += 4 * step) {
-      int iv[4];
-      size_t ov[4];
-      float4 g[4], u[4];
+    for (int i0 = et; i0 < items; i0 += GI * step) {
+      int iv[GI];
+      size_t ov[2 * GI];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < GI; ++k) {
         iv[k] = (i0 + k * step < items) ? i0 + k * step : i0;
         ov[k] = (size_t)(iv[k] >> 4) * kTileM + 4 * (iv[k] & 15);
-        g[k] = ld4cg(first + ov[k]);
-        u[k] = ld4cg(first + ov[k] + 64);
+        ov[GI + k] = ov[k] + 64;
       }
-      if (!kOne) {
-        for (int j = 1; j < nseg; ++j) {
-          const float* bk = part + seg[j];
-          float4 tg[4], tu[4];
+      float4 a[2 * GI];
+      seg_sumn<kOne, 2 * GI>(first, part, seg, nseg, ov, a);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            tg[k] = ld4cg(bk + ov[k]);
-            tu[k] = ld4cg(bk + ov[k] + 64);
-          }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            add4(g[k], tg[k]);
-            add4(u[k], tu[k]);
-          }
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (k == 0 || iv[k] != i0) swiglu_store(p.u + (size_t)(iv[k] >> 4) * F, t * 64 + 4 * (iv[k] & 15), F, g[k], u[k]);
+      for (int k = 0; k < GI; ++k)
+        if (k == 0 || iv[k] != i0)
+          swiglu_store(p.u + (size_t)(iv[k] >> 4) * F, t * 64 + 4 * (iv[k] & 15), F, a[k], a[GI + k]);
     }
   } else if (kind == kProj) {
     // item (s, r4): the next frame's input x[frame][s][n..n+3] in bf16; four items per pass
