@@ -9,8 +9,9 @@ latency and the HBM roofline fraction of the step kernel.
   python bench.py [--gpus N --steps K --warmup W] [--S 80] [--impl reference]
   python bench.py --sweep 1,8,16,32,48,56,64,80,96,128 --steps 20
   python bench.py --beat 2
-  python bench.py --depth
-  python bench.py --hybrid
+  python bench.py --depth [--phases]
+  python bench.py --hybrid [--phases]
+  python bench.py --phases [--layers L]      (per-phase times of one step)
 
 Inputs are seeded and synthetic and are drawn on the device (weights and the
 raw history by the generator's device twin, the history quantised by the
@@ -821,7 +822,10 @@ def main():
     if args.hybrid:
         run_hybrid(args)
     elif args.depth:
-        run_depth(args)
+        if args.phases:  # one dependent step of the loop's model, phase by phase
+            run_phases(args, synth.DEPTH)
+        else:
+            run_depth(args)
     elif args.beat:
         run_beat(args, w)
     elif args.sweep:
