@@ -114,6 +114,7 @@ constexpr int kTileCntWords = 2048;
 constexpr int kDoneCntOff = 2 * kTileCntWords;   // per projection kind: tiles finished so far this frame
 constexpr int kHeadsDone = 8;                    // done_cnt[8]: heads whose attention rows are all written
 constexpr int kNormRows = 9;                     // done_cnt[9]: RMSNorm rows written this frame
+constexpr int kSsmDone = 10;                     // done_cnt[10]: selective-state items finished this frame
 constexpr int kQkvDoneOff = kDoneCntOff + 32;
 constexpr int kHeadCntOff = kQkvDoneOff + 1024;  // per head: (session, head) rows written this frame
 constexpr int kAttCtrOff = kHeadCntOff + 1024;

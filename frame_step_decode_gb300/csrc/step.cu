@@ -1200,7 +1200,12 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
 // Returns false if a copy wait gave up.
 constexpr int kSsmSide = 64 + 64 + kSsmN + kSsmN + 4;              // x, z, B, C, dt group (floats)
 constexpr int kSsmStageF = kSsmP * kSsmN + ((kSsmSide + 31) / 32) * 32;  // floats per stage
-__device__ __forceinline__ bool ssm_phase(const StepParams& p, Ctx& c, int lm, int l) {
+// The items read the in-projection's rows once every tile of this block's
+// in-projection is published (wait_target on its finished-tile count; 0: a
+// grid barrier came before); every CTA counts its items done in the
+// selective-state count when they are written, which the out-projection
+// waits for.
+__device__ __forceinline__ bool ssm_phase(const StepParams& p, Ctx& c, int lm, int l, int wait_target) {
   static_assert(kWarps * 8 == kSsmP && 32 * 4 == kSsmN, "state phase layout");
   constexpr uint32_t kBlk = kSsmP * kSsmN * 4;
   constexpr uint32_t kTx = kBlk + (64 + 64 + kSsmN + kSsmN + 4) * 4;
@@ -1231,6 +1236,15 @@ __device__ __forceinline__ bool ssm_phase(const StepParams& p, Ctx& c, int lm, i
       bulk_load(dst + kBlk + 512 + 2 * kSsmN * 4, zrow + 2 * di + 2 * N + (hh & ~3), 16, b);  // dt
     }
   };
+  if (wait_target > 0 && my > 0) {
+    if (threadIdx.x == 0) {
+      const bool ok0 = wait_flag_ge(p, p.done_cnt + kIn, wait_target);
+      fence_proxy_async_global();  // the copies below read those tiles' rows
+      *misc_word(c, 7) = ok0 ? 1 : 0;
+    }
+    __syncthreads();
+    if (!*misc_word(c, 7)) return false;
+  }
   if (threadIdx.x == 0) {
     fence_proxy_async_smem();  // earlier generic accesses to the ring come first
     for (int k = 0; k < min(my, kSsmStages); ++k) issue(k);
@@ -1297,6 +1311,14 @@ __device__ __forceinline__ bool ssm_phase(const StepParams& p, Ctx& c, int lm, i
   }
   c.ssm_it += (uint32_t)my;
   fence_proxy_async_smem();  // the next phase's copies overwrite the ring
+  if (wait_target > 0 && my > 0) {
+    fence_proxy_async_global();  // the out-projection reads these rows by TMA
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      atomicAdd(p.done_cnt + kSsmDone, my);
+    }
+  }
   return true;
 }
 
@@ -1587,7 +1609,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       // attention starts without a grid barrier: each piece waits for the QKV
       // tiles it reads (the selective-state phase still takes one; the dump
       // kernel takes one to read the projection's output whole)
-      if (kDump || !attn_layer) {
+      // attention and the selective-state phase start without a grid barrier:
+      // a piece waits for the QKV tiles it reads, the state items for every
+      // tile of the in-projection (the dump kernel takes a barrier to read
+      // the projection's output whole)
+      if (kDump) {
         if (!(ok = grid_sync(p, c))) break;
       } else {
         __syncthreads();
@@ -1611,8 +1637,14 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         }
         mark_phase(p, c);
       } else if constexpr (kHybrid) {
-        const bool sok = ssm_phase(p, c, l - l / e, l);
-        if (!(ok = grid_sync(p, c) && sok)) break;
+        const int lm = l - l / e;
+        const bool sok = ssm_phase(p, c, lm, l, kDump ? 0 : (lm + 1) * p.tiles[kIn]);
+        if constexpr (kDump) {
+          if (!(ok = grid_sync(p, c) && sok)) break;
+        } else {
+          __syncthreads();
+          if (!(ok = sok)) break;
+        }
         mark_phase(p, c);
         if (kDump) act_dump_rows(p, c.frame, l, kActMix, p.ssm_out, p.d_inner, p.d_inner);
       }
@@ -1620,8 +1652,15 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       // written; with no live session there is none to wait for), or the
       // selective-state out-projection
       if constexpr (kHybrid) {
-        gemm_phase(p, c, attn_layer ? kO : kOut, li, last,
-                   attn_layer && __ldcg(p.n_pieces + 1) > 0 ? p.done_cnt + kHeadsDone : nullptr, (li + 1) * p.H);
+        // the out-projection: O once every head's rows are written (with no
+        // live session there is none to wait for), the selective-state one
+        // once every item of the block is
+        const int lm = l - l / e;
+        if (attn_layer)
+          gemm_phase(p, c, kO, li, last, __ldcg(p.n_pieces + 1) > 0 ? p.done_cnt + kHeadsDone : nullptr,
+                     (li + 1) * p.H);
+        else
+          gemm_phase(p, c, kOut, li, last, kDump ? nullptr : p.done_cnt + kSsmDone, (lm + 1) * p.S * p.ssm_heads);
       } else {
         gemm_phase(p, c, kO, li, false, __ldcg(p.n_pieces + 1) > 0 ? p.done_cnt + kHeadsDone : nullptr,
                    (li + 1) * p.H);
@@ -1733,9 +1772,7 @@ int phases_per_step(int L, bool hybrid, int attn_every) {
   return n;
 }
 int hybrid_barriers_per_step(int L, int attn_every, int T_max) {
-  int n = 1;  // prologue
-  for (int l = 0; l < L; ++l) n += (l % attn_every == attn_every - 1) ? 0 : 2;  // in-projection, state phase
-  return n;
+  return 1;  // the prologue's; every other hand-over is a count or a flag
 }
 int barriers_per_launch(int L, int T_max, int frames, bool advance, bool depth) {
   return frames * barriers_per_step(L, T_max) + (frames - 1) * (depth ? 2 : 1) + (advance ? 1 : 0);
