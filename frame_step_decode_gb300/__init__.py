@@ -251,7 +251,9 @@ class Wave:
     def debug_skip_signal(self, which: int, index: int) -> None:
         """Testing hook: later steps never publish item `index` of kind
         `which` (0 QKV tile, 1 gate/up tile, 2 a head's attention rows, 3 O
-        tile, 4 down tile, 5 norm row); index < 0 disables."""
+        tile, 4 down tile, 5 norm row; hybrid: 6 selective-state
+        in-projection tile, 7 a CTA's finished state items, 8 selective-state
+        out-projection tile); index < 0 disables."""
         rc = lib().wave_debug_skip_signal(self.h, which, index)
         if rc != WAVE_OK:
             raise WaveError(rc, "wave_debug_skip_signal")

@@ -300,7 +300,7 @@ extern "C" int wave_debug_skip_barrier(wave_t* h, int cta, int barrier) {
 }
 
 extern "C" int wave_debug_skip_signal(wave_t* h, int which, int index) {
-  if (!h || (index >= 0 && (which < 0 || which > 5))) return WAVE_EINVAL;
+  if (!h || (index >= 0 && (which < 0 || which > 8))) return WAVE_EINVAL;
   h->skip_sig = index;
   h->skip_sig_kind = which;
   return WAVE_OK;

@@ -135,9 +135,13 @@ __device__ __forceinline__ bool wait_flag_ge_light(const StepParams& p, const in
 }
 
 // What a testing hook may withhold (wave_debug_skip_signal's `which`).
-enum SigKind : int { kSigQkv = 0, kSigGu = 1, kSigAttn = 2, kSigO = 3, kSigDown = 4, kSigNorm = 5 };
+enum SigKind : int {
+  kSigQkv = 0, kSigGu = 1, kSigAttn = 2, kSigO = 3, kSigDown = 4, kSigNorm = 5,
+  kSigIn = 6, kSigSsm = 7, kSigOut = 8  // the hybrid's selective-state blocks
+};
 __device__ __forceinline__ int sig_of(int kind) {
-  return kind == kQKV ? kSigQkv : kind == kGU ? kSigGu : kind == kO ? kSigO : kind == kDown ? kSigDown : -1;
+  return kind == kQKV ? kSigQkv : kind == kGU ? kSigGu : kind == kO ? kSigO : kind == kDown ? kSigDown
+       : kind == kIn ? kSigIn : kind == kOut ? kSigOut : -1;
 }
 
 // Projections whose next phase starts without a grid barrier publish every
@@ -1314,7 +1318,7 @@ __device__ __forceinline__ bool ssm_phase(const StepParams& p, Ctx& c, int lm, i
   if (wait_target > 0 && my > 0) {
     fence_proxy_async_global();  // the out-projection reads these rows by TMA
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && !(p.skip_sig == (int)blockIdx.x && p.skip_sig_kind == kSigSsm)) {
       __threadfence();
       atomicAdd(p.done_cnt + kSsmDone, my);
     }

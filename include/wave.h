@@ -318,8 +318,11 @@ int wave_debug_skip_barrier(wave_t* h, int cta, int barrier);
  * down projection waits), 2 the attention rows of head `index` (the output
  * projection waits), 3 the output-projection tile `index` (the second
  * RMSNorm waits), 4 the down-projection tile `index` (the next layer's first
- * RMSNorm waits), 5 the RMSNorm row `index` (the next projection waits).
- * index < 0 disables. */
+ * RMSNorm waits), 5 the RMSNorm row `index` (the next projection waits);
+ * in the hybrid step also 6 the selective-state in-projection tile `index`
+ * (the state items wait), 7 the finished state items of CTA `index` (the
+ * out-projection waits), 8 the selective-state out-projection tile `index`
+ * (the next RMSNorm waits).  index < 0 disables. */
 int wave_debug_skip_signal(wave_t* h, int which, int index);
 /* Make later steps also write, for every session with a valid position, the
  * fp32 K (after RoPE) and V rows they quantise into dst, a device buffer of

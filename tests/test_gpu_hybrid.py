@@ -172,6 +172,34 @@ def test_hybrid_prefix_batch_in_a_larger_handle_matches_oracle():
         assert _normwise(st_g[lm], st_o[lm]) <= 2e-2, lm
 
 
+@pytest.mark.parametrize("which", [6, 7, 8, 0])
+def test_hybrid_timeout_at_each_hand_over(which):
+    # one item never published: a selective-state in-projection tile (the
+    # state items wait), one CTA's finished state items (the out-projection
+    # waits), an out-projection tile (the next norm waits), an attention
+    # block's QKV tile (attention waits).  Every CTA gives up, drains its
+    # copies and returns WAVE_ETIMEOUT; the next step on the same context
+    # is right again
+    w = synth.HYBRID_SMALL
+    case = HybridCase(w)
+    wave = fsd.HybridWave(case.cfg, case.S_max, w.T_max)
+    try:
+        assert wave.barriers_per_step == 1
+        wave.set_timeout_ns(20_000_000)  # 20 ms
+        wave.debug_skip_signal(which, {6: 2, 7: 2, 8: 1, 0: 1}[which])   # items that exist at this shape
+        case.step(wave)
+        assert wave.status() == fsd.WAVE_ETIMEOUT
+        wave.debug_skip_signal(0, -1)
+        wave.set_timeout_ns(2_000_000_000)
+        fresh = HybridCase(w)
+        fresh.step(wave)
+        assert wave.status() == fsd.WAVE_OK
+    finally:
+        wave.close()
+    W = synth.hybrid_weights_host(w)
+    _y_within_oracle_sensitivity(w, W, list(range(w.S)), fresh.pos_h, fresh.x_h, fresh.y_bits())
+
+
 @pytest.fixture(scope="module")
 def full():
     w = synth.HYBRID
