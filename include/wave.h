@@ -285,8 +285,8 @@ int wave_fp8_encode(const float* in, int64_t n, uint8_t* out, void* stream);
  * wave_step for callers that cannot allocate device memory (inside another
  * runtime's memory pool or a fixed device-memory budget, a plug-in that must
  * not create untracked allocations, or a real-time loop where cudaMalloc's
- * implicit synchronisation is not allowed).  The paper has no counterpart:
- * this is an interface addition of this library.
+ * implicit synchronisation is not allowed).  No source page describes such
+ * a call: it is an interface addition of this library.
  *
  * Same arguments and layouts as wave_create(cfg, S_max, T_max) followed by
  * wave_step(S, ...), but no handle and no allocation: the workspace lives in
