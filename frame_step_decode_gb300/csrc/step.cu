@@ -1,18 +1,19 @@
 // step.cu -- the persistent frame-step kernel: one cooperative launch runs
-// every layer for all S sessions, phases separated by device-side grid
-// barriers (no CPU round trip between operations: dotwave.ai case study,
-// "02 / The solution" and "04 / Under the hood").
+// every layer for all S sessions, with no CPU round trip between operations
+// (dotwave.ai case study, "02 / The solution" and "04 / Under the hood").
+// One grid barrier per frame (after its prologue); every other hand-over
+// between phases is a bounded wait on a count or flag in global memory, for
+// exactly the data the next phase reads.
 //
-// Decoder layer l (8 grid barriers per layer; 7 when no history is long
-// enough to be split into several attention pieces):
+// Decoder layer l:
 //   norm     RMSNorm rows of the fp32 residual -> bf16 xn           (CUDA cores)
 //   QKV      xn . Wqkv^T -> fp32 q,k,v                              (tcgen05, stream-K)
 //   attn     per (session, head) piece: RoPE(q); the piece holding the
 //            current slot also RoPEs k, quantises k and v to E4M3 and
 //            appends them at slot pos; then split-T flash-decode over the
-//            FP8 history (mma.sync f16 with in-register dequantisation),
-//            partials of split (session, head) pairs kept     (TMA + mma.sync)
-//   merge    combine the split-T partials -> bf16 attention output
+//            FP8 history (mma.sync f16 with in-register dequantisation);
+//            the warp finishing a split pair's last piece merges its
+//            partials -> bf16 attention output                 (TMA + mma.sync)
 //   O        resid += attn . Wo^T                                  (tcgen05, stream-K)
 //   norm     RMSNorm -> xn
 //   GU       u = bf16(silu(xn . Wg^T) * (xn . Wu^T))               (tcgen05, stream-K)
@@ -28,9 +29,9 @@
 // weight/activation tiles into a shared-memory ring, warp 1 issues tcgen05
 // MMAs into a double-buffered TMEM accumulator, warps 2..5 drain TMEM into
 // split-K partial slots; the split tile a CTA's span ends in is then summed
-// by all its threads.  Attention, the norms, the merge and the state update
-// use all 8 warps.  Every wait is bounded (globaltimer) and reports
-// WAVE_ETIMEOUT through the device error word instead of hanging.
+// by all its threads.  Attention, the norms and the state update use all 8
+// warps.  Every wait is bounded (globaltimer) and reports WAVE_ETIMEOUT
+// through the device error word instead of hanging.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
@@ -1610,9 +1611,6 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       // follows the prologue's grid barrier)
       const int n_rows = (hyb ? l : 2 * l) * p.S;
       gemm_phase(p, c, attn_layer ? kQKV : kIn, li, false, l > 0 ? p.done_cnt + kNormRows : nullptr, n_rows);
-      // attention starts without a grid barrier: each piece waits for the QKV
-      // tiles it reads (the selective-state phase still takes one; the dump
-      // kernel takes one to read the projection's output whole)
       // attention and the selective-state phase start without a grid barrier:
       // a piece waits for the QKV tiles it reads, the state items for every
       // tile of the in-projection (the dump kernel takes a barrier to read
