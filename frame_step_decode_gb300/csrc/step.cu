@@ -1258,13 +1258,17 @@ __device__ __forceinline__ bool ssm_phase(const StepParams& p, Ctx& c, int lm, i
   for (int k = 0; k < my; ++k) {
     const int i = (int)blockIdx.x + k * (int)gridDim.x, s = i / Hs, hh = i - s * Hs;
     const uint32_t st = (c.ssm_it + (uint32_t)k) % kSsmStages;
+    volatile int* flag = misc_word(c, (k & 1) ? 10 : 7);  // alternating: no word is rewritten while read
     if (threadIdx.x == 0) {
       const bool ok0 = mbar_wait(bar_ssm(c, st), ((c.ssm_it + (uint32_t)k) / kSsmStages) & 1u, p.timeout_ns, p.err);
       if (!ok0) set_err(p, kErrTimeout);
-      *misc_word(c, 7) = ok0 ? 1 : 0;
+      *flag = ok0 ? 1 : 0;
     }
+    // one barrier per item: every thread is past item k - 1 (its reads of
+    // that stage fenced), so the stage it used is refilled now
     __syncthreads();
-    if (!*misc_word(c, 7)) return false;
+    if (!*flag) return false;
+    if (threadIdx.x == 0 && k >= 1 && k - 1 + kSsmStages < my) issue(k - 1 + kSsmStages);
     uint16_t* orow = p.ssm_out + (size_t)s * di + hh * kSsmP + warp * 8;
     if (p.pos[s] < 0) {
       if (lane < 8) orow[lane] = 0;
@@ -1295,27 +1299,44 @@ __device__ __forceinline__ bool ssm_phase(const StepParams& p, Ctx& c, int lm, i
         __stcs((float4*)(gst + pr * N + 4 * lane), h);  // streamed: read again only next frame
         yv[j] = C4.x * h.x + C4.y * h.y + C4.z * h.z + C4.w * h.w;
       }
+      // y over the 32 lanes of each of the 8 rows by recursive halving: lane
+      // bits 4, 3, 2 pick a half of the rows at each of the first three
+      // levels (4 + 2 + 1 shuffles), bits 1, 0 sum the last value; lane l
+      // then holds row 4 b4 + 2 b3 + b2 whole
+      {
+        const bool h4 = lane & 16, h3 = lane & 8, h2 = lane & 4;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
+        for (int j = 0; j < 4; ++j) {
+          const float send = h4 ? yv[j] : yv[j + 4];
+          const float keep = h4 ? yv[j + 4] : yv[j];
+          yv[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) yv[j] += __shfl_xor_sync(0xffffffffu, yv[j], o);
-      if (lane < 8) {
-        float yj = yv[0];
-#pragma unroll
-        for (int j = 1; j < 8; ++j)
-          if (lane == j) yj = yv[j];
-        const int pr = warp * 8 + lane;
+        for (int j = 0; j < 2; ++j) {
+          const float send = h3 ? yv[j] : yv[j + 2];
+          const float keep = h3 ? yv[j + 2] : yv[j];
+          yv[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+        {
+          const float send = h2 ? yv[0] : yv[1];
+          const float keep = h2 ? yv[1] : yv[0];
+          yv[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+        yv[0] += __shfl_xor_sync(0xffffffffu, yv[0], 2);
+        yv[0] += __shfl_xor_sync(0xffffffffu, yv[0], 1);
+      }
+      if ((lane & 3) == 0) {
+        const int j = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+        const int pr = warp * 8 + j;
         const float xp = xs[pr], zp = zs[pr];
-        const float yp = yj + Dh * xp;
-        orow[lane] = f32_to_bf16(yp * zp / (1.0f + expf(-zp)));
+        const float yp = yv[0] + Dh * xp;
+        orow[j] = f32_to_bf16(yp * zp / (1.0f + expf(-zp)));
       }
     }
-    fence_proxy_async_smem();  // this stage's reads come before its next copy
-    __syncthreads();
-    if (threadIdx.x == 0 && k + kSsmStages < my) issue(k + kSsmStages);
+    fence_proxy_async_smem();  // this stage's reads come before its refill
   }
   c.ssm_it += (uint32_t)my;
-  fence_proxy_async_smem();  // the next phase's copies overwrite the ring
+  __syncthreads();           // every thread is past the last item before the ring is reused
   if (wait_target > 0 && my > 0) {
     fence_proxy_async_global();  // the out-projection reads these rows by TMA
     __syncthreads();
