@@ -41,7 +41,18 @@ import synth  # noqa: E402
 METRIC = "session-frames/s"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "step_kernel_7b_traffic.txt")
 FALLBACK_HBM_GBS = 6800.0
-STEP_SRC = os.path.join(ROOT, "frame_step_decode_gb300", "csrc", "step.cu")
+# Every source the step kernel compiles from, in a fixed order: the committed
+# traffic figure holds only while their joint hash is the one it was taken on.
+STEP_SRCS = [os.path.join(ROOT, "frame_step_decode_gb300", "csrc", f)
+             for f in ("step.cu", "internal.h", "ptx.cuh", "fp8.cuh")]
+
+
+def step_sources_sha():
+    h = hashlib.sha256()
+    for path in STEP_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def algorithmic_bytes(w, pos) -> int:
@@ -114,9 +125,7 @@ def traffic_per_launch():
         if ":" in line:
             k, v = line.split(":", 1)
             vals[k.strip()] = v.strip()
-    with open(STEP_SRC, "rb") as f:
-        src_sha = hashlib.sha256(f.read()).hexdigest()[:16]
-    if vals.get("step_cu_sha256_16") != src_sha:
+    if vals.get("step_sources_sha256_16") != step_sources_sha():
         return None
     try:
         return int(float(vals["dram_bytes_per_full_launch"]))
