@@ -377,7 +377,7 @@ int encode_kv_maps(const Plan& pl, uint8_t* kv, float* scales, Maps* m) {
   }
   {
     cuuint64_t dims[3] = {n1, 2, L}, str[2] = {n1 * 4, 2 * n1 * 4};
-    cuuint32_t box[3] = {(cuuint32_t)kChunk, 2, 1};
+    cuuint32_t box[3] = {(cuuint32_t)(kChunk * kScaleGroup), 2, 1};  // a group of chunks, K and V planes
     if (!enc(&m->tm_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, scales, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
       return WAVE_ECUDA;
   }

@@ -75,6 +75,7 @@ __device__ __forceinline__ uint32_t bar_ssm(const Ctx& c, int i) {
   return c.sbase + c.lay.bar_off + 176 + 8 * kWarps * kAttStages + 8 * i;
 }
 static_assert(176 + 8 * kWarps * kAttStages + 8 * kSsmStages <= 64 * 8, "mbarrier slots exceed their region");
+static_assert(kAttStages <= kScaleGroup, "a scale buffer would be refilled before its last chunk is read");
 static_assert(kSsmStages * (kSsmP * kSsmN + 512) * 4 <= 200 * 1024, "state stages exceed the ring");
 __device__ __forceinline__ volatile int* misc_word(const Ctx& c, int i) {
   return (volatile int*)(c.smem + c.lay.misc_off + 4 * i);
@@ -844,12 +845,20 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
     auto issue = [&](int ci, int st) {
       const uint32_t base = wbuf_s + st * stage_bytes;
       const uint32_t fb = bar_att(c, warp, st);
-      // one box holds the chunk's K tile then its V tile; one more its scales
+      // one box holds the chunk's K tile then its V tile; the first chunk of
+      // each group of kScaleGroup in the piece also brings the group's K and
+      // V scales, into the warp's buffer (group & 1).  A buffer is refilled
+      // two groups later, when the issue is kAttStages <= kScaleGroup chunks
+      // ahead of a read that is already past the group it held.
       const int xrow = sh * p.T_max + ci * kChunk;
-      mbar_arrive_expect_tx(fb, 2u * kChunk * D + 2u * kChunk * 4u);
+      const int gk = ci - c_lo;
+      const bool grp = (gk % kScaleGroup) == 0;
+      mbar_arrive_expect_tx(fb, 2u * kChunk * D + (grp ? (uint32_t)kScaleBufBytes : 0u));
       tma_load_4d(base, &p.tm_kv, 0, xrow, 0, layer, fb, kv_policy);
-      const uint32_t sc_s = c.sbase + c.lay.ascale_off + (warp * kAttStages + st) * 256;
-      tma_load_3d(sc_s, &p.tm_sc, xrow, 0, layer, fb, kv_policy);
+      if (grp) {
+        const uint32_t sc_s = c.sbase + c.lay.ascale_off + (warp * 2 + (gk / kScaleGroup) % 2) * kScaleBufBytes;
+        tma_load_3d(sc_s, &p.tm_sc, xrow, 0, layer, fb, kv_policy);
+      }
     };
     if (lane == 0) {
       for (int k = 0; k < min(n, kAttStages); ++k) issue(c_lo + k, (c.att_it + k) % kAttStages);
@@ -963,8 +972,9 @@ __device__ void attention_phase(const StepParams& p, Ctx& c, int layer) {
       }
       uint8_t* kt = wbuf + st * stage_bytes;
       uint8_t* vt = kt + kChunk * D;
-      float* ksm = (float*)(c.smem + c.lay.ascale_off + (warp * kAttStages + st) * 256);
-      float* vsm = ksm + 32;
+      float* ksm = (float*)(c.smem + c.lay.ascale_off + (warp * 2 + (k / kScaleGroup) % 2) * kScaleBufBytes) +
+                   (k % kScaleGroup) * kChunk;
+      float* vsm = ksm + kScaleGroup * kChunk;
       const bool last = tail && (ci == nch - 1);
       const int valid = last ? (P - ci * kChunk + 1) : kChunk;
       if (last) {  // the current slot: use the codes just written
