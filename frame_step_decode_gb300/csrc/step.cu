@@ -1624,7 +1624,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
           if (!(ok = grid_sync(p, c))) break;
         }
         const bool nok = norm_phase(p, c, wl + p.off_g_attn, false, true, kDump ? nullptr : p.done_cnt + wk, wt);
-        if (!(ok = nok)) break;
+        ok = nok;
+        if (!ok) break;
         if constexpr (kDump) {
           if (!(ok = grid_sync(p, c))) break;
         } else {
@@ -1676,7 +1677,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
           if (!(ok = grid_sync(p, c) && sok)) break;
         } else {
           __syncthreads();
-          if (!(ok = sok)) break;
+          ok = sok;
+          if (!ok) break;
         }
         mark_phase(p, c);
         if (kDump) act_dump_rows(p, c.frame, l, kActMix, p.ssm_out, p.d_inner, p.d_inner);
@@ -1706,7 +1708,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         mark_phase(p, c);
         const bool nok2 = norm_phase(p, c, wl + p.off_g_mlp, false, true, kDump ? nullptr : p.done_cnt + kO,
                                      (l + 1) * p.tiles[kO]);
-        if (!(ok = nok2)) break;
+        ok = nok2;
+        if (!ok) break;
         if constexpr (kDump) {
           if (!(ok = grid_sync(p, c))) break;
           act_dump_rows(p, c.frame, l, kActXn2, p.xn, p.d, p.d);
