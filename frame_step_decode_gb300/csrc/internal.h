@@ -26,8 +26,8 @@ constexpr int kScaleBufBytes = 2 * kScaleGroup * kChunk * 4;  // [K|V][kScaleGro
 constexpr int kPieceChunks = WAVE_PIECE_CHUNKS;  // chunks per attention work piece
 // GEMM ring depth cap.  At S = 80 four stages fill the ring; smaller S fit
 // five to seven, but a fifth and sixth stage measured 0.4-2.5% slower per
-// step (S = 1 to 48): more weights issued ahead of a hand-over only delay
-// the previous phase's last copies.
+// step (S = 1 to 48), presumably because the weights issued ahead of a
+// hand-over then compete with the previous phase's last copies.
 constexpr int kMaxStages = 4;
 constexpr int kTmemCols = 256;    // two fp32 accumulators of up to 128 columns
 

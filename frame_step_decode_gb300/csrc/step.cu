@@ -312,14 +312,15 @@ __device__ __forceinline__ void seg_sumn(const float* first, const float* part, 
                                          const size_t* o, float4* a) {
 #pragma unroll
   for (int k = 0; k < NI; ++k) a[k] = __ldcg((const float4*)(first + o[k]));
-  if (kOne) return;
-  for (int j = 1; j < nseg; ++j) {
-    const float* bk = part + seg[j];
-    float4 tv[NI];
+  if constexpr (!kOne) {
+    for (int j = 1; j < nseg; ++j) {
+      const float* bk = part + seg[j];
+      float4 tv[NI];
 #pragma unroll
-    for (int k = 0; k < NI; ++k) tv[k] = __ldcg((const float4*)(bk + o[k]));
+      for (int k = 0; k < NI; ++k) tv[k] = __ldcg((const float4*)(bk + o[k]));
 #pragma unroll
-    for (int k = 0; k < NI; ++k) add4(a[k], tv[k]);
+      for (int k = 0; k < NI; ++k) add4(a[k], tv[k]);
+    }
   }
 }
 // The same for four offsets passed one by one.
@@ -328,11 +329,12 @@ __device__ __forceinline__ void seg_sum4(const float* first, const float* part, 
                                          int nseg, size_t o0, size_t o1, size_t o2, size_t o3,
                                          float4& a0, float4& a1, float4& a2, float4& a3) {
   a0 = ld4cg(first + o0); a1 = ld4cg(first + o1); a2 = ld4cg(first + o2); a3 = ld4cg(first + o3);
-  if (kOne) return;
-  for (int j = 1; j < nseg; ++j) {
-    const float* bk = part + seg[j];
-    const float4 t0 = ld4cg(bk + o0), t1 = ld4cg(bk + o1), t2 = ld4cg(bk + o2), t3 = ld4cg(bk + o3);
-    add4(a0, t0); add4(a1, t1); add4(a2, t2); add4(a3, t3);
+  if constexpr (!kOne) {
+    for (int j = 1; j < nseg; ++j) {
+      const float* bk = part + seg[j];
+      const float4 t0 = ld4cg(bk + o0), t1 = ld4cg(bk + o1), t2 = ld4cg(bk + o2), t3 = ld4cg(bk + o3);
+      add4(a0, t0); add4(a1, t1); add4(a2, t2); add4(a3, t3);
+    }
   }
 }
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
