@@ -172,6 +172,21 @@ def test_hybrid_prefix_batch_in_a_larger_handle_matches_oracle():
         assert _normwise(st_g[lm], st_o[lm]) <= 2e-2, lm
 
 
+def test_hybrid_maximum_batch():
+    # S = S_max = 128: the projections' MMA at N = 128, three ring stages,
+    # and 128 x 4 state items per block; every phase of sessions 0..3, and y
+    # of sessions spread over the batch (the last one included)
+    w = synth.HYBRID_SMALL
+    case = HybridCase(w, S=128, S_max=128)
+    _check_phases(case, 4)
+    case = HybridCase(w, S=128, S_max=128)
+    _run(case, range(128))
+    W = synth.hybrid_weights_host(w)
+    sess = [0, 1, 64, 126, 127]
+    _y_within_oracle_sensitivity(w, W, sess, case.pos_h[sess], np.ascontiguousarray(case.x_h[sess]),
+                                 case.y_bits()[sess])
+
+
 @pytest.mark.parametrize("which", [6, 7, 8, 0])
 def test_hybrid_timeout_at_each_hand_over(which):
     # one item never published: a selective-state in-projection tile (the

@@ -143,6 +143,18 @@ def test_ragged_batch_sizes(S):
         wave.close()
 
 
+@pytest.mark.parametrize("w", [synth.TINY, synth.MID], ids=["tiny", "mid"])
+def test_maximum_batch(w):
+    # S = S_max = 128, the largest batch the library takes: the projections'
+    # MMA runs at N = 128 and their ring holds three stages instead of four
+    case = DeviceCase(w, S=128, S_max=128)
+    wave = fsd.Wave(case.cfg, 128, w.T_max)
+    try:
+        _check_case(case, wave)
+    finally:
+        wave.close()
+
+
 def test_edge_positions():
     w = synth.MID
     # 32-token chunk boundaries and the extremes (T_max = 320 is below one
