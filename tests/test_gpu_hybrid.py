@@ -157,6 +157,18 @@ def test_hybrid_empty_slot_leaves_its_state_and_passes_x():
                                  case.y_bits()[keep])
 
 
+def test_hybrid_all_slots_empty():
+    # no session at all: y = x, no state, history byte or scale written
+    w = synth.HYBRID_SMALL
+    pos = np.full(w.S, -1, dtype=np.int32)
+    case = HybridCase(w, pos=pos)
+    kv0, sc0, st0, _ = _run(case, range(w.S))
+    assert np.array_equal(case.y_bits(), case.x_h)
+    assert torch.equal(case.state.view(torch.int32), st0.view(torch.int32))
+    assert torch.equal(case.kv, kv0)
+    assert torch.equal(case.sc.view(torch.int32), sc0.view(torch.int32))
+
+
 def test_hybrid_prefix_batch_in_a_larger_handle_matches_oracle():
     # S < S_max: the state and history are indexed by S_max-strided sessions
     w = synth.HYBRID_SMALL

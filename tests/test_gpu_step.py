@@ -244,6 +244,25 @@ def test_empty_slots_pass_x_through_and_touch_no_cache():
         wave.close()
 
 
+def test_all_slots_empty():
+    # a batch with no session at all: no attention work, y = x everywhere,
+    # not one history byte or scale written
+    w = synth.MID
+    pos = np.full(w.S, -1, dtype=np.int32)
+    case = DeviceCase(w, pos=pos)
+    wave = fsd.Wave(case.cfg, case.S_max, w.T_max)
+    try:
+        kv0, sc0 = case.kv.clone(), case.sc.clone()
+        for _ in range(2):
+            case.step(wave)
+            assert wave.status() == fsd.WAVE_OK
+            assert np.array_equal(case.y_bits(), case.x_h)
+            assert torch.equal(case.kv, kv0)
+            assert torch.equal(case.sc.view(torch.int32), sc0.view(torch.int32))
+    finally:
+        wave.close()
+
+
 @pytest.mark.parametrize("w", [synth.TINY, synth.MID])
 def test_two_frame_beat_equals_two_steps_and_rolls_positions(w):
     # one launch of two frames against two single-frame launches with the
