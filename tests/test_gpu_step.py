@@ -244,6 +244,19 @@ def test_empty_slots_pass_x_through_and_touch_no_cache():
         wave.close()
 
 
+def test_shortest_history_capacity():
+    # T_max = 4, the smallest the library takes: every chunk and scale copy
+    # reaches past the end of a session's history (and of the whole cache)
+    from dataclasses import replace
+    w = replace(synth.TINY, T_max=4, pos_lo=0, pos_hi=4, name="tiny-2L-d256-h4x64-f688-T4")
+    case = DeviceCase(w, S=8, pos=np.array([0, 1, 2, 3, 3, 2, 1, 0], dtype=np.int32))
+    wave = fsd.Wave(case.cfg, case.S_max, w.T_max)
+    try:
+        _check_case(case, wave)
+    finally:
+        wave.close()
+
+
 def test_all_slots_empty():
     # a batch with no session at all: no attention work, y = x everywhere,
     # not one history byte or scale written
