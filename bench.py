@@ -10,7 +10,7 @@ latency and the HBM roofline fraction of the step kernel.
   python bench.py --sweep 1,8,16,32,48,56,64,80,96,128 --steps 20
   python bench.py --beat 2
   python bench.py --depth [--phases]
-  python bench.py --hybrid [--phases]
+  python bench.py --hybrid [--phases] [--layers 6k]
   python bench.py --phases [--layers L]      (per-phase times of one step)
 
 Inputs are seeded and synthetic and are drawn on the device (weights and the
@@ -693,6 +693,11 @@ def run_hybrid(args):
     import torch
     import frame_step_decode_gb300 as fsd
     w = synth.HYBRID
+    if args.layers:  # a shorter copy (whole groups of attn_every layers) for profiling a small case
+        if args.layers % w.attn_every:
+            raise SystemExit(f"--layers with --hybrid must be a multiple of {w.attn_every}")
+        from dataclasses import replace
+        w = replace(w, n_layers=args.layers, name=f"{w.name}-L{args.layers}")
     S = w.S
     aw = w.attention_view()
     device = torch.device("cuda", 0)
