@@ -117,7 +117,8 @@ struct StepParams {
 };
 
 // CTAs taking part in a stream-K GEMM phase of `tiles` tiles and U units:
-// every participating span is non-empty and a tile has at most 64 segments.
+// every participating span is non-empty, and at least U / (seg_cap * tiles)
+// units long, so that a tile has at most seg_cap + 1 segments.
 // Counter words of the workspace (zeroed at each frame's start): two banks of
 // two words per GEMM tile (1024 tiles at most; consecutive projections with
 // no grid barrier between them use different banks), the gate/up tiles'

@@ -477,9 +477,10 @@ __device__ void gemm_phase(const StepParams& p, Ctx& c, int kind, int layer, boo
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KB = p.kblocks[kind];
   const long long U = (long long)p.tiles[kind] * KB;
-  // Split over min(grid, units, 62 * tiles) CTAs: every participating span is
-  // non-empty, the owners of a tile's units are consecutive CTAs, and a tile
-  // has at most 64 segments.
+  // Split over min(grid, units, seg_cap * tiles) CTAs: every participating
+  // span is non-empty, the owners of a tile's units are consecutive CTAs, and
+  // a tile has at most seg_cap + 1 segments (the plan checks 64, the size of
+  // the reduction's segment table).
   const int G = stream_k_ctas(gridDim.x, U, p.tiles[kind], gemm_seg_cap(kind)), cta = blockIdx.x;
   const Span sp = (cta < G) ? cta_span(U, G, cta) : Span{0, 0};
   const int S_pad = p.S_pad, nst = p.nstage;
