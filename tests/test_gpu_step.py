@@ -257,6 +257,28 @@ def test_shortest_history_capacity():
         wave.close()
 
 
+def test_output_may_alias_input():
+    # y written over x (the header allows it): the same bits as with a
+    # separate y, empty slots included
+    w = synth.MID
+    pos = synth.positions(w, w.S).copy()
+    pos[[3, 11]] = -1
+    ref = DeviceCase(w, pos=pos)
+    inplace = DeviceCase(w, pos=pos)
+    wave = fsd.Wave(ref.cfg, ref.S_max, w.T_max)
+    try:
+        ref.step(wave)
+        assert wave.status() == fsd.WAVE_OK
+        wave.step(inplace.S, inplace.weights, inplace.kv, inplace.sc, inplace.pos, inplace.x, inplace.x)
+        assert wave.status() == fsd.WAVE_OK
+        got = inplace.x.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, ref.y_bits())
+        assert torch.equal(inplace.kv, ref.kv)
+        assert torch.equal(inplace.sc.view(torch.int32), ref.sc.view(torch.int32))
+    finally:
+        wave.close()
+
+
 def test_all_slots_empty():
     # a batch with no session at all: no attention work, y = x everywhere,
     # not one history byte or scale written
