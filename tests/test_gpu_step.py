@@ -211,6 +211,19 @@ def test_invalid_arguments_are_rejected(tiny):
     rc = wave.step(case.S, case.weights.data_ptr() + 2, case.kv, case.sc, case.pos, case.x, case.y,
                    check=False)
     assert rc == fsd.WAVE_EINVAL
+    # every buffer off its required alignment (16 bytes; 4 for the positions)
+    args = [case.weights.data_ptr(), case.kv.data_ptr(), case.sc.data_ptr(), case.pos.data_ptr(),
+            case.x.data_ptr(), case.y.data_ptr()]
+    for i, off in ((1, 1), (2, 4), (3, 2), (4, 2), (5, 8)):
+        bad_args = list(args)
+        bad_args[i] += off
+        assert wave.step(case.S, *bad_args, check=False) == fsd.WAVE_EINVAL, i
+    for i in range(6):  # and null
+        bad_args = list(args)
+        bad_args[i] = 0
+        assert wave.step(case.S, *bad_args, check=False) == fsd.WAVE_EINVAL, i
+    torch.cuda.synchronize()
+    assert wave.status() == fsd.WAVE_OK  # nothing was launched
     bad = fsd.WaveConfig(2, 256, 4, 96, 688, 1e-5, 1e4)
     with pytest.raises(fsd.WaveError):
         fsd.Wave(bad, 4, 64)
