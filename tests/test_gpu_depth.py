@@ -134,3 +134,35 @@ def test_every_phase_of_every_step_matches_oracle(run):
                                             run["y"][k, s], worst)
     print({k: round(v, 3) for k, v in worst.items()})
     assert all(v <= 1.0 for v in worst.values()), worst
+
+
+def test_depth_loop_with_x0_inside_xs():
+    # xs may start at x0 (no copy of x0 then): the same bits as with x0 apart
+    w = W
+    S, d = 24, w.d_model
+    L, H, T, D = w.n_layers, w.n_heads, w.T_max, w.head_dim
+    dev = "cuda"
+    weights = fsd.pack_weights(fsd.WaveConfig.of(w),
+                               torch.from_numpy(synth.weights_host(w).view(np.int16)).to(dev).view(torch.bfloat16))
+    wp = torch.from_numpy(synth.proj_host(w).view(np.int16)).to(dev).view(torch.bfloat16)
+    x0 = torch.from_numpy(synth.x_bf16(w, S).view(np.int16)).to(dev).view(torch.bfloat16)
+    outs = []
+    wave = fsd.Wave(fsd.WaveConfig.of(w), S, T)
+    try:
+        for inside in (False, True):
+            kv = torch.full((L, 2, S, H, T, D), 0x7F, dtype=torch.uint8, device=dev)
+            sc = torch.full((L, 2, S, H, T), float("nan"), dtype=torch.float32, device=dev)
+            xs = torch.zeros((STEPS, S, d), dtype=torch.bfloat16, device=dev)
+            y = torch.zeros((STEPS, S, d), dtype=torch.bfloat16, device=dev)
+            if inside:
+                xs[0].copy_(x0)
+                wave.depth(S, STEPS, weights, wp, kv, sc, xs[0], xs, y)
+            else:
+                wave.depth(S, STEPS, weights, wp, kv, sc, x0, xs, y)
+            assert wave.status() == fsd.WAVE_OK
+            outs.append((y, xs))
+    finally:
+        wave.close()
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
+

@@ -169,6 +169,29 @@ def test_hybrid_all_slots_empty():
     assert torch.equal(case.sc.view(torch.int32), sc0.view(torch.int32))
 
 
+def test_handle_kinds_are_not_interchangeable():
+    # the decoder calls refuse a hybrid handle and the hybrid step a decoder
+    # handle, before any launch
+    w = synth.HYBRID_SMALL
+    case = HybridCase(w)
+    hw = fsd.HybridWave(case.cfg, case.S_max, w.T_max)
+    dw = fsd.Wave(fsd.WaveConfig(2, 256, 4, 64, 688, 1e-5, 1e4), case.S_max, w.T_max)
+    try:
+        lib = fsd.lib()
+        p = [case.weights.data_ptr(), case.kv.data_ptr(), case.sc.data_ptr(), case.pos.data_ptr(),
+             case.x.data_ptr(), case.y.data_ptr()]
+        assert lib.wave_step(hw.h, case.S, *p, None) == fsd.WAVE_EINVAL
+        assert lib.wave_beat(hw.h, case.S, 2, p[0], p[1], p[2], p[3], 0, p[4], p[5], None) == fsd.WAVE_EINVAL
+        assert lib.wave_depth(hw.h, case.S, 2, p[0], p[0], p[1], p[2], p[4], p[4], p[5], None) == fsd.WAVE_EINVAL
+        assert lib.wave_hybrid_step(dw.h, case.S, p[0], p[1], p[2], case.state.data_ptr(), p[3], p[4], p[5],
+                                    None) == fsd.WAVE_EINVAL
+        torch.cuda.synchronize()
+        assert hw.status() == fsd.WAVE_OK and dw.status() == fsd.WAVE_OK
+    finally:
+        hw.close()
+        dw.close()
+
+
 def test_hybrid_prefix_batch_in_a_larger_handle_matches_oracle():
     # S < S_max: the state and history are indexed by S_max-strided sessions
     w = synth.HYBRID_SMALL
