@@ -222,6 +222,12 @@ def test_invalid_arguments_are_rejected(tiny):
         bad_args = list(args)
         bad_args[i] = 0
         assert wave.step(case.S, *bad_args, check=False) == fsd.WAVE_EINVAL, i
+    lib = fsd.lib()
+    for frames in (0, -1, 65):  # a beat of 1..64 frames
+        assert lib.wave_beat(wave.h, case.S, frames, *args[:4], 0, args[4], args[5], None) == fsd.WAVE_EINVAL
+    for steps in (0, case.w.T_max + 1, 65):  # a depth loop of 1..min(64, T_max) steps
+        assert lib.wave_depth(wave.h, case.S, steps, args[0], args[0], args[1], args[2], args[4], args[4],
+                              args[5], None) == fsd.WAVE_EINVAL
     torch.cuda.synchronize()
     assert wave.status() == fsd.WAVE_OK  # nothing was launched
     bad = fsd.WaveConfig(2, 256, 4, 96, 688, 1e-5, 1e4)
